@@ -1,0 +1,66 @@
+"""Seeded synthetic inputs, shared by the CUDA path's tests/bench and the oracle.
+
+This module holds no attention arithmetic: it only draws numbers.  Every
+tensor is i.i.d. N(0, 1) (the unit-variance query/key assumption of
+"Механизм внимания", section "Почему делить на корень из d_h"), drawn in
+float32 from one ``torch.Generator('cpu')`` seeded per workload and rounded
+to bfloat16, in the fixed order Q, K, V, then (for a decode step) the
+per-sequence cache lengths.  The same host tensors feed both sides.
+"""
+from __future__ import annotations
+
+import torch
+
+# The workloads, named by what they are.  ``seed`` fixes every number drawn.
+WORKLOADS = {
+    # causal MHA core attention, the smallest case (every row checked)
+    "prefill_mha_b1_h2_s128_d64": dict(kind="prefill", B=1, Hq=2, Hkv=2, S=128, Dh=64,
+                                       causal=True, window=0, seed=0),
+    # causal MHA prefill, hidden 4096 = 32 heads x 128
+    "prefill_mha_b2_h32_s1024_d128": dict(kind="prefill", B=2, Hq=32, Hkv=32, S=1024, Dh=128,
+                                          causal=True, window=0, seed=1),
+    # causal MHA prefill at 4096 tokens, and its non-causal counterpart
+    "prefill_mha_b1_h32_s4096_d128": dict(kind="prefill", B=1, Hq=32, Hkv=32, S=4096, Dh=128,
+                                          causal=True, window=0, seed=2),
+    "prefill_mha_b1_h32_s4096_d128_noncausal": dict(kind="prefill", B=1, Hq=32, Hkv=32, S=4096,
+                                                    Dh=128, causal=False, window=0, seed=2),
+    # causal GQA prefill (32 query heads over 8 K/V heads) with a 4096-key sliding window
+    "prefill_gqa_b1_h32kv8_s32768_d128_w4096": dict(kind="prefill", B=1, Hq=32, Hkv=8, S=32768,
+                                                    Dh=128, causal=True, window=4096, seed=3),
+    # one decode step for 16 sequences against caches of 16384..32768 keys
+    "decode_gqa_b16_h32kv8_t32768_d128": dict(kind="decode", B=16, Hq=32, Hkv=8, Tmax=32768,
+                                              Dh=128, lmin=16384, lmax=32768, window=0, seed=4),
+}
+
+
+def _randn_bf16(shape, gen):
+    return torch.randn(shape, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+
+
+def prefill_inputs(B, Hq, Hkv, S, Dh, seed):
+    """q [B,Hq,S,Dh], k and v [B,Hkv,S,Dh], bf16 on the host."""
+    gen = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = _randn_bf16((B, Hq, S, Dh), gen)
+    k = _randn_bf16((B, Hkv, S, Dh), gen)
+    v = _randn_bf16((B, Hkv, S, Dh), gen)
+    return q, k, v
+
+
+def decode_inputs(B, Hq, Hkv, Tmax, Dh, lmin, lmax, seed):
+    """q [B,Hq,1,Dh], kcache and vcache [B,Hkv,Tmax,Dh] (bf16), and the
+    per-sequence key counts seqlens [B] (int32, uniform in [lmin, lmax])."""
+    gen = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = _randn_bf16((B, Hq, 1, Dh), gen)
+    kc = _randn_bf16((B, Hkv, Tmax, Dh), gen)
+    vc = _randn_bf16((B, Hkv, Tmax, Dh), gen)
+    seqlens = torch.randint(int(lmin), int(lmax) + 1, (B,), generator=gen, dtype=torch.int64)
+    return q, kc, vc, seqlens.to(torch.int32)
+
+
+def workload_inputs(name):
+    """The inputs of a named workload (see WORKLOADS)."""
+    w = WORKLOADS[name]
+    if w["kind"] == "prefill":
+        return prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["S"], w["Dh"], w["seed"])
+    return decode_inputs(w["B"], w["Hq"], w["Hkv"], w["Tmax"], w["Dh"], w["lmin"], w["lmax"],
+                         w["seed"])
