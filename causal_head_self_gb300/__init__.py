@@ -1,1 +1,11 @@
-"""GB300-native scaled dot-product causal multi-head self-attention."""
+"""GB300-native (sm_103a) scaled dot-product causal multi-head self-attention.
+
+The compute path is the CUDA library ``libattn_sm103a.so`` (C ABI in
+``include/attn.h``); this package is its thin Python binding.  ``attn_fwd``
+runs the tcgen05/TMA prefill kernel, ``attn_decode`` the split-KV decode and
+log-sum-exp combine kernels.  There is no CPU or PyTorch fallback: without the
+built library every call raises.
+"""
+from ._binding import (ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_NO_MEMORY,  # noqa: F401
+                       ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED, ATTN_OK, AttnError, attn_decode,
+                       attn_fwd, attn_status, error_string, version)

@@ -1,0 +1,136 @@
+"""ctypes binding of libattn_sm103a.so (include/attn.h), same names as the
+C ABI.  Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  torch is used for device memory and streams.
+
+If the library has not been built the first call raises: there is no other
+implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn_sm103a.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_NO_MEMORY = 5
+
+# every symbol include/attn.h declares
+ABI_SYMBOLS = ("attn_fwd", "attn_decode", "attn_status", "attn_error_string", "attn_version")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {error_string(code)} ({code})")
+
+
+def load():
+    """Load (once) and return the ctypes handle of the built library."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            lib.attn_fwd.restype = i
+            lib.attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+            lib.attn_decode.restype = i
+            lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+            lib.attn_status.restype = i
+            lib.attn_status.argtypes = [vp]
+            lib.attn_error_string.restype = ctypes.c_char_p
+            lib.attn_error_string.argtypes = [i]
+            lib.attn_version.restype = i
+            lib.attn_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def error_string(code: int) -> str:
+    return load().attn_error_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(load().attn_version())
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check_bf16(name, t, ndim):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def attn_fwd(q, k, v, o=None, *, causal=True, window=0, scale=0.0, stream=None):
+    """O = softmax(Q K^T * scale + M) V.  q [B,Hq,S,Dh], k/v [B,Hkv,S,Dh] bf16.
+    scale 0 means 1/sqrt(Dh).  Returns o (allocated if not given)."""
+    _check_bf16("q", q, 4)
+    _check_bf16("k", k, 4)
+    _check_bf16("v", v, 4)
+    B, Hq, S, Dh = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, S, Dh) or tuple(v.shape) != (B, Hkv, S, Dh):
+        raise ValueError("k and v must be [B, Hkv, S, Dh] matching q")
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _check_bf16("o", o, 4)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    rc = load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, S,
+                         Dh, int(bool(causal)), int(window), float(scale), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return o
+
+
+def attn_decode(q, kcache, vcache, seqlens, o=None, *, window=0, scale=0.0, stream=None):
+    """One decode step.  q [B,Hq,1,Dh]; caches [B,Hkv,Tmax,Dh] bf16; seqlens
+    [B] int32 on the device (keys held per sequence, own key included)."""
+    _check_bf16("q", q, 4)
+    _check_bf16("kcache", kcache, 4)
+    _check_bf16("vcache", vcache, 4)
+    B, Hq, one, Dh = q.shape
+    Hkv, Tmax = kcache.shape[1], kcache.shape[2]
+    if one != 1 or tuple(kcache.shape) != (B, Hkv, Tmax, Dh) or vcache.shape != kcache.shape:
+        raise ValueError("q must be [B,Hq,1,Dh] and the caches [B,Hkv,Tmax,Dh]")
+    if (not isinstance(seqlens, torch.Tensor) or seqlens.dtype != torch.int32 or not seqlens.is_cuda
+            or seqlens.numel() != B or not seqlens.is_contiguous()):
+        raise TypeError("seqlens must be a contiguous CUDA int32 tensor of B entries")
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _check_bf16("o", o, 4)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    rc = load().attn_decode(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), seqlens.data_ptr(),
+                            o.data_ptr(), B, Hq, Hkv, Tmax, Dh, int(window), float(scale),
+                            _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode")
+    return o
+
+
+def attn_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device's latched error code."""
+    return int(load().attn_status(_stream_handle(stream)))

@@ -1,0 +1,208 @@
+// attn_api.cu -- the C ABI declared in include/attn.h: argument checks,
+// per-device state (SM count, latched error word, decode workspace), tensor
+// maps, and the kernel launches.  No torch types cross this boundary.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+#include "launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Latched device-side status of the kernels (one per device: every device
+// that loads this library holds its own copy of the symbol).
+__device__ int g_attn_error_word;
+
+struct DeviceState {
+  bool ready = false;
+  chs::DeviceInfo info{};
+  void* workspace = nullptr;
+  size_t workspace_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool load_encode_fn() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult qres;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &qres) != cudaSuccess ||
+      qres != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// Per-device set-up on first use, with that device current.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    void* word = nullptr;
+    if (cudaGetSymbolAddress(&word, g_attn_error_word) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (!load_encode_fn()) return ATTN_ERR_CUDA;
+    st.info.device = dev;
+    st.info.num_sms = sms;
+    st.info.error_word = static_cast<int*>(word);
+    st.ready = true;
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// scale == 0 -> 1/sqrt(Dh); returns false for a negative or non-finite scale
+bool resolve_scale(float scale, int Dh, float* scale_log2) {
+  if (!std::isfinite(scale) || scale < 0.f) return false;
+  const double s = scale == 0.f ? 1.0 / std::sqrt((double)Dh) : (double)scale;
+  *scale_log2 = (float)(s * 1.4426950408889634);   // log2(e)
+  return true;
+}
+
+}  // namespace
+
+namespace chs {
+
+bool encode_bf16_map(CUtensorMap* map, const void* base, int Dh, int rows, long long outer,
+                     int box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)Dh, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)Dh * 2, (cuuint64_t)Dh * 2 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace chs
+
+extern "C" {
+
+int attn_version(void) { return (1 << 16) | 0; }
+
+const char* attn_error_string(int code) {
+  switch (code) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    case ATTN_ERR_NO_MEMORY: return "ATTN_ERR_NO_MEMORY";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int S,
+             int Dh, int causal, int window, float scale, cudaStream_t stream) {
+  if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (window < 0) window = 0;
+  if (window > 0 && !causal) return ATTN_ERR_INVALID_ARG;
+  float scale_log2 = 0.f;
+  if (!resolve_scale(scale, Dh, &scale_log2)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return ATTN_OK;
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  const size_t qo_bytes = (size_t)B * Hq * S * Dh * 2, kv_bytes = (size_t)B * Hkv * S * Dh * 2;
+  if ((long long)B * Hq * ((S + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, k, kv_bytes) ||
+      overlaps(o, qo_bytes, v, kv_bytes))
+    return ATTN_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != ATTN_OK) return rc;
+  cudaError_t e = chs::launch_prefill(q, k, v, o, B, Hq, Hkv, S, Dh, causal, window, scale_log2,
+                                      st->info, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens, void* o,
+                int B, int Hq, int Hkv, int Tmax, int Dh, int window, float scale,
+                cudaStream_t stream) {
+  if (B < 0 || Tmax < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
+  if (window < 0) window = 0;
+  float scale_log2 = 0.f;
+  if (!resolve_scale(scale, Dh, &scale_log2)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0) return ATTN_OK;
+  if (!q || !kcache || !vcache || !seqlens || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t qo_bytes = (size_t)B * Hq * Dh * 2;
+  const size_t kv_bytes = (size_t)B * Hkv * Tmax * Dh * 2;
+  if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, kcache, kv_bytes) ||
+      overlaps(o, qo_bytes, vcache, kv_bytes) || overlaps(o, qo_bytes, seqlens, (size_t)B * 4))
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * Hkv * (Hq / Hkv) > 65535LL * 65535LL) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535) return ATTN_ERR_INVALID_ARG;   // grid.z
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != ATTN_OK) return rc;
+  const chs::DecodePlan plan = chs::plan_decode(B, Hq, Hkv, Tmax, Dh, st->info.num_sms);
+  if ((long long)Hkv * ((Hq / Hkv) / plan.heads_per_cta) > 65535) return ATTN_ERR_INVALID_ARG;
+  const size_t need = chs::decode_workspace_bytes(B, Hq, Dh, plan);
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (st->workspace_bytes < need) {
+      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess ||
+          cap != cudaStreamCaptureStatusNone)
+        return ATTN_ERR_NO_MEMORY;   // cannot grow the workspace inside a capture
+      if (st->workspace) cudaFree(st->workspace);
+      st->workspace = nullptr;
+      st->workspace_bytes = 0;
+      if (cudaMalloc(&st->workspace, need) != cudaSuccess) {
+        st->workspace = nullptr;
+        cudaGetLastError();
+        return ATTN_ERR_NO_MEMORY;
+      }
+      st->workspace_bytes = need;
+    }
+    ws = st->workspace;
+  }
+  cudaError_t e = chs::launch_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, window,
+                                     scale_log2, plan, ws, st->info, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_status(cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != ATTN_OK) return rc;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyAsync(&word, st->info.error_word, sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaMemsetAsync(st->info.error_word, 0, sizeof(int), stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return word;
+}
+
+}  // extern "C"

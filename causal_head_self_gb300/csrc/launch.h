@@ -1,0 +1,42 @@
+// launch.h -- internal interface between the C-ABI layer and the kernel
+// translation units.  Not part of the public ABI (see include/attn.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace chs {
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int* error_word;   // device address of this device's latched error word
+};
+
+// Encode a 3-D tensor map over a contiguous [outer, rows, Dh] bf16 tensor:
+// dims {Dh, rows, outer}, 128-byte swizzle, box {64, box_rows, 1}.
+bool encode_bf16_map(CUtensorMap* map, const void* base, int Dh, int rows, long long outer,
+                     int box_rows);
+
+cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                           int Hkv, int S, int Dh, int causal, int window, float scale_log2,
+                           const DeviceInfo& dev, cudaStream_t stream);
+
+struct DecodePlan {
+  int chunk;          // keys per split
+  int nsplit;         // splits per (b, query head)
+  int heads_per_cta;  // query heads of a GQA group handled by one CTA
+};
+
+DecodePlan plan_decode(int B, int Hq, int Hkv, int Tmax, int Dh, int num_sms);
+
+// Bytes of split partials a decode call with this plan needs.
+size_t decode_workspace_bytes(int B, int Hq, int Dh, const DecodePlan& plan);
+
+cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int* seqlens,
+                          void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,
+                          float scale_log2, const DecodePlan& plan, void* workspace,
+                          const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace chs

@@ -1,0 +1,117 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) scaled dot-product causal
+ * multi-head self-attention library (libattn_sm103a.so).
+ *
+ * The operation is the one defined in "Механизм внимания"
+ * (llm-arch-research.openidealab.com/textbook/attention), section
+ * "Scaled dot-product attention":
+ *
+ *     O = softmax(Q K^T * scale + M) V        per (batch b, query head h)
+ *
+ * with M in {0, -inf} the mask of sections "Маскирование" (causal: key j is
+ * visible to query i only if j <= i) and "Скользящее окно" (sliding window),
+ * and query head h reading K/V head g(h) = floor(h / (Hq / Hkv)) as in
+ * section "Виды по числу голов K/V: MHA, GQA, MQA" (Hkv == Hq is MHA,
+ * Hkv == 1 is MQA).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are bf16, contiguous, row-major, in the layout [B, H, S, Dh]
+ *     ("多头注意力机制" (blog.euler0525.cn), section "Multi-head Attention":
+ *     heads moved ahead of the sequence axis).  All tensor pointers are
+ *     DEVICE pointers, 16-byte aligned.  The caller owns every tensor.
+ *   - Dh must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise).
+ *   - Hq % Hkv == 0 is required (ATTN_ERR_INVALID_ARG otherwise).
+ *   - scale == 0 selects 1/sqrt(Dh), the textbook's choice (divide by the
+ *     square root of the HEAD size, not the model width); a positive scale is
+ *     used as given; a negative or non-finite scale is ATTN_ERR_INVALID_ARG.
+ *   - window <= 0 means no window.  window = W > 0 keeps key j visible to the
+ *     query at position i only if i - W < j <= i: W keys including the
+ *     query's own (the i - j < W form the textbook quotes from HuggingFace;
+ *     the page's own rule 0 <= i - j <= W equals window W + 1 here).
+ *   - Argument errors are returned before anything is launched.  Kernels run
+ *     asynchronously on `stream`; a launch failure returns ATTN_ERR_CUDA.
+ *     Errors found on the device (a bounded wait that gave up, an invalid
+ *     sequence length) are latched in a per-device error word that
+ *     attn_status() reads.  After a non-OK status the output is undefined.
+ *   - The same inputs give bit-identical outputs (no atomics in any
+ *     reduction; the decode split plan depends only on the arguments and
+ *     the device's SM count).
+ */
+#ifndef CAUSAL_HEAD_SELF_ATTN_H_
+#define CAUSAL_HEAD_SELF_ATTN_H_
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* bad shape, pointer, alignment, aliasing, scale or window */
+  ATTN_ERR_UNSUPPORTED = 2,  /* a head size other than 64 or 128 */
+  ATTN_ERR_CUDA = 3,         /* a CUDA runtime or launch error */
+  ATTN_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (reported by attn_status) */
+  ATTN_ERR_NO_MEMORY = 5     /* the decode workspace could not be allocated */
+} attn_status_t;
+
+/*
+ * attn_fwd -- prefill / full-sequence attention.
+ *   q  [B, Hq,  S, Dh]   queries          (device, bf16, read)
+ *   k  [B, Hkv, S, Dh]   keys             (device, bf16, read)
+ *   v  [B, Hkv, S, Dh]   values           (device, bf16, read)
+ *   o  [B, Hq,  S, Dh]   output           (device, bf16, written; must not
+ *                                           overlap q, k or v)
+ *   causal   1: causal mask; 0: every key visible (window must then be <= 0)
+ *   window, scale: see the conventions above.
+ * B == 0 or S == 0 is a no-op returning ATTN_OK.
+ * Work: 4*Dh FLOPs per visible (query, key) pair per query head; masked tiles
+ * of 128x128 are never computed.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+             int S, int Dh, int causal, int window, float scale, cudaStream_t stream);
+
+/*
+ * attn_decode -- one KV-cache decode step ("Механизм внимания", section
+ * "Prefill и decode": the new token's key and value are appended to the
+ * cache first, then its query meets every cached key, its own included).
+ *   q        [B, Hq, 1, Dh]     the new tokens' queries   (device, bf16, read)
+ *   kcache   [B, Hkv, Tmax, Dh] cached keys               (device, bf16, read)
+ *   vcache   [B, Hkv, Tmax, Dh] cached values             (device, bf16, read)
+ *   seqlens  [B]                keys held per sequence, 1 <= seqlens[b] <= Tmax
+ *                               (device, int32, read).  Only rows
+ *                               [0, seqlens[b]) of a cache are read.
+ *   o        [B, Hq, 1, Dh]     output (device, bf16, written)
+ * The query of sequence b sits at position seqlens[b] - 1 and sees keys
+ * [max(0, seqlens[b] - window), seqlens[b]) (all of them when window <= 0).
+ * A seqlens entry outside [1, Tmax] zeroes that sequence's output and latches
+ * ATTN_ERR_INVALID_ARG for attn_status().
+ * The split-KV partials live in a library-owned device workspace, allocated
+ * on first use per device and grown on demand (cudaMalloc): make the first
+ * call with the largest shape outside any CUDA graph capture.  Calls on one
+ * device share that workspace, so decode calls that overlap on the GPU
+ * (different streams, no ordering) race.
+ * B == 0 is a no-op returning ATTN_OK.
+ */
+int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window, float scale,
+                cudaStream_t stream);
+
+/*
+ * attn_status -- synchronise `stream`, then return (and clear) the current
+ * device's latched error word: ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_INVALID_ARG,
+ * or ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+int attn_status(cudaStream_t stream);
+
+/* attn_error_string -- a static, human-readable name for a status code. */
+const char* attn_error_string(int code);
+
+/* attn_version -- library ABI version, (major << 16) | minor. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAUSAL_HEAD_SELF_ATTN_H_ */
