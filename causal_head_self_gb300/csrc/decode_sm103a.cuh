@@ -219,6 +219,19 @@ __global__ void __launch_bounds__(kDecodeThreads)
       if (++st == kDecodeStages) { st = 0; ph ^= 1; }
     }
 
+    // bring every slot to the chunk order of key slot 0 (lane == part), whose
+    // lanes write the merged result below
+    const int flip0 = (part >> 2) & 1;
+    if (flip != flip0) {
+#pragma unroll
+      for (int h = 0; h < HPB; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float t = acc[h][e];
+          acc[h][e] = acc[h][8 + e];
+          acc[h][8 + e] = t;
+        }
+    }
     // merge the key slots of this warp (lanes with equal `part`)
 #pragma unroll
     for (int h = 0; h < HPB; ++h) {
