@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  1. attn_fwd    causal MHA prefill, B=2, 32 heads, S=1024, Dh=128 (the
+                 headline workload: hidden 4096 = 32 x 128);
+  2. attn_decode one KV-cache decode step, B=16, 32 query / 8 K/V heads,
+                 Dh=128, cache lengths uniform in [16384, 32768].
+`value` is the prefill throughput in TFLOP/s (4*Dh FLOPs per unmasked
+(query, key) pair per query head, masked pairs not counted), whole job over
+all ranks.  The decode leg is reported beside it in KV-cache GB/s (every
+valid K/V byte counted once, plus q and o) and tokens/s.  L2 is flushed (a
+256 MiB write) before every step, outside the timed kernels.
+
+--impl reference times the float64 CPU oracle (the reference this build is
+checked against) on a bounded sample of the same workloads.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from causal_head_self_gb300 import inputs  # noqa: E402
+
+METRIC = "causal attn fwd TFLOP/s & % BF16 peak; decode KV-cache GB/s & % HBM peak"
+PREFILL = "prefill_mha_b2_h32_s1024_d128"
+DECODE = "decode_gqa_b16_h32kv8_t32768_d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def visible_pairs(S, causal, window):
+    """Unmasked (query, key) pairs of one head."""
+    if not causal:
+        return S * S
+    if window <= 0 or window >= S:
+        return S * (S + 1) // 2
+    W = window
+    return W * (W + 1) // 2 + (S - W) * W
+
+
+def prefill_flops(w):
+    return 4 * w["Dh"] * w["B"] * w["Hq"] * visible_pairs(w["S"], w["causal"], w["window"])
+
+
+def prefill_bytes(w):
+    """Q, K, V read once and O written once (bf16)."""
+    return 2 * w["Dh"] * w["S"] * w["B"] * (2 * w["Hq"] + 2 * w["Hkv"])
+
+
+def decode_keys(w, seqlens):
+    L = np.asarray(seqlens, np.int64)
+    if w["window"] > 0:
+        L = np.minimum(L, w["window"])
+    return int(L.sum())
+
+
+def decode_bytes(w, seqlens):
+    """Every visible cached K and V row once (GQA shares it across the group),
+    plus q, o and the lengths."""
+    kv = decode_keys(w, seqlens) * w["Hkv"] * w["Dh"] * 2 * 2
+    return kv + 2 * w["B"] * w["Hq"] * w["Dh"] * 2 + 4 * w["B"]
+
+
+def decode_flops(w, seqlens):
+    return 4 * w["Dh"] * w["Hq"] * decode_keys(w, seqlens)
+
+
+# ------------------------------------------------------------------ environment
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def read_traffic():
+    """DRAM bytes per launch from a committed ncu summary, kept only while
+    the kernel source it was taken from is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    out = {}
+    for kernel, rec in data.items():
+        src = os.path.join(ROOT, rec.get("source", ""))
+        try:
+            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        except OSError:
+            continue
+        if sha == rec.get("source_sha16"):
+            out[kernel] = rec
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        out_dir = os.path.join(ROOT, "gpurun_out")
+        os.makedirs(out_dir, exist_ok=True)
+        self.path = os.path.join(out_dir, f"clocks_gpu{self.gpu}.csv")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def time_oracle(prefill_host, decode_host, w_p, w_d, prefill_heads=None, decode_seqs=None,
+                prefill_rows=None, min_prefill_s=0.0):
+    """Time the float64 oracle on a sample; returns (sample description,
+    prefill TFLOP/s, decode GB/s, seconds, threads).  The prefill sample is
+    repeated until it has run for at least min_prefill_s seconds."""
+    import oracle
+    q, k, v = prefill_host
+    B, Hq = w_p["B"], w_p["Hq"]
+    heads = prefill_heads or B * Hq
+    bsel = [i // Hq for i in range(heads)]
+    hsel = [i % Hq for i in range(heads)]
+    qs = torch.stack([q[b, h] for b, h in zip(bsel, hsel)])[None]
+    ks = torch.stack([k[b, h] for b, h in zip(bsel, hsel)])[None]
+    vs = torch.stack([v[b, h] for b, h in zip(bsel, hsel)])[None]
+    rows = None if prefill_rows is None else np.arange(w_p["S"] - prefill_rows, w_p["S"])
+    q64, k64, v64 = (x.double().numpy() for x in (qs, ks, vs))
+    reps, tp = 0, 0.0
+    while reps == 0 or tp < min_prefill_s:
+        t0 = time.perf_counter()
+        oracle.attention(q64, k64, v64, causal=w_p["causal"], window=w_p["window"], rows=rows)
+        tp += time.perf_counter() - t0
+        reps += 1
+    if rows is None:
+        pflops = 4 * w_p["Dh"] * heads * visible_pairs(w_p["S"], w_p["causal"], w_p["window"])
+    else:
+        pflops = 4 * w_p["Dh"] * heads * int(sum(r + 1 for r in rows))
+    pflops *= reps
+    qd, kc, vc, sl = decode_host
+    nseq = decode_seqs or w_d["B"]
+    Lmax = int(sl[:nseq].max())
+    kc64 = kc[:nseq, :, :Lmax].double().numpy()
+    vc64 = vc[:nseq, :, :Lmax].double().numpy()
+    q64d = qd[:nseq].double().numpy()
+    t0 = time.perf_counter()
+    oracle.decode(q64d, kc64, vc64, sl[:nseq].numpy(), window=w_d["window"])
+    td = time.perf_counter() - t0
+    wd = dict(w_d, B=nseq)
+    dbytes = decode_bytes(wd, sl[:nseq].numpy())
+    sample = (f"prefill {heads} of {B * Hq} (batch, head) pairs"
+              + (f", last {prefill_rows} rows" if rows is not None else ", all rows")
+              + (f", {reps} repetitions" if reps > 1 else "")
+              + f"; decode {nseq} of {w_d['B']} sequences, all heads")
+    return sample, pflops / tp / 1e12, dbytes / td / 1e9, tp + td, oracle.num_threads()
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores, as the reference arm."""
+    if rank != 0:
+        return None
+    w_p, w_d = inputs.WORKLOADS[PREFILL], inputs.WORKLOADS[DECODE]
+    ph = inputs.workload_inputs(PREFILL)
+    dh = inputs.workload_inputs(DECODE)
+    # each step: the last `rows` query rows of one head (the costliest rows of
+    # a causal pass) and one decode sequence; sized so the run stays short
+    budget = max(0.01, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = 64
+    _, _, _, sec, _ = time_oracle(ph, dh, w_p, w_d, prefill_heads=1, decode_seqs=1,
+                                  prefill_rows=rows)
+    while sec < 0.5 * budget and rows < w_p["S"]:
+        rows = min(w_p["S"], rows * 2)
+        _, _, _, sec, _ = time_oracle(ph, dh, w_p, w_d, prefill_heads=1, decode_seqs=1,
+                                      prefill_rows=rows)
+    for _ in range(args.warmup):
+        time_oracle(ph, dh, w_p, w_d, prefill_heads=1, decode_seqs=1, prefill_rows=rows)
+    pv, dv, secs = [], [], 0.0
+    for _ in range(args.steps):
+        sample, p, d, sec, thr = time_oracle(ph, dh, w_p, w_d, prefill_heads=1, decode_seqs=1,
+                                             prefill_rows=rows)
+        pv.append(p)
+        dv.append(d)
+        secs += sec
+    value = statistics.median(pv)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{PREFILL} + {DECODE}", "sample_per_step": sample},
+        "decode": {"value": statistics.median(dv), "unit": "GB/s"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def run_gpu(args, rank, world, local_rank):
+    import causal_head_self_gb300 as chs
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w_p, w_d = inputs.WORKLOADS[PREFILL], inputs.WORKLOADS[DECODE]
+    # weak scaling: every rank runs its own batch (seeds differ per rank)
+    qh, kh, vh = inputs.prefill_inputs(w_p["B"], w_p["Hq"], w_p["Hkv"], w_p["S"], w_p["Dh"],
+                                       w_p["seed"] + 1000 * rank)
+    qdh, kch, vch, slh = inputs.decode_inputs(w_d["B"], w_d["Hq"], w_d["Hkv"], w_d["Tmax"],
+                                              w_d["Dh"], w_d["lmin"], w_d["lmax"],
+                                              w_d["seed"] + 1000 * rank)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    o = torch.empty_like(q)
+    qd, kc, vc, sl = qdh.to(dev), kch.to(dev), vch.to(dev), slh.to(dev)
+    od = torch.empty_like(qd)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    pf, pb = prefill_flops(w_p), prefill_bytes(w_p)
+    db, dfl = decode_bytes(w_d, slh.numpy()), decode_flops(w_d, slh.numpy())
+
+    def step(ev=None):
+        flush.zero_()
+        if ev is not None:
+            ev[0].record(stream)
+        chs.attn_fwd(q, k, v, o, causal=bool(w_p["causal"]), window=w_p["window"])
+        if ev is not None:
+            ev[1].record(stream)
+        chs.attn_decode(qd, kc, vc, sl, od, window=w_d["window"])
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if chs.attn_status() != chs.ATTN_OK:
+        raise RuntimeError("device error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    status = chs.attn_status()
+    if status != chs.ATTN_OK:
+        raise RuntimeError(f"device error in the timed region: {status}")
+    t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3   # seconds
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    if world > 1:
+        t = torch.tensor([t_pre, t_dec, t_wall], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_pre, t_dec, t_wall = t.tolist()
+
+    # ---------------------------------------------------------- end to end (host buffers)
+    e2e_steps = max(3, min(20, args.steps))
+    qp, kp, vp = (x.pin_memory() for x in (qh, kh, vh))
+    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    qdp, kcp, vcp, slp = (x.pin_memory() for x in (qdh, kch, vch, slh))
+    odp = torch.empty(od.shape, dtype=od.dtype).pin_memory()
+    e2e_p, e2e_d = [], []
+    for i in range(e2e_steps + 2):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        flush.zero_()
+        e[0].record(stream)
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        chs.attn_fwd(q, k, v, o, causal=bool(w_p["causal"]), window=w_p["window"])
+        op.copy_(o, non_blocking=True)
+        e[1].record(stream)
+        qd.copy_(qdp, non_blocking=True)
+        kc.copy_(kcp, non_blocking=True)
+        vc.copy_(vcp, non_blocking=True)
+        sl.copy_(slp, non_blocking=True)
+        chs.attn_decode(qd, kc, vc, sl, od, window=w_d["window"])
+        odp.copy_(od, non_blocking=True)
+        e[2].record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= 2:
+            e2e_p.append(e[0].elapsed_time(e[1]) / 1e3)
+            e2e_d.append(e[1].elapsed_time(e[2]) / 1e3)
+    if chs.attn_status() != chs.ATTN_OK:
+        raise RuntimeError("device error in the end-to-end loop")
+    tp_e2e, td_e2e = statistics.mean(e2e_p), statistics.mean(e2e_d)
+    if world > 1:
+        t = torch.tensor([tp_e2e, td_e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tp_e2e, td_e2e = t.tolist()
+    if rank != 0:
+        return None
+
+    # ---------------------------------------------------------- report
+    K = args.steps
+    peaks, peak_src = read_peaks()
+    traffic = read_traffic()
+    pre_launch = t_pre / K
+    dec_launch = t_dec / K
+    pre_tflops = pf / pre_launch / 1e12
+    dec_gbs = db / dec_launch / 1e9
+    kp_name = "attn_prefill_sm103a<128>"
+    kd_name = "attn_decode_split_sm103a<128,4>+attn_decode_combine_sm103a<128>"
+    roof_p = {"kernel": kp_name, "bound": "tensor", "achieved": pre_tflops,
+              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+              "frac": pre_tflops / peaks["bf16_tflops"],
+              "traffic": traffic.get(kp_name, {}).get("bytes_per_launch"),
+              "peak_source": f"{peak_src} bf16 burst (kernel timed alone)",
+              "algorithmic_flops_per_launch": pf, "launch_ms": pre_launch * 1e3}
+    roof_d = {"kernel": kd_name, "bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
+              "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+              "traffic": traffic.get("attn_decode_split_sm103a<128,4>", {}).get("bytes_per_launch"),
+              "peak_source": f"{peak_src} HBM copy bandwidth",
+              "algorithmic_bytes_per_launch": db, "launch_ms": dec_launch * 1e3}
+    dominant = roof_d if dec_launch >= pre_launch else roof_p
+
+    # CPU baseline: the oracle on this machine's host cores, N=1 only
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        sample, p_tf, d_gbs, sec, thr = time_oracle((qh, kh, vh), (qdh, kch, vch, slh), w_p, w_d,
+                                                    min_prefill_s=10.0)
+        cpu = {"value": p_tf, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": sample,
+               "seconds": sec, "decode_value": d_gbs, "decode_unit": "GB/s"}
+
+    return {
+        "impl": "gb300", "metric": METRIC, "value": pre_tflops * world, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": (t_pre + t_dec) / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": f"{PREFILL} + {DECODE}",
+            "prefill": {k: w_p[k] for k in ("B", "Hq", "Hkv", "S", "Dh", "causal", "window")},
+            "decode": {k: w_d[k] for k in ("B", "Hq", "Hkv", "Tmax", "Dh", "lmin", "lmax", "window")},
+            "l2": "flushed by a 256 MiB write before every step (outside the timed kernels)",
+            "parallelism": f"dp{world} (independent batches per GPU)",
+        },
+        "frac_of_peak": {"prefill_bf16_burst": pre_tflops / peaks["bf16_tflops"],
+                         "prefill_bf16_sustained": pre_tflops / peaks["bf16_tflops_sustained"],
+                         "decode_hbm": dec_gbs / peaks["hbm_gbs"],
+                         "decode_hbm_8TBps_spec": dec_gbs / 8000.0, "peaks": peak_src},
+        "decode": {"value": dec_gbs * world, "unit": "GB/s",
+                   "tokens_per_s": w_d["B"] * world / dec_launch,
+                   "tflops": dfl / dec_launch / 1e12 * world, "ms_per_launch": dec_launch * 1e3},
+        "roofline": dominant,
+        "rooflines": {"prefill": roof_p, "decode": roof_d},
+        "cpu_baseline": cpu,
+        "e2e": {"value": pf / tp_e2e / 1e12 * world, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (qh, kh, vh)),
+                "d2h_bytes_per_step": o.numel() * o.element_size(),
+                "decode": {"value": db / td_e2e / 1e9 * world, "unit": "GB/s",
+                           "h2d_bytes_per_step": sum(x.numel() * x.element_size()
+                                                     for x in (qdh, kch, vch, slh)),
+                           "d2h_bytes_per_step": od.numel() * od.element_size()}},
+        "gpu_launches": 3 * K,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        line = run_gpu(args, rank, world, local_rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
