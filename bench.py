@@ -372,7 +372,7 @@ def run_gpu(args, rank, world, local_rank):
     pre_tflops = pf / pre_launch / 1e12
     dec_gbs = db / dec_launch / 1e9
     kp_name = "attn_prefill_sm103a<128>"
-    kd_name = "attn_decode_split_sm103a<128,4>+attn_decode_combine_sm103a<128>"
+    kd_name = "attn_decode_sm103a<128,4>"
     roof_p = {"kernel": kp_name, "bound": "tensor", "achieved": pre_tflops,
               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
               "frac": pre_tflops / peaks["bf16_tflops"],
@@ -381,7 +381,7 @@ def run_gpu(args, rank, world, local_rank):
               "algorithmic_flops_per_launch": pf, "launch_ms": pre_launch * 1e3}
     roof_d = {"kernel": kd_name, "bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
               "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
-              "traffic": traffic.get("attn_decode_split_sm103a<128,4>", {}).get("bytes_per_launch"),
+              "traffic": traffic.get(kd_name, {}).get("bytes_per_launch"),
               "peak_source": f"{peak_src} HBM copy bandwidth",
               "algorithmic_bytes_per_launch": db, "launch_ms": dec_launch * 1e3}
     dominant = roof_d if dec_launch >= pre_launch else roof_p
@@ -423,7 +423,7 @@ def run_gpu(args, rank, world, local_rank):
                            "h2d_bytes_per_step": sum(x.numel() * x.element_size()
                                                      for x in (qdh, kch, vch, slh)),
                            "d2h_bytes_per_step": od.numel() * od.element_size()}},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,   # one prefill and one decode kernel per step
         "clocks": clocks.summary(),
         "wall_s_timed_region": t_wall,
     }

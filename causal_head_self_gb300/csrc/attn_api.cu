@@ -24,9 +24,36 @@ __device__ int g_attn_error_word;
 struct DeviceState {
   bool ready = false;
   chs::DeviceInfo info{};
-  void* workspace = nullptr;
-  size_t workspace_bytes = 0;
+  // decode workspace: split partials, and completion counters kept in a
+  // buffer of their own (always zero between calls)
+  void* partials = nullptr;
+  size_t partials_bytes = 0;
+  int* counters = nullptr;
+  size_t counters_n = 0;
 };
+
+// Grow a device buffer (never inside a stream capture); zero it if asked.
+int grow_buffer(void** buf, size_t* have, size_t need, bool zero, cudaStream_t stream) {
+  if (*have >= need) return ATTN_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return ATTN_ERR_NO_MEMORY;   // cudaMalloc cannot run inside a capture
+  if (*buf) cudaFree(*buf);      // cudaFree waits for work still using it
+  *buf = nullptr;
+  *have = 0;
+  if (cudaMalloc(buf, need) != cudaSuccess) {
+    *buf = nullptr;
+    cudaGetLastError();
+    return ATTN_ERR_NO_MEMORY;
+  }
+  if (zero && cudaMemset(*buf, 0, need) != cudaSuccess) {
+    cudaFree(*buf);
+    *buf = nullptr;
+    return ATTN_ERR_CUDA;
+  }
+  *have = need;
+  return ATTN_OK;
+}
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
@@ -165,29 +192,25 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
   if (rc != ATTN_OK) return rc;
   const chs::DecodePlan plan = chs::plan_decode(B, Hq, Hkv, Tmax, Dh, st->info.num_sms);
   if ((long long)Hkv * ((Hq / Hkv) / plan.heads_per_cta) > 65535) return ATTN_ERR_INVALID_ARG;
-  const size_t need = chs::decode_workspace_bytes(B, Hq, Dh, plan);
-  void* ws = nullptr;
+  const size_t need_partials = chs::decode_partials_bytes(B, Hq, Dh, plan);
+  const size_t need_counters = chs::decode_counter_count(B, Hq, Hkv, plan);
+  void* partials = nullptr;
+  int* counters = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (st->workspace_bytes < need) {
-      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-      if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess ||
-          cap != cudaStreamCaptureStatusNone)
-        return ATTN_ERR_NO_MEMORY;   // cannot grow the workspace inside a capture
-      if (st->workspace) cudaFree(st->workspace);
-      st->workspace = nullptr;
-      st->workspace_bytes = 0;
-      if (cudaMalloc(&st->workspace, need) != cudaSuccess) {
-        st->workspace = nullptr;
-        cudaGetLastError();
-        return ATTN_ERR_NO_MEMORY;
-      }
-      st->workspace_bytes = need;
-    }
-    ws = st->workspace;
+    rc = grow_buffer(&st->partials, &st->partials_bytes, need_partials, false, stream);
+    if (rc != ATTN_OK) return rc;
+    size_t counter_bytes = st->counters_n * sizeof(int);
+    void* cbuf = st->counters;
+    rc = grow_buffer(&cbuf, &counter_bytes, need_counters * sizeof(int), true, stream);
+    st->counters = static_cast<int*>(cbuf);
+    st->counters_n = counter_bytes / sizeof(int);
+    if (rc != ATTN_OK) return rc;
+    partials = st->partials;
+    counters = st->counters;
   }
   cudaError_t e = chs::launch_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, window,
-                                     scale_log2, plan, ws, st->info, stream);
+                                     scale_log2, plan, counters, partials, st->info, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

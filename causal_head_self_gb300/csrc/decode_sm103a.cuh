@@ -7,19 +7,22 @@
 // sections "KV-кэш", "Prefill и decode" and "Скользящее окно").  The step reads
 // the whole cache for little arithmetic, so it is bound by HBM bandwidth.
 //
-// Split kernel: grid (nsplit, Hkv * groups, B).  A CTA takes `chunk` keys of
-// one (b, K/V head) and every query head of its GQA group that it holds
-// (heads_per_cta of them), so each cached K/V byte is read once per group.
-// One producer thread streams 64-key blocks of K and V into a shared-memory
-// ring with cp.async.bulk; four consumer warps take 16 keys each per block.
-// Within a warp, LPK = DH/16 lanes share one key (16 elements of DH each),
-// dot products are finished with xor shuffles, and each key slot keeps its
-// own running max / running sum / output (the online softmax).  The CTA then
-// merges its 16 slot states and writes an unnormalised partial output with
-// its max and sum.
+// One kernel, grid (nsplit, Hkv * groups, B).  A CTA takes `chunk` keys of one
+// (b, K/V head) and the HPB query heads of that head's GQA group it holds, so
+// each cached byte is read from HBM once per group.  One producer thread
+// streams 32-key blocks of K and V into a four-stage shared-memory ring with
+// cp.async.bulk; four consumer warps take 8 keys of each block.  In a warp,
+// LPK = DH/8 lanes share a key, one 16-byte chunk (8 elements) each; every
+// lane holds all HPB query heads' matching chunks and output accumulators as
+// packed float2 (fma.rn.f32x2).  A key's HPB dot products are finished with a
+// transposing xor-shuffle reduction, and each key slot keeps its own running
+// max, running sum and output (the online softmax).  The CTA merges its slots
+// and writes an unnormalised partial with its max and sum.
 //
-// Combine kernel: grid B * Hq.  Merges the partials of a query head:
-// o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s with M = max_s m_s.
+// The last CTA to finish a (b, K/V head, group) -- counted with one atomic per
+// CTA -- merges the partials of all splits in split order (so the result does
+// not depend on which CTA was last):
+//   o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
 #pragma once
 
 #include "sm103a_ptx.cuh"
@@ -35,16 +38,18 @@ struct DecodeParams {
   float* o_part;            // [B, Hq, nsplit, DH]
   float* m_part;            // [B, Hq, nsplit]   (log2 domain)
   float* l_part;            // [B, Hq, nsplit]
+  int* counters;            // [B, Hkv * groups], zero between calls
   int B, Hq, Hkv, Tmax, window;
   int nsplit, chunk;
   float scale_log2;
   int* error_word;
 };
 
-constexpr int kDecodeBlockKeys = 64;    // keys per pipeline stage
-constexpr int kDecodeStages = 3;
+constexpr int kDecodeBlockKeys = 32;    // keys per pipeline stage
+constexpr int kDecodeStages = 4;
 constexpr int kDecodeConsumerWarps = 4;
 constexpr int kDecodeThreads = 32 * (kDecodeConsumerWarps + 1);
+constexpr int kDecodeCtasPerSm = 3;
 
 template <int DH, int HPB>
 struct __align__(128) DecodeSmem {
@@ -55,6 +60,7 @@ struct __align__(128) DecodeSmem {
   float red_l[kDecodeConsumerWarps][HPB];
   uint64_t full[kDecodeStages], empty[kDecodeStages];
   int abort_flag;
+  int is_last;
 };
 
 // keys [k_begin, k_end) of split `split`, for a sequence of L keys
@@ -65,20 +71,54 @@ __device__ __forceinline__ void decode_split_range(int L, int window, int split,
   k_end = min((split + 1) * chunk, L);
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+// bf16 pair (low half = lower-addressed element) -> float2
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t x) {
+  return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
 
-__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (&f)[16]) {
-  f[0] = bf16lo(a.x); f[1] = bf16hi(a.x); f[2] = bf16lo(a.y); f[3] = bf16hi(a.y);
-  f[4] = bf16lo(a.z); f[5] = bf16hi(a.z); f[6] = bf16lo(a.w); f[7] = bf16hi(a.w);
-  f[8] = bf16lo(b.x); f[9] = bf16hi(b.x); f[10] = bf16lo(b.y); f[11] = bf16hi(b.y);
-  f[12] = bf16lo(b.z); f[13] = bf16hi(b.z); f[14] = bf16lo(b.w); f[15] = bf16hi(b.w);
+__device__ __forceinline__ void unpack_chunk(const uint4& w, float2 (&f)[4]) {
+  f[0] = bf16x2_to_float2(w.x);
+  f[1] = bf16x2_to_float2(w.y);
+  f[2] = bf16x2_to_float2(w.z);
+  f[3] = bf16x2_to_float2(w.w);
+}
+
+// Sum each of s[0..HPB) over the LPK lanes of a key group (aligned groups of
+// LPK consecutive lanes); every lane of the group ends with all HPB sums.
+// For four heads the first two rounds transpose (each lane passes on half of
+// its values and keeps half), so one head's sum is finished per lane with
+// 5 shuffles, then broadcast with 4 more.
+template <int HPB, int LPK>
+__device__ __forceinline__ void key_group_allreduce(float (&s)[HPB], int lane) {
+  if constexpr (HPB == 4 && LPK >= 4) {
+    constexpr int o1 = LPK / 2, o2 = LPK / 4;
+    const bool up1 = (lane & o1) != 0, up2 = (lane & o2) != 0;
+    float k0 = up1 ? s[2] : s[0], k1 = up1 ? s[3] : s[1];
+    const float x0 = up1 ? s[0] : s[2], x1 = up1 ? s[1] : s[3];
+    k0 += __shfl_xor_sync(0xffffffffu, x0, o1);
+    k1 += __shfl_xor_sync(0xffffffffu, x1, o1);
+    float k = up2 ? k1 : k0;
+    const float x = up2 ? k0 : k1;
+    k += __shfl_xor_sync(0xffffffffu, x, o2);
+#pragma unroll
+    for (int off = LPK / 8; off >= 1; off /= 2) k += __shfl_xor_sync(0xffffffffu, k, off);
+    // this lane now holds head (2*up1 + up2); fetch every head from its holder
+    const int base = lane & ~(LPK - 1);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      s[h] = __shfl_sync(0xffffffffu, k, base + (h >> 1) * o1 + (h & 1) * o2);
+  } else {
+#pragma unroll
+    for (int off = LPK / 2; off >= 1; off /= 2)
+#pragma unroll
+      for (int h = 0; h < HPB; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
+  }
 }
 
 template <int DH, int HPB>
-__global__ void __launch_bounds__(kDecodeThreads)
-    attn_decode_split_sm103a(const DecodeParams p) {
-  constexpr int LPK = DH / 16;          // lanes per key
+__global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
+    attn_decode_sm103a(const DecodeParams p) {
+  constexpr int LPK = DH / 8;           // lanes per key (one 16-byte chunk each)
   constexpr int KPS = 32 / LPK;         // keys per warp step
   constexpr int KPW = kDecodeBlockKeys / kDecodeConsumerWarps;   // keys per warp per block
   constexpr int ROW = DH * 2;           // bytes per cached row
@@ -93,14 +133,22 @@ __global__ void __launch_bounds__(kDecodeThreads)
   const int g = blockIdx.y / groups;
   const int hsub = blockIdx.y % groups;
   const int b = blockIdx.z;
+  const int hq0 = g * (p.Hq / p.Hkv) + hsub * HPB;   // first query head of this CTA
   const int L = p.seqlens[b];
-  if (L < 1 || L > p.Tmax) return;   // rejected by the combine kernel
+  if (L < 1 || L > p.Tmax) {
+    // a sequence length outside [1, Tmax]: zero output, latch the error
+    if (split == 0) {
+      for (int i = threadIdx.x; i < HPB * DH; i += blockDim.x)
+        p.o[(size_t)(b * p.Hq + hq0) * DH + i] = __float2bfloat16(0.f);
+      if (threadIdx.x == 0) atomicExch(p.error_word, 1);   // ATTN_ERR_INVALID_ARG
+    }
+    return;
+  }
   int k_begin, k_end;
   decode_split_range(L, p.window, split, p.chunk, k_begin, k_end);
   if (k_begin >= k_end) return;      // this split holds no visible key
   const int nkeys = k_end - k_begin;
   const int nblk = (nkeys + kDecodeBlockKeys - 1) / kDecodeBlockKeys;
-  const int hq0 = g * (p.Hq / p.Hkv) + hsub * HPB;   // first query head of this CTA
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -132,6 +180,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         par = (par & ~(1u << st)) | (ph << st);
         if (++st == kDecodeStages) { st = 0; ph ^= 1; }
       }
+      // every copy this thread started has landed before the CTA may exit
       for (int i = 0; i < kDecodeStages; ++i) {
         if (!(loaded & (1u << i))) continue;
         const uint32_t a = smem_u32(&sm.full[i]);
@@ -143,25 +192,21 @@ __global__ void __launch_bounds__(kDecodeThreads)
   } else {
     // ------------------------------------------------------------ consumers
     const int kslot = lane / LPK, part = lane % LPK;
-    const int flip = (lane >> 2) & 1;   // spreads a quarter-warp over all banks
-    const int c1 = 2 * part + flip, c2 = 2 * part + 1 - flip;   // 16-byte chunks of a row
-
-    float qr[HPB][16];
+    float2 q2[HPB][4], acc[HPB][4];
+    float m[HPB], l[HPB];
 #pragma unroll
     for (int h = 0; h < HPB; ++h) {
-      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (size_t)(b * p.Hq + hq0 + h) * DH);
-      float f[16];
-      unpack16(qrow[c1], qrow[c2], f);
+      const uint4 w =
+          reinterpret_cast<const uint4*>(p.q + (size_t)(b * p.Hq + hq0 + h) * DH)[part];
+      unpack_chunk(w, q2[h]);
+      const float2 sc = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) qr[h][e] = f[e] * p.scale_log2;
-    }
-    float acc[HPB][16], m[HPB], l[HPB];
-#pragma unroll
-    for (int h = 0; h < HPB; ++h) {
+      for (int i = 0; i < 4; ++i) {
+        q2[h][i] = __fmul2_rn(q2[h][i], sc);
+        acc[h][i] = make_float2(0.f, 0.f);
+      }
       m[h] = -INFINITY;
       l[h] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) acc[h][e] = 0.f;
     }
 
     uint32_t st = 0, ph = 0;
@@ -174,43 +219,40 @@ __global__ void __launch_bounds__(kDecodeThreads)
       for (int step = 0; step < KPW / KPS; ++step) {
         const int key = warp * KPW + step * KPS + kslot;
         const bool valid = key < n;
-        uint4 ka = make_uint4(0, 0, 0, 0), kb2 = ka, va = ka, vb2 = ka;
+        uint4 kw = make_uint4(0, 0, 0, 0), vw = kw;
         if (valid) {
-          ka = *reinterpret_cast<const uint4*>(kb + key * ROW + c1 * 16);
-          kb2 = *reinterpret_cast<const uint4*>(kb + key * ROW + c2 * 16);
-          va = *reinterpret_cast<const uint4*>(vb + key * ROW + c1 * 16);
-          vb2 = *reinterpret_cast<const uint4*>(vb + key * ROW + c2 * 16);
+          kw = *reinterpret_cast<const uint4*>(kb + key * ROW + part * 16);
+          vw = *reinterpret_cast<const uint4*>(vb + key * ROW + part * 16);
         }
-        float kf[16];
-        unpack16(ka, kb2, kf);
+        float2 k2[4];
+        unpack_chunk(kw, k2);
         float s[HPB];
 #pragma unroll
         for (int h = 0; h < HPB; ++h) {
-          float d = 0.f;
+          float2 d = __fmul2_rn(q2[h][0], k2[0]);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) d = fmaf(qr[h][e], kf[e], d);
-          s[h] = d;
+          for (int i = 1; i < 4; ++i) d = __ffma2_rn(q2[h][i], k2[i], d);
+          s[h] = d.x + d.y;
         }
-#pragma unroll
-        for (int off = LPK / 2; off >= 1; off /= 2)
-#pragma unroll
-          for (int h = 0; h < HPB; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
+        key_group_allreduce<HPB, LPK>(s, lane);
         if (valid) {
-          float vf[16];
-          unpack16(va, vb2, vf);
+          float2 v2[4];
+          unpack_chunk(vw, v2);
 #pragma unroll
           for (int h = 0; h < HPB; ++h) {
             if (s[h] > m[h]) {   // the running max grows: rescale this slot's state
               const float corr = ex2_approx(m[h] - s[h]);
+              const float2 c2 = make_float2(corr, corr);
               l[h] *= corr;
 #pragma unroll
-              for (int e = 0; e < 16; ++e) acc[h][e] *= corr;
+              for (int i = 0; i < 4; ++i) acc[h][i] = __fmul2_rn(acc[h][i], c2);
               m[h] = s[h];
             }
             const float pw = ex2_approx(s[h] - m[h]);
+            const float2 p2 = make_float2(pw, pw);
             l[h] += pw;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+            for (int i = 0; i < 4; ++i) acc[h][i] = __ffma2_rn(p2, v2[i], acc[h][i]);
           }
         }
       }
@@ -219,19 +261,6 @@ __global__ void __launch_bounds__(kDecodeThreads)
       if (++st == kDecodeStages) { st = 0; ph ^= 1; }
     }
 
-    // bring every slot to the chunk order of key slot 0 (lane == part), whose
-    // lanes write the merged result below
-    const int flip0 = (part >> 2) & 1;
-    if (flip != flip0) {
-#pragma unroll
-      for (int h = 0; h < HPB; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float t = acc[h][e];
-          acc[h][e] = acc[h][8 + e];
-          acc[h][8 + e] = t;
-        }
-    }
     // merge the key slots of this warp (lanes with equal `part`)
 #pragma unroll
     for (int h = 0; h < HPB; ++h) {
@@ -239,14 +268,18 @@ __global__ void __launch_bounds__(kDecodeThreads)
 #pragma unroll
       for (int off = LPK; off < 32; off *= 2) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
       const float f = (m[h] == -INFINITY) ? 0.f : ex2_approx(m[h] - mw);
+      const float2 f2 = make_float2(f, f);
       float lw = l[h] * f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) acc[h][e] *= f;
+      for (int i = 0; i < 4; ++i) acc[h][i] = __fmul2_rn(acc[h][i], f2);
 #pragma unroll
       for (int off = LPK; off < 32; off *= 2) {
         lw += __shfl_xor_sync(0xffffffffu, lw, off);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], off);
+        for (int i = 0; i < 4; ++i) {
+          acc[h][i].x += __shfl_xor_sync(0xffffffffu, acc[h][i].x, off);
+          acc[h][i].y += __shfl_xor_sync(0xffffffffu, acc[h][i].y, off);
+        }
       }
       if (lane == 0) {
         sm.red_m[warp][h] = mw;
@@ -254,14 +287,18 @@ __global__ void __launch_bounds__(kDecodeThreads)
       }
       if (kslot == 0) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          sm.red_o[warp][h][8 * c1 + e] = acc[h][e];
-          sm.red_o[warp][h][8 * c2 + e] = acc[h][8 + e];
+        for (int i = 0; i < 4; ++i) {
+          sm.red_o[warp][h][part * 8 + 2 * i] = acc[h][i].x;
+          sm.red_o[warp][h][part * 8 + 2 * i + 1] = acc[h][i].y;
         }
       }
     }
     named_bar_sync(1, 32 * kDecodeConsumerWarps);
-    // merge the warps and write this split's partial
+
+    const int lo = p.window > 0 ? max(0, L - p.window) : 0;
+    const int s_first = lo / p.chunk, s_last = (L - 1) / p.chunk;
+    const bool single = s_first == s_last;   // the whole key range is this CTA's
+    // merge the warps: this CTA's result for each (head, d)
     for (int idx = threadIdx.x; idx < HPB * DH; idx += 32 * kDecodeConsumerWarps) {
       const int h = idx / DH, d = idx % DH;
       float M = sm.red_m[0][h];
@@ -275,45 +312,54 @@ __global__ void __launch_bounds__(kDecodeThreads)
         o = fmaf(f, sm.red_o[w][h][d], o);
         lsum = fmaf(f, sm.red_l[w][h], lsum);
       }
-      const size_t ph_idx = ((size_t)b * p.Hq + hq0 + h) * p.nsplit + split;
-      p.o_part[ph_idx * DH + d] = o;
-      if (d == 0) {
-        p.m_part[ph_idx] = M;
-        p.l_part[ph_idx] = lsum;
+      const size_t bh = (size_t)b * p.Hq + hq0 + h;
+      if (single) {
+        p.o[bh * DH + d] = __float2bfloat16(o / lsum);
+      } else {
+        const size_t ps = bh * p.nsplit + split;
+        p.o_part[ps * DH + d] = o;
+        if (d == 0) {
+          p.m_part[ps] = M;
+          p.l_part[ps] = lsum;
+        }
+      }
+    }
+
+    if (!single) {
+      // the last CTA of this (b, K/V head, group) to get here merges all splits
+      __threadfence();
+      named_bar_sync(1, 32 * kDecodeConsumerWarps);
+      int* counter = p.counters + (size_t)b * gridDim.y + blockIdx.y;
+      if (threadIdx.x == 0) {
+        const int prev = atomicAdd(counter, 1);
+        sm.is_last = prev == s_last - s_first;
+      }
+      named_bar_sync(1, 32 * kDecodeConsumerWarps);
+      if (sm.is_last) {
+        __threadfence();
+        for (int idx = threadIdx.x; idx < HPB * DH; idx += 32 * kDecodeConsumerWarps) {
+          const int h = idx / DH, d = idx % DH;
+          const size_t bh = (size_t)b * p.Hq + hq0 + h;
+          const float* mp = p.m_part + bh * p.nsplit;
+          const float* lp = p.l_part + bh * p.nsplit;
+          const float* op = p.o_part + bh * p.nsplit * DH;
+          float M = -INFINITY;
+          for (int s = s_first; s <= s_last; ++s) M = fmaxf(M, __ldcg(mp + s));
+          float o = 0.f, lsum = 0.f;
+          for (int s = s_first; s <= s_last; ++s) {
+            const float f = ex2_approx(__ldcg(mp + s) - M);
+            o = fmaf(f, __ldcg(op + (size_t)s * DH + d), o);
+            lsum = fmaf(f, __ldcg(lp + s), lsum);
+          }
+          p.o[bh * DH + d] = __float2bfloat16(o / lsum);
+        }
+        if (threadIdx.x == 0) *counter = 0;   // ready for the next call
       }
     }
   }
   __syncwarp();
   __syncthreads();
   if (threadIdx.x == 0 && sm.abort_flag) atomicExch(p.error_word, 4);   // ATTN_ERR_TIMEOUT
-}
-
-template <int DH>
-__global__ void __launch_bounds__(DH) attn_decode_combine_sm103a(const DecodeParams p) {
-  const int bh = blockIdx.x;
-  const int b = bh / p.Hq;
-  const int d = threadIdx.x;
-  const int L = p.seqlens[b];
-  __nv_bfloat16* out = p.o + (size_t)bh * DH;
-  if (L < 1 || L > p.Tmax) {   // a sequence length outside [1, Tmax]: zeros + error
-    out[d] = __float2bfloat16(0.f);
-    if (d == 0) atomicExch(p.error_word, 1);   // ATTN_ERR_INVALID_ARG
-    return;
-  }
-  const int lo = p.window > 0 ? max(0, L - p.window) : 0;
-  const int s0 = lo / p.chunk, s1 = (L - 1) / p.chunk;
-  const float* mp = p.m_part + (size_t)bh * p.nsplit;
-  const float* lp = p.l_part + (size_t)bh * p.nsplit;
-  const float* op = p.o_part + (size_t)bh * p.nsplit * DH;
-  float M = -INFINITY;
-  for (int s = s0; s <= s1; ++s) M = fmaxf(M, mp[s]);
-  float o = 0.f, lsum = 0.f;
-  for (int s = s0; s <= s1; ++s) {
-    const float f = ex2_approx(mp[s] - M);
-    o = fmaf(f, op[(size_t)s * DH + d], o);
-    lsum = fmaf(f, lp[s], lsum);
-  }
-  out[d] = __float2bfloat16(o / lsum);
 }
 
 template <int DH, int HPB>

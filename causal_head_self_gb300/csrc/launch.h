@@ -31,12 +31,17 @@ struct DecodePlan {
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int Tmax, int Dh, int num_sms);
 
-// Bytes of split partials a decode call with this plan needs.
-size_t decode_workspace_bytes(int B, int Hq, int Dh, const DecodePlan& plan);
+// Bytes of split partials (o, max, sum) a decode call with this plan needs.
+size_t decode_partials_bytes(int B, int Hq, int Dh, const DecodePlan& plan);
+
+// Completion counters (one int per CTA group) a decode call needs.  They
+// must be zero before the call, and every call leaves them zero again, so a
+// buffer that only ever holds counters stays valid across calls and shapes.
+size_t decode_counter_count(int B, int Hq, int Hkv, const DecodePlan& plan);
 
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int* seqlens,
                           void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,
-                          float scale_log2, const DecodePlan& plan, void* workspace,
-                          const DeviceInfo& dev, cudaStream_t stream);
+                          float scale_log2, const DecodePlan& plan, int* counters,
+                          void* partials, const DeviceInfo& dev, cudaStream_t stream);
 
 }  // namespace chs

@@ -18,6 +18,9 @@
 //   warps 4-7  softmax + epilogue of sub-tile 1
 //   warp  8    TMEM allocation; one thread issues every tcgen05.mma
 //   warp  9    one thread issues every TMA load (Q once, then K/V tiles)
+// With three warps on some SM sub-partitions, 168 registers per thread is the
+// most a 10-warp CTA gets; the softmax keeps a 128-score row plus a few
+// running values live within that.
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DH),
 // O1 [384,384+DH).  P (bf16) is written over the first 64 columns of its S
 // and fed to the P.V MMA straight from TMEM.
@@ -206,26 +209,26 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, DH, false, true);
-      const uint32_t colS[2] = {tbase + Cfg::kColS0, tbase + Cfg::kColS1};
-      const uint32_t colO[2] = {tbase + Cfg::kColO0, tbase + Cfg::kColO1};
       // S_s = Q_s K^T: K-major operands, 16 columns (32 bytes) of DH per MMA
       auto issue_qk = [&](int s, int kst) {
+        const uint32_t d = tbase + (s ? Cfg::kColS1 : Cfg::kColS0);
         const uint32_t qa = smem_u32(sm.q[s]), ka = smem_u32(sm.k[kst]);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-          mma_bf16_ss(colS[s], smem_desc_sw128(qa + off, 16, 1024),
-                      smem_desc_sw128(ka + off, 16, 1024), idesc_qk, kk > 0);
+          mma_bf16_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                      idesc_qk, kk > 0);
         }
       };
       // O_s (+)= P_s V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
       auto issue_pv = [&](int s, int vst, bool acc) {
+        const uint32_t d = tbase + (s ? Cfg::kColO1 : Cfg::kColO0);
+        const uint32_t a = tbase + (s ? Cfg::kColS1 : Cfg::kColS0);
         const uint32_t va = smem_u32(sm.v[vst]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(colO[s], colS[s] + kk * 8,
-                      smem_desc_sw128(va + kk * 2048, Cfg::kBoxBytes, 1024), idesc_pv,
-                      (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(d, a + kk * 8, smem_desc_sw128(va + kk * 2048, Cfg::kBoxBytes, 1024),
+                      idesc_pv, (acc || kk > 0) ? 1u : 0u);
       };
       int n_active[2] = {0, 0};
       uint32_t kst = 0, kph = 0, vst = 0, vph = 0, pph0 = 0, pph1 = 0;
@@ -345,9 +348,17 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 128; ++c)
           if (c < clo || c > chi) x[c] = -INFINITY;
       }
-      float mt = x[0];
+      // row maximum as four independent chains of three-input max
+      float mx[4];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, x[c]);
+      for (int i = 0; i < 4; ++i) mx[i] = fmax3(x[i], x[4 + i], x[8 + i]);
+#pragma unroll
+      for (int c = 12; c < 124; c += 8)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], x[c + i], x[c + 4 + i]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], x[124 + i]);
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float m_tile = mt * sl2;
       // lazy rescale: keep the old maximum unless the new one exceeds it by
       // more than 8 (weights stay <= 2^8); the result is exact either way
@@ -356,21 +367,10 @@ __global__ void __launch_bounds__(320, 1)
       const bool upd = (n_done == 0) || (m_new > m_run + 8.0f);
       const float m_use = upd ? m_new : m_run;
       const float corr = (upd && n_done > 0) ? ex2_approx(m_run - m_new) : 1.0f;
-      if (__any_sync(0xffffffffu, corr != 1.0f)) {
-#pragma unroll
-        for (int c = 0; c < DH / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(colO + 32 * c, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          tmem_st_32x32b_x32(colO + 32 * c, o);
-        }
-      }
-      l_run *= corr;
-      m_run = m_use;
       const float msub = (m_use == -INFINITY) ? 0.f : m_use;
-      float lsum = 0.f;
+      // P = exp2(x - m) as bf16 over the first 64 columns of S (the scores
+      // die here, before O is touched, to keep register pressure down)
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};   // independent partial sums
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t pk[16];
@@ -378,12 +378,27 @@ __global__ void __launch_bounds__(320, 1)
         for (int e = 0; e < 16; ++e) {
           const float p0 = ex2_approx(fmaf(x[32 * c4 + 2 * e], sl2, -msub));
           const float p1 = ex2_approx(fmaf(x[32 * c4 + 2 * e + 1], sl2, -msub));
-          lsum += p0 + p1;
+          ls[e & 3] += p0 + p1;
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st_32x32b_x16(colS + 16 * c4, pk);
       }
-      l_run += lsum;
+      const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // a raised maximum rescales this row's O (all earlier P.V are done:
+      // the S MMA just waited for was issued after them)
+      if (__any_sync(0xffffffffu, corr != 1.0f)) {
+#pragma unroll 1
+        for (int c = 0; c < DH / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld_32x32b_x16(colO + 16 * c, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+          tmem_st_32x32b_x16(colO + 16 * c, o);
+        }
+      }
+      l_run = l_run * corr + lsum;
+      m_run = m_use;
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&sm.p_full[s]);
