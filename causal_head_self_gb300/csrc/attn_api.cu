@@ -138,6 +138,7 @@ const char* attn_error_string(int code) {
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
     case ATTN_ERR_NO_MEMORY: return "ATTN_ERR_NO_MEMORY";
+    case ATTN_ERR_SCRATCH_LIMIT: return "ATTN_ERR_SCRATCH_LIMIT";
     default: return "ATTN_ERR_UNKNOWN";
   }
 }
@@ -229,3 +230,72 @@ int attn_status(cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// attn_decode_noalloc: the decode step for callers that must not allocate
+// device memory.  Its split partials and completion counters live in one
+// file-scope device array instead of the library's cudaMalloc'd workspace.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB per device
+
+// Held by every device that loads this library, until the process exits.
+// In host code this name is only a stand-in: the device address comes from
+// cudaGetSymbolAddress, taken once per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                                   const int* seqlens, void* o, int B, int Hq, int Hkv, int Tmax,
+                                   int Dh, int window, float scale, cudaStream_t stream) {
+  if (B < 0 || Tmax < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
+  if (window < 0) window = 0;
+  float scale_log2 = 0.f;
+  if (!resolve_scale(scale, Dh, &scale_log2)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0) return ATTN_OK;
+  if (!q || !kcache || !vcache || !seqlens || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t qo_bytes = (size_t)B * Hq * Dh * 2;
+  const size_t kv_bytes = (size_t)B * Hkv * Tmax * Dh * 2;
+  if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, kcache, kv_bytes) ||
+      overlaps(o, qo_bytes, vcache, kv_bytes) || overlaps(o, qo_bytes, seqlens, (size_t)B * 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (B > 65535) return ATTN_ERR_INVALID_ARG;   // grid.z
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != ATTN_OK) return rc;
+  const chs::DecodePlan plan = chs::plan_decode(B, Hq, Hkv, Tmax, Dh, st->info.num_sms);
+  if ((long long)Hkv * ((Hq / Hkv) / plan.heads_per_cta) > 65535) return ATTN_ERR_INVALID_ARG;
+  // scratch layout: counters (256-byte aligned) | split partials
+  const size_t n_counters = chs::decode_counter_count(B, Hq, Hkv, plan);
+  const size_t counter_bytes = (n_counters * sizeof(int) + 255) / 256 * 256;
+  const size_t partial_bytes = chs::decode_partials_bytes(B, Hq, Dh, plan);
+  if (counter_bytes + partial_bytes > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH_LIMIT;
+  unsigned char* scratch = nullptr;
+  {
+    // set-up, once per device, with that device current
+    std::lock_guard<std::mutex> lock(g_mutex);
+    const int dev = st->info.device;
+    if (!g_noalloc_ptr[dev]) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+        return ATTN_ERR_CUDA;
+      g_noalloc_ptr[dev] = static_cast<unsigned char*>(ptr);
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  int* counters = reinterpret_cast<int*>(scratch);
+  // the array keeps the previous call's contents: the counters must start at zero
+  if (cudaMemsetAsync(counters, 0, n_counters * sizeof(int), stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  cudaError_t e = chs::launch_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, window,
+                                     scale_log2, plan, counters, scratch + counter_bytes, st->info,
+                                     stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}

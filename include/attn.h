@@ -52,7 +52,8 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2,  /* a head size other than 64 or 128 */
   ATTN_ERR_CUDA = 3,         /* a CUDA runtime or launch error */
   ATTN_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (reported by attn_status) */
-  ATTN_ERR_NO_MEMORY = 5     /* the decode workspace could not be allocated */
+  ATTN_ERR_NO_MEMORY = 5,    /* the decode workspace could not be allocated */
+  ATTN_ERR_SCRATCH_LIMIT = 6 /* attn_decode_noalloc: the call needs more than its fixed scratch */
 } attn_status_t;
 
 /*
@@ -96,6 +97,37 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq
 int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens,
                 void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window, float scale,
                 cudaStream_t stream);
+
+/*
+ * attn_decode_noalloc -- the same decode step as attn_decode (same arguments,
+ * same result up to rounding, same errors), for callers that must not
+ * allocate device memory.  The pages describe no such call; it exists for
+ * this library's users.  A serving runtime that reserves nearly all device
+ * memory up front for its own KV-cache pool, or a process that runs under a
+ * fixed device-memory budget, cannot let a library allocate behind its back:
+ * an allocation there can fail, and cudaMalloc / cudaFree also stall on the
+ * device.  attn_decode allocates its workspace on first use; this entry point
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Its scratch (split partials and completion counters) is one fixed
+ *     16 MiB device array inside this library.  Every GPU that loads the
+ *     library holds it until the process exits.
+ *   - A call needs 4*B*Hkv*(Hq/Hkv)/h bytes of counters (h = 4, 2 or 1
+ *     query heads per CTA, rounded up to 256 bytes) plus
+ *     B*Hq*nsplit*(Dh+2)*4 bytes of partials (each part rounded up to 256),
+ *     where nsplit is the split count attn_decode would use.  A call that
+ *     needs more than 16 MiB returns ATTN_ERR_SCRATCH_LIMIT before anything
+ *     runs.  (The B=16, Hq=32, Hkv=8, Tmax=32768, Dh=128 decode step needs
+ *     about 7.7 MB.)
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the previous call's
+ *     contents; each call clears the counters it uses (cudaMemsetAsync on
+ *     `stream`).  Calls that overlap on the GPU (on different streams with no
+ *     ordering between them) race on the array and give wrong results.
+ */
+int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                        const int* seqlens, void* o, int B, int Hq, int Hkv, int Tmax, int Dh,
+                        int window, float scale, cudaStream_t stream);
 
 /*
  * attn_status -- synchronise `stream`, then return (and clear) the current

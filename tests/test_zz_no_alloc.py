@@ -1,0 +1,58 @@
+"""attn_decode_noalloc: the decode step for callers that must not allocate
+device memory (a serving runtime that has reserved the device memory for its
+own KV-cache pool, or a process under a fixed device-memory budget).  Its
+scratch is a fixed device array inside the library instead of a cudaMalloc'd
+workspace, so its results are checked against attn_decode, through the C ABI,
+on two calls in a row (the second call finds the first call's contents in the
+shared array).  This file is collected last on purpose."""
+import ctypes
+
+import pytest
+import torch
+
+import causal_head_self_gb300 as chs
+from causal_head_self_gb300 import _binding
+from causal_head_self_gb300 import build as _build
+from causal_head_self_gb300 import inputs
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    _build.build()
+
+
+# (B, Hq, Hkv, Tmax, Dh, lmin, lmax, window): several splits per sequence
+CASES = [
+    (4, 32, 8, 4096, 128, 1000, 4096, 0),
+    (3, 8, 2, 2000, 64, 1, 2000, 300),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tmax,Dh,lmin,lmax,window", CASES)
+def test_noalloc_matches_decode_on_two_calls(B, Hq, Hkv, Tmax, Dh, lmin, lmax, window):
+    d = torch.device("cuda")
+    q, kc, vc, sl = (x.to(d) for x in inputs.decode_inputs(B, Hq, Hkv, Tmax, Dh, lmin, lmax,
+                                                             seed=77 + Dh))
+    ref = chs.attn_decode(q, kc, vc, sl, window=window)
+    assert chs.attn_status() == chs.ATTN_OK
+    ref = ref.float().cpu().numpy()
+    for _ in range(2):
+        o = chs.attn_decode_noalloc(q, kc, vc, sl, window=window)
+        assert chs.attn_status() == chs.ATTN_OK
+        assert_close(o.float().cpu().numpy(), ref, what="noalloc vs decode")
+
+
+def test_noalloc_rejects_a_call_beyond_its_scratch():
+    """B=256 sequences of a 32768-key cache need more than the 16 MiB scratch;
+    the call is refused before anything is launched (the pointers are never
+    dereferenced)."""
+    lib = _binding.load()
+    torch.cuda.init()
+    big = 1 << 40
+    rc = lib.attn_decode_noalloc(0x10000, big, 2 * big, 3 * big, 4 * big, 256, 32, 8, 32768, 128,
+                                 0, 0.0, None)
+    assert rc == chs.ATTN_ERR_SCRATCH_LIMIT
+    assert chs.error_string(rc) == "ATTN_ERR_SCRATCH_LIMIT"
