@@ -84,35 +84,66 @@ __device__ __forceinline__ void unpack_chunk(const uint4& w, float2 (&f)[4]) {
 }
 
 // Sum each of s[0..HPB) over the LPK lanes of a key group (aligned groups of
-// LPK consecutive lanes); every lane of the group ends with all HPB sums.
-// For four heads the first two rounds transpose (each lane passes on half of
-// its values and keeps half), so one head's sum is finished per lane with
-// 5 shuffles, then broadcast with 4 more.
+// LPK consecutive lanes), transposing as it goes: in each of the first
+// log2(HPB) rounds a lane passes on half of its values and keeps half, so a
+// lane ends holding the full sum of ONE head (2 + 1 shuffles for four heads,
+// then one per remaining round).  Returns that sum; key_group_owner() names
+// a lane of the group that holds head h.
 template <int HPB, int LPK>
-__device__ __forceinline__ void key_group_allreduce(float (&s)[HPB], int lane) {
-  if constexpr (HPB == 4 && LPK >= 4) {
+__device__ __forceinline__ float key_group_reduce_owned(const float (&s)[HPB], int lane) {
+  static_assert(HPB == 1 || HPB == 2 || HPB == 4, "heads per CTA");
+  static_assert(LPK >= HPB, "a key group must hold every head");
+  float k;
+  int first_plain;   // first offset of the plain (non-transposing) rounds
+  if constexpr (HPB == 4) {
     constexpr int o1 = LPK / 2, o2 = LPK / 4;
     const bool up1 = (lane & o1) != 0, up2 = (lane & o2) != 0;
     float k0 = up1 ? s[2] : s[0], k1 = up1 ? s[3] : s[1];
     const float x0 = up1 ? s[0] : s[2], x1 = up1 ? s[1] : s[3];
     k0 += __shfl_xor_sync(0xffffffffu, x0, o1);
     k1 += __shfl_xor_sync(0xffffffffu, x1, o1);
-    float k = up2 ? k1 : k0;
+    k = up2 ? k1 : k0;
     const float x = up2 ? k0 : k1;
     k += __shfl_xor_sync(0xffffffffu, x, o2);
-#pragma unroll
-    for (int off = LPK / 8; off >= 1; off /= 2) k += __shfl_xor_sync(0xffffffffu, k, off);
-    // this lane now holds head (2*up1 + up2); fetch every head from its holder
-    const int base = lane & ~(LPK - 1);
-#pragma unroll
-    for (int h = 0; h < 4; ++h)
-      s[h] = __shfl_sync(0xffffffffu, k, base + (h >> 1) * o1 + (h & 1) * o2);
+    first_plain = LPK / 8;
+  } else if constexpr (HPB == 2) {
+    constexpr int o1 = LPK / 2;
+    const bool up1 = (lane & o1) != 0;
+    k = up1 ? s[1] : s[0];
+    const float x = up1 ? s[0] : s[1];
+    k += __shfl_xor_sync(0xffffffffu, x, o1);
+    first_plain = LPK / 4;
   } else {
-#pragma unroll
-    for (int off = LPK / 2; off >= 1; off /= 2)
-#pragma unroll
-      for (int h = 0; h < HPB; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
+    k = s[0];
+    first_plain = LPK / 2;
   }
+#pragma unroll
+  for (int off = LPK / 2; off >= 1; off /= 2)
+    if (off <= first_plain) k += __shfl_xor_sync(0xffffffffu, k, off);
+  return k;
+}
+
+// Head whose sum key_group_reduce_owned leaves in `lane`.
+template <int HPB, int LPK>
+__device__ __forceinline__ int key_group_owned_head(int lane) {
+  if constexpr (HPB == 4)
+    return 2 * ((lane & (LPK / 2)) != 0) + ((lane & (LPK / 4)) != 0);
+  else if constexpr (HPB == 2)
+    return (lane & (LPK / 2)) != 0;
+  else
+    return 0;
+}
+
+// A lane of `lane`'s key group that holds head h after key_group_reduce_owned.
+template <int HPB, int LPK>
+__device__ __forceinline__ int key_group_owner(int h, int lane) {
+  const int base = lane & ~(LPK - 1);
+  if constexpr (HPB == 4)
+    return base + (h >> 1) * (LPK / 2) + (h & 1) * (LPK / 4);
+  else if constexpr (HPB == 2)
+    return base + h * (LPK / 2);
+  else
+    return base;
 }
 
 template <int DH, int HPB>
@@ -193,7 +224,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     // ------------------------------------------------------------ consumers
     const int kslot = lane / LPK, part = lane % LPK;
     float2 q2[HPB][4], acc[HPB][4];
-    float m[HPB], l[HPB];
 #pragma unroll
     for (int h = 0; h < HPB; ++h) {
       const uint4 w =
@@ -205,62 +235,85 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
         q2[h][i] = __fmul2_rn(q2[h][i], sc);
         acc[h][i] = make_float2(0.f, 0.f);
       }
-      m[h] = -INFINITY;
-      l[h] = 0.f;
     }
+    // Online-softmax state of the one head whose score this lane finishes in
+    // the reduction (every lane of a key slot holding that head agrees).  The
+    // running max is raised lazily: only when a score exceeds it by more than
+    // 8 (weights then stay <= 2^8), which after the first key is rare, so the
+    // rescale of the accumulators sits in a warp-uniform branch.
+    float m_own = -INFINITY, l_own = 0.f;
+    const int lane_off = (warp * KPW + kslot) * ROW + part * 16;   // this lane's chunk
+
+    // one warp step: KPS keys, one per key slot
+    auto step = [&](const uint8_t* kp, const uint8_t* vp, bool valid) {
+      uint4 kw = make_uint4(0, 0, 0, 0), vw = kw;
+      if (valid) {
+        kw = *reinterpret_cast<const uint4*>(kp);
+        vw = *reinterpret_cast<const uint4*>(vp);
+      }
+      float2 k2[4];
+      unpack_chunk(kw, k2);
+      float s[HPB];
+#pragma unroll
+      for (int h = 0; h < HPB; ++h) {
+        float2 d = __fmul2_rn(q2[h][0], k2[0]);
+#pragma unroll
+        for (int i = 1; i < 4; ++i) d = __ffma2_rn(q2[h][i], k2[i], d);
+        s[h] = d.x + d.y;
+      }
+      const float s_own = key_group_reduce_owned<HPB, LPK>(s, lane);
+      const bool grow = valid && s_own > m_own + 8.0f;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float corr = grow ? ex2_approx(m_own - s_own) : 1.0f;   // 0 for the first key
+        if (grow) m_own = s_own;
+        l_own *= corr;
+#pragma unroll
+        for (int h = 0; h < HPB; ++h) {
+          const float c = __shfl_sync(0xffffffffu, corr, key_group_owner<HPB, LPK>(h, lane));
+          const float2 c2 = make_float2(c, c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[h][i] = __fmul2_rn(acc[h][i], c2);
+        }
+      }
+      const float p_own = valid ? ex2_approx(s_own - m_own) : 0.f;
+      l_own += p_own;
+      float2 v2[4];
+      unpack_chunk(vw, v2);
+#pragma unroll
+      for (int h = 0; h < HPB; ++h) {
+        const float pw = __shfl_sync(0xffffffffu, p_own, key_group_owner<HPB, LPK>(h, lane));
+        const float2 p2 = make_float2(pw, pw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[h][i] = __ffma2_rn(p2, v2[i], acc[h][i]);
+      }
+    };
 
     uint32_t st = 0, ph = 0;
     for (int blk = 0; blk < nblk; ++blk) {
       if (!mbar_wait(&sm.full[st], ph, abort)) break;
       const int n = min(kDecodeBlockKeys, nkeys - blk * kDecodeBlockKeys);
-      const uint8_t* kb = reinterpret_cast<const uint8_t*>(sm.k[st]);
-      const uint8_t* vb = reinterpret_cast<const uint8_t*>(sm.v[st]);
+      const uint8_t* kp = reinterpret_cast<const uint8_t*>(sm.k[st]) + lane_off;
+      const uint8_t* vp = reinterpret_cast<const uint8_t*>(sm.v[st]) + lane_off;
+      if (n == kDecodeBlockKeys) {
 #pragma unroll
-      for (int step = 0; step < KPW / KPS; ++step) {
-        const int key = warp * KPW + step * KPS + kslot;
-        const bool valid = key < n;
-        uint4 kw = make_uint4(0, 0, 0, 0), vw = kw;
-        if (valid) {
-          kw = *reinterpret_cast<const uint4*>(kb + key * ROW + part * 16);
-          vw = *reinterpret_cast<const uint4*>(vb + key * ROW + part * 16);
-        }
-        float2 k2[4];
-        unpack_chunk(kw, k2);
-        float s[HPB];
+        for (int j = 0; j < KPW / KPS; ++j) step(kp + j * KPS * ROW, vp + j * KPS * ROW, true);
+      } else {
 #pragma unroll
-        for (int h = 0; h < HPB; ++h) {
-          float2 d = __fmul2_rn(q2[h][0], k2[0]);
-#pragma unroll
-          for (int i = 1; i < 4; ++i) d = __ffma2_rn(q2[h][i], k2[i], d);
-          s[h] = d.x + d.y;
-        }
-        key_group_allreduce<HPB, LPK>(s, lane);
-        if (valid) {
-          float2 v2[4];
-          unpack_chunk(vw, v2);
-#pragma unroll
-          for (int h = 0; h < HPB; ++h) {
-            if (s[h] > m[h]) {   // the running max grows: rescale this slot's state
-              const float corr = ex2_approx(m[h] - s[h]);
-              const float2 c2 = make_float2(corr, corr);
-              l[h] *= corr;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) acc[h][i] = __fmul2_rn(acc[h][i], c2);
-              m[h] = s[h];
-            }
-            const float pw = ex2_approx(s[h] - m[h]);
-            const float2 p2 = make_float2(pw, pw);
-            l[h] += pw;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[h][i] = __ffma2_rn(p2, v2[i], acc[h][i]);
-          }
-        }
+        for (int j = 0; j < KPW / KPS; ++j)
+          step(kp + j * KPS * ROW, vp + j * KPS * ROW, warp * KPW + j * KPS + kslot < n);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[st]);
       if (++st == kDecodeStages) { st = 0; ph ^= 1; }
     }
 
+    // every lane of a key slot gets all heads' running max and sum
+    float m[HPB], l[HPB];
+#pragma unroll
+    for (int h = 0; h < HPB; ++h) {
+      m[h] = __shfl_sync(0xffffffffu, m_own, key_group_owner<HPB, LPK>(h, lane));
+      l[h] = __shfl_sync(0xffffffffu, l_own, key_group_owner<HPB, LPK>(h, lane));
+    }
     // merge the key slots of this warp (lanes with equal `part`)
 #pragma unroll
     for (int h = 0; h < HPB; ++h) {
