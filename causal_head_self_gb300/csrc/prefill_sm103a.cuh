@@ -13,13 +13,19 @@
 //
 // One CTA owns 256 query rows of one (b, h): two 128-row sub-tiles that take
 // turns on the tensor core, so that the softmax of one overlaps the MMAs of
-// the other.  Roles (320 threads):
+// the other.  Roles (352 threads):
 //   warps 0-3  softmax + epilogue of sub-tile 0 (thread t owns row t, TMEM lane t)
 //   warps 4-7  softmax + epilogue of sub-tile 1
-//   warp  8    TMEM allocation; one thread issues every tcgen05.mma
+//   warp  8    TMEM allocation; one thread issues the MMAs of sub-tile 0
 //   warp  9    one thread issues every TMA load (Q once, then K/V tiles)
+//   warp  10   one thread issues the MMAs of sub-tile 1
+// A tcgen05.mma is accepted only about as fast as the tensor core executes
+// it, so time an issuing thread spends waiting on a barrier is tensor time
+// lost.  Two issuers, each owning one sub-tile's chain S(j) -> softmax ->
+// P.V(j) -> S(j+1), keep the tensor core fed while either waits; in-order
+// issue within a thread keeps S(j+1) from overwriting P(j) too early.
 // With three warps on some SM sub-partitions, 168 registers per thread is the
-// most a 10-warp CTA gets; the softmax keeps a 128-score row plus a few
+// most an 11-warp CTA gets; the softmax keeps a 128-score row plus a few
 // running values live within that.
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DH),
 // O1 [384,384+DH).  P (bf16) is written over the first 64 columns of its S
@@ -47,9 +53,12 @@ struct PrefillCfg {
   static constexpr int kHalves = DH / 64;            // 128-byte swizzle boxes across DH
   static constexpr int kBoxBytes = 128 * 64 * 2;     // one 128 x 64 bf16 box
   static constexpr int kTileBytes = kHalves * kBoxBytes;
-  static constexpr int kStagesK = DH == 128 ? 2 : 4;
+  static constexpr int kStagesK = DH == 128 ? 3 : 4;
   static constexpr int kStagesV = DH == 128 ? 2 : 4;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
+  static constexpr int kWarpProducer = 9;
+  // warp issuing the MMAs of sub-tile s: 8 + 2 s (different sub-partitions)
+  static constexpr int kWarpIssuer0 = 8, kWarpIssuer1 = 10;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 };
 
@@ -62,9 +71,10 @@ struct __align__(1024) PrefillSmem {
   uint64_t q_full;
   uint64_t k_full[Cfg::kStagesK], k_empty[Cfg::kStagesK];
   uint64_t v_full[Cfg::kStagesV], v_empty[Cfg::kStagesV];
-  uint64_t s_full[2], p_full[2], o_final[2], mma_done;
+  uint64_t s_full[2], p_full[2], o_final[2], mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
+  int s0_issued;   // tiles whose S0 MMAs issuer 0 has issued (orders S1 after S0)
 };
 
 // Geometry of one CTA's work item.
@@ -106,6 +116,20 @@ __device__ __forceinline__ PrefillTile prefill_tile_of(const PrefillParams& p, i
   return t;
 }
 
+// Spin (bounded, abort-aware) until *p >= v; returns false on abort/timeout.
+__device__ __forceinline__ bool spin_until_ge(volatile int* p, int v, volatile int* abort) {
+  if (*p >= v) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (*p < v) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
 // Drain wait used at teardown: ignores the abort flag, bounded by time.
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -116,7 +140,7 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 }
 
 template <int DH>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     attn_prefill_sm103a(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v,
@@ -143,15 +167,18 @@ __global__ void __launch_bounds__(320, 1)
   // ---- setup
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
+    sm.s0_issued = 0;
     mbar_init(&sm.q_full, 1);
-    for (int i = 0; i < Cfg::kStagesK; ++i) { mbar_init(&sm.k_full[i], 1); mbar_init(&sm.k_empty[i], 1); }
-    for (int i = 0; i < Cfg::kStagesV; ++i) { mbar_init(&sm.v_full[i], 1); mbar_init(&sm.v_empty[i], 1); }
+    // a K/V stage is free once both issuers' MMAs reading it are done
+    for (int i = 0; i < Cfg::kStagesK; ++i) { mbar_init(&sm.k_full[i], 1); mbar_init(&sm.k_empty[i], 2); }
+    for (int i = 0; i < Cfg::kStagesV; ++i) { mbar_init(&sm.v_full[i], 1); mbar_init(&sm.v_empty[i], 2); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.p_full[s], 128);
       mbar_init(&sm.o_final[s], 1);
     }
-    mbar_init(&sm.mma_done, 1);
+    mbar_init(&sm.mma_done[0], 1);
+    mbar_init(&sm.mma_done[1], 1);
     fence_mbarrier_init();
   }
   if (warp == 8) {
@@ -163,7 +190,7 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after_sync();
   const uint32_t tbase = sm.tmem_base;
 
-  if (warp == 9) {
+  if (warp == Cfg::kWarpProducer) {
     // =================================================================== TMA producer
     if (lane == 0) {
       prefetch_tensormap(&map_q);
@@ -204,102 +231,81 @@ __global__ void __launch_bounds__(320, 1)
       for (int i = 0; i < Cfg::kStagesV; ++i)
         if (v_loaded & (1u << i)) mbar_wait_drain(&sm.v_full[i], (v_par >> i) & 1u);
     }
-  } else if (warp == 8) {
-    // =================================================================== MMA issuer
+  } else if (warp == Cfg::kWarpIssuer0 || warp == Cfg::kWarpIssuer1) {
+    // =================================================================== MMA issuers
+    const int s = warp == Cfg::kWarpIssuer0 ? 0 : 1;   // this issuer's sub-tile
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, DH, false, true);
-      // S_s = Q_s K^T: K-major operands, 16 columns (32 bytes) of DH per MMA
-      auto issue_qk = [&](int s, int kst) {
-        const uint32_t d = tbase + (s ? Cfg::kColS1 : Cfg::kColS0);
-        const uint32_t qa = smem_u32(sm.q[s]), ka = smem_u32(sm.k[kst]);
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-          mma_bf16_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                      idesc_qk, kk > 0);
-        }
-      };
-      // O_s (+)= P_s V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
-      auto issue_pv = [&](int s, int vst, bool acc) {
-        const uint32_t d = tbase + (s ? Cfg::kColO1 : Cfg::kColO0);
-        const uint32_t a = tbase + (s ? Cfg::kColS1 : Cfg::kColS0);
-        const uint32_t va = smem_u32(sm.v[vst]);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(d, a + kk * 8, smem_desc_sw128(va + kk * 2048, Cfg::kBoxBytes, 1024),
-                      idesc_pv, (acc || kk > 0) ? 1u : 0u);
-      };
-      int n_active[2] = {0, 0};
-      uint32_t kst = 0, kph = 0, vst = 0, vph = 0, pph0 = 0, pph1 = 0;
-      bool pend1 = false, pend_ready = false;
-      uint32_t pend_vst = 0, pend_vph = 0;
+      // Descriptors are a fixed template OR'ed with (address >> 4); every
+      // operand slice used below is that plus a compile-time offset, so an
+      // MMA costs one 64-bit add and the issue itself.  Shared-memory
+      // addresses stay below 2^18, so the offsets never carry out of the
+      // 14-bit address field.
+      constexpr uint64_t kKmajor = smem_desc_sw128(0, 16, 1024);                // Q, K
+      constexpr uint64_t kMnMajor = smem_desc_sw128(0, Cfg::kBoxBytes, 1024);   // V
+      const uint64_t dq = kKmajor | (smem_u32(sm.q[s]) >> 4);
+      const uint64_t dk = kKmajor | (smem_u32(sm.k[0]) >> 4);
+      const uint64_t dv = kMnMajor | (smem_u32(sm.v[0]) >> 4);
+      const uint32_t dS = tbase + (s ? Cfg::kColS1 : Cfg::kColS0);
+      const uint32_t dO = tbase + (s ? Cfg::kColO1 : Cfg::kColO0);
+      int n_active = 0;
+      uint32_t pph = 0;
       bool ok = mbar_wait(&sm.q_full, 0, abort);
       tc_fence_after_sync();
       for (int j = tile.lo; ok && j <= tile.hi; ++j) {
-        const bool a0 = tile.active(0, j), a1 = tile.active(1, j);
+        const uint32_t i = (uint32_t)(j - tile.lo);
+        const uint32_t kst = i % Cfg::kStagesK, kph = (i / Cfg::kStagesK) & 1u;
+        const uint32_t vst = i % Cfg::kStagesV, vph = (i / Cfg::kStagesV) & 1u;
+        const bool act = tile.active(s, j);
+        // every issuer waits for every tile before releasing it, so neither
+        // can run a whole ring ahead of the other
         if (!(ok = mbar_wait(&sm.k_full[kst], kph, abort))) break;
         tc_fence_after_sync();
-        if (a0) {
-          issue_qk(0, kst);
-          mma_commit(&sm.s_full[0]);
-        }
-        if (pend1) {   // P.V of sub-tile 1 for the previous tile
-          if (!(ok = mbar_wait(&sm.p_full[1], pph1, abort))) break;
-          pph1 ^= 1;
-          if (!pend_ready && !(ok = mbar_wait(&sm.v_full[pend_vst], pend_vph, abort))) break;
-          tc_fence_after_sync();
-          issue_pv(1, pend_vst, n_active[1] > 0);
-          ++n_active[1];
-          mma_commit(&sm.v_empty[pend_vst]);
-          pend1 = false;
-        }
-        if (a1) {
-          issue_qk(1, kst);
-          mma_commit(&sm.s_full[1]);
+        // Sub-tile 1 issues S(j) only after sub-tile 0 has issued its own, so
+        // the two S products run one after the other and the two softmaxes
+        // are staggered by one S time instead of competing in lockstep.
+        if (s == 1 && act && tile.active(0, j) &&
+            !(ok = spin_until_ge(&sm.s0_issued, (int)i + 1, abort)))
+          break;
+        if (act) {
+          // S_s = Q_s K^T: K-major operands, 16 columns (32 bytes) of DH per MMA
+          const uint64_t b = dk + (uint64_t)(kst * (Cfg::kTileBytes >> 4));
+          mma_bf16_ss(dS, dq, b, idesc_qk, 0u);
+#pragma unroll
+          for (int kk = 1; kk < DH / 16; ++kk) {
+            const uint32_t off = ((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4;
+            mma_bf16_ss(dS, dq + off, b + off, idesc_qk, 1u);
+          }
+          mma_commit(&sm.s_full[s]);
+          if (s == 0) {
+            __threadfence_block();
+            *reinterpret_cast<volatile int*>(&sm.s0_issued) = (int)i + 1;
+          }
         }
         mma_commit(&sm.k_empty[kst]);
-        if (++kst == Cfg::kStagesK) { kst = 0; kph ^= 1; }
-        bool vready = false;
-        if (a0) {
-          if (!(ok = mbar_wait(&sm.p_full[0], pph0, abort))) break;
-          pph0 ^= 1;
-          if (!(ok = mbar_wait(&sm.v_full[vst], vph, abort))) break;
-          vready = true;
-          tc_fence_after_sync();
-          issue_pv(0, vst, n_active[0] > 0);
-          ++n_active[0];
+        if (act) {
+          if (!(ok = mbar_wait(&sm.p_full[s], pph, abort))) break;
+          pph ^= 1;
         }
-        if (a1) {
-          pend1 = true;
-          pend_vst = vst;
-          pend_vph = vph;
-          pend_ready = vready;
-        } else {
-          if (!vready && !(ok = mbar_wait(&sm.v_full[vst], vph, abort))) break;
-          mma_commit(&sm.v_empty[vst]);
+        if (!(ok = mbar_wait(&sm.v_full[vst], vph, abort))) break;
+        tc_fence_after_sync();
+        if (act) {
+          // O_s (+)= P_s V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
+          const uint64_t b = dv + (uint64_t)(vst * (Cfg::kTileBytes >> 4));
+          mma_bf16_ts(dO, dS, b, idesc_pv, n_active > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 1; kk < 8; ++kk) mma_bf16_ts(dO, dS + kk * 8, b + kk * (2048 >> 4), idesc_pv, 1u);
+          ++n_active;
         }
-        if (++vst == Cfg::kStagesV) { vst = 0; vph ^= 1; }
+        mma_commit(&sm.v_empty[vst]);
       }
-      if (ok && pend1) {
-        ok = mbar_wait(&sm.p_full[1], pph1, abort);
-        if (ok && !pend_ready) ok = mbar_wait(&sm.v_full[pend_vst], pend_vph, abort);
-        if (ok) {
-          tc_fence_after_sync();
-          issue_pv(1, pend_vst, n_active[1] > 0);
-          ++n_active[1];
-          mma_commit(&sm.v_empty[pend_vst]);
-        }
-      }
-      if (ok) {
-        if (n_active[0] > 0) mma_commit(&sm.o_final[0]);
-        if (n_active[1] > 0) mma_commit(&sm.o_final[1]);
-      }
-      // nothing may still be running on the tensor core at teardown
-      mma_commit(&sm.mma_done);
-      mbar_wait_drain(&sm.mma_done, 0);
+      if (ok && n_active > 0) mma_commit(&sm.o_final[s]);
+      // nothing of this thread's may still run on the tensor core at teardown
+      mma_commit(&sm.mma_done[s]);
+      mbar_wait_drain(&sm.mma_done[s], 0);
     }
-  } else {
+  } else if (warp < 8) {
     // =================================================================== softmax + epilogue
     const int s = warp / 4;                 // sub-tile
     const int wl = warp % 4;                // warp within the warpgroup = TMEM lane quarter
@@ -320,15 +326,17 @@ __global__ void __launch_bounds__(320, 1)
       sph ^= 1;
       tc_fence_after_sync();
 
+      // scores, with each 32-column chunk's maximum from the load itself
       uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld_32x32b_x32(colS + 0, r0);
-      tmem_ld_32x32b_x32(colS + 32, r1);
-      tmem_ld_32x32b_x32(colS + 64, r2);
-      tmem_ld_32x32b_x32(colS + 96, r3);
-      tmem_ld_wait(r0);
-      tmem_ld_wait(r1);
-      tmem_ld_wait(r2);
-      tmem_ld_wait(r3);
+      float mc0, mc1, mc2, mc3;
+      tmem_ld_max_32x32b_x32(colS + 0, r0, mc0);
+      tmem_ld_max_32x32b_x32(colS + 32, r1, mc1);
+      tmem_ld_max_32x32b_x32(colS + 64, r2, mc2);
+      tmem_ld_max_32x32b_x32(colS + 96, r3, mc3);
+      tmem_ld_wait(r0, mc0);
+      tmem_ld_wait(r1, mc1);
+      tmem_ld_wait(r2, mc2);
+      tmem_ld_wait(r3, mc3);
       float x[128];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
@@ -337,8 +345,10 @@ __global__ void __launch_bounds__(320, 1)
         x[64 + c] = __uint_as_float(r2[c]);
         x[96 + c] = __uint_as_float(r3[c]);
       }
+      float mt = fmaxf(fmaxf(mc0, mc1), fmaxf(mc2, mc3));
       if (tile.needs_mask(s, j)) {
-        // visible keys of this row: [klo, khi] (absolute), as column offsets
+        // visible keys of this row: [klo, khi] (absolute), as column offsets;
+        // the maximum is retaken over the visible keys only
         const int kv0 = 128 * j;
         int khi = tile.S - 1;
         if (tile.causal) khi = min(khi, row);
@@ -347,18 +357,17 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c < clo || c > chi) x[c] = -INFINITY;
+        float mx[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = fmax3(x[i], x[4 + i], x[8 + i]);
+#pragma unroll
+        for (int c = 12; c < 124; c += 8)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], x[c + i], x[c + 4 + i]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], x[124 + i]);
+        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       }
-      // row maximum as four independent chains of three-input max
-      float mx[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = fmax3(x[i], x[4 + i], x[8 + i]);
-#pragma unroll
-      for (int c = 12; c < 124; c += 8)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], x[c + i], x[c + 4 + i]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], x[124 + i]);
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float m_tile = mt * sl2;
       // lazy rescale: keep the old maximum unless the new one exceeds it by
       // more than 8 (weights stay <= 2^8); the result is exact either way
@@ -370,20 +379,23 @@ __global__ void __launch_bounds__(320, 1)
       const float msub = (m_use == -INFINITY) ? 0.f : m_use;
       // P = exp2(x - m) as bf16 over the first 64 columns of S (the scores
       // die here, before O is touched, to keep register pressure down)
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};   // independent partial sums
+      // (pairs of columns go through packed f32x2 arithmetic)
+      const float2 scale2 = make_float2(sl2, sl2), neg_m2 = make_float2(-msub, -msub);
+      float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // four partial sums
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(x[32 * c4 + 2 * e], sl2, -msub));
-          const float p1 = ex2_approx(fmaf(x[32 * c4 + 2 * e + 1], sl2, -msub));
-          ls[e & 3] += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          const float2 xs = __ffma2_rn(make_float2(x[32 * c4 + 2 * e], x[32 * c4 + 2 * e + 1]),
+                                       scale2, neg_m2);
+          const float2 pp = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
+          ls[e & 1].x += pp.x; ls[e & 1].y += pp.y;
+          pk[e] = pack_bf16x2(pp.x, pp.y);
         }
         tmem_st_32x32b_x16(colS + 16 * c4, pk);
       }
-      const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      const float lsum = (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
       // a raised maximum rescales this row's O (all earlier P.V are done:
       // the S MMA just waited for was issued after them)
       if (__any_sync(0xffffffffu, corr != 1.0f)) {
