@@ -74,7 +74,7 @@ struct __align__(1024) PrefillSmem {
   uint64_t s_full[2], p_full[2], o_final[2], mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
-  int s0_issued;   // tiles whose S0 MMAs issuer 0 has issued (orders S1 after S0)
+  int groups_done[2];   // MMA groups each issuer has issued (orders the two issuers)
 };
 
 // Geometry of one CTA's work item.
@@ -139,6 +139,101 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
+// One MMA issuer: the chain of sub-tile S (0 or 1), run by a whole warp that
+// stays converged; one elected lane issues each tcgen05 instruction.  All it
+// computes descends from compile-time constants, the CTA's shared-memory base
+// and loop counters, so descriptors and tensor-memory addresses stay in
+// uniform registers: a tcgen05.mma is accepted only about as fast as the
+// tensor core runs it, so every instruction between two of them is a bubble.
+// Wait results are made warp-uniform so the warp never diverges.
+template <int DH, int S>
+__device__ __forceinline__ void prefill_issuer(PrefillSmem<DH>& sm, const PrefillTile& tile,
+                                               volatile int* abort, int lane) {
+  using Cfg = PrefillCfg<DH>;
+  constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t idesc_pv = idesc_bf16_f32(128, DH, false, true);
+  // Descriptors are a fixed template OR'ed with (address >> 4); every
+  // operand slice used below is that plus a compile-time offset, so an MMA
+  // costs one 64-bit add and the issue itself.  Shared-memory addresses stay
+  // below 2^18, so the offsets never carry out of the 14-bit address field.
+  constexpr uint64_t kKmajor = smem_desc_sw128(0, 16, 1024);                // Q, K
+  constexpr uint64_t kMnMajor = smem_desc_sw128(0, Cfg::kBoxBytes, 1024);   // V
+  const uint64_t dq = kKmajor | (smem_u32(sm.q[S]) >> 4);
+  const uint64_t dk = kKmajor | (smem_u32(sm.k[0]) >> 4);
+  const uint64_t dv = kMnMajor | (smem_u32(sm.v[0]) >> 4);
+  // the CTA owns all 512 columns, so its allocation starts at column 0
+  constexpr uint32_t dS = S ? Cfg::kColS1 : Cfg::kColS0;
+  constexpr uint32_t dO = S ? Cfg::kColO1 : Cfg::kColO0;
+  // The work of each issuer is a sequence of groups: group g holds its P.V
+  // of tile lo+g-1 and its S of tile lo+g.  The tensor core runs
+  //   S0(lo) | PV1(-) S1(lo) | PV0(lo) S0(lo+1) | PV1(lo) S1(lo+1) | ...
+  // i.e. group g of sub-tile 0, then group g of sub-tile 1, then group g+1
+  // of sub-tile 0: each softmax runs while the other sub-tile's two MMA
+  // groups keep the tensor core busy.  An issuer first waits for everything
+  // of its own (P, V, K), then for the other issuer's previous group (a
+  // counter in shared memory), so the tensor core idles only for that
+  // handover.
+  volatile int* mine = &sm.groups_done[S];
+  volatile int* other = &sm.groups_done[1 - S];
+  const int n_tiles = tile.hi - tile.lo + 1;
+  int n_active = 0;
+  uint32_t pph = 0;
+  bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0, abort));
+  tc_fence_after_sync();
+  for (int g = 0; ok && g <= n_tiles; ++g) {
+    const bool do_pv = g >= 1 && tile.active(S, tile.lo + g - 1);
+    const bool do_s = g < n_tiles && tile.active(S, tile.lo + g);
+    const uint32_t vi = (uint32_t)(g - 1), ki = (uint32_t)g;
+    const uint32_t vst = vi % Cfg::kStagesV, vph = (vi / Cfg::kStagesV) & 1u;
+    const uint32_t kst = ki % Cfg::kStagesK, kph = (ki / Cfg::kStagesK) & 1u;
+    if (do_pv) {
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_full[S], pph, abort)))) break;
+      pph ^= 1;
+    }
+    // every issuer waits for every tile before releasing it, so neither can
+    // run a whole ring ahead of the other
+    if (g >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[vst], vph, abort))))
+      break;
+    if (g < n_tiles && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[kst], kph, abort))))
+      break;
+    // sub-tile 0 waits for sub-tile 1's group g-1, sub-tile 1 for sub-tile 0's group g
+    if (!(ok = __all_sync(0xffffffffu, spin_until_ge(other, S ? g + 1 : g, abort)))) break;
+    tc_fence_after_sync();
+    if (g >= 1) {   // P.V of the previous tile
+      if (do_pv) {
+        // O_s (+)= P_s V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
+        const uint64_t b = dv + (uint64_t)(vst * (Cfg::kTileBytes >> 4));
+        mma_bf16_ts_warp(dO, dS, b, idesc_pv, n_active > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 1; kk < 8; ++kk) mma_bf16_ts_warp(dO, dS + kk * 8, b + kk * (2048 >> 4), idesc_pv, 1u);
+        ++n_active;
+      }
+      mma_commit_warp(&sm.v_empty[vst]);
+    }
+    if (g < n_tiles) {   // S of this tile
+      if (do_s) {
+        // S_s = Q_s K^T: K-major operands, 16 columns (32 bytes) of DH per MMA
+        const uint64_t b = dk + (uint64_t)(kst * (Cfg::kTileBytes >> 4));
+        mma_bf16_ss_warp(dS, dq, b, idesc_qk, 0u);
+#pragma unroll
+        for (int kk = 1; kk < DH / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4;
+          mma_bf16_ss_warp(dS, dq + off, b + off, idesc_qk, 1u);
+        }
+        mma_commit_warp(&sm.s_full[S]);
+      }
+      mma_commit_warp(&sm.k_empty[kst]);
+    }
+    __threadfence_block();
+    if (lane == 0) *mine = g + 1;
+    __syncwarp();
+  }
+  if (ok && n_active > 0) mma_commit_warp(&sm.o_final[S]);
+  // nothing of this thread's may still run on the tensor core at teardown
+  mma_commit_warp(&sm.mma_done[S]);
+  mbar_wait_drain(&sm.mma_done[S], 0);
+}
+
 template <int DH>
 __global__ void __launch_bounds__(352, 1)
     attn_prefill_sm103a(const __grid_constant__ CUtensorMap map_q,
@@ -167,7 +262,8 @@ __global__ void __launch_bounds__(352, 1)
   // ---- setup
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
-    sm.s0_issued = 0;
+    sm.groups_done[0] = 0;
+    sm.groups_done[1] = 0;
     mbar_init(&sm.q_full, 1);
     // a K/V stage is free once both issuers' MMAs reading it are done
     for (int i = 0; i < Cfg::kStagesK; ++i) { mbar_init(&sm.k_full[i], 1); mbar_init(&sm.k_empty[i], 2); }
@@ -189,6 +285,9 @@ __global__ void __launch_bounds__(352, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = sm.tmem_base;
+  // all 512 columns are this CTA's, so the allocation starts at column 0;
+  // the MMA issuers rely on that (compile-time tensor-memory addresses)
+  if (threadIdx.x == 0 && tbase != 0) sm.abort_flag = 1;
 
   if (warp == Cfg::kWarpProducer) {
     // =================================================================== TMA producer
@@ -233,78 +332,10 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else if (warp == Cfg::kWarpIssuer0 || warp == Cfg::kWarpIssuer1) {
     // =================================================================== MMA issuers
-    const int s = warp == Cfg::kWarpIssuer0 ? 0 : 1;   // this issuer's sub-tile
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, DH, false, true);
-      // Descriptors are a fixed template OR'ed with (address >> 4); every
-      // operand slice used below is that plus a compile-time offset, so an
-      // MMA costs one 64-bit add and the issue itself.  Shared-memory
-      // addresses stay below 2^18, so the offsets never carry out of the
-      // 14-bit address field.
-      constexpr uint64_t kKmajor = smem_desc_sw128(0, 16, 1024);                // Q, K
-      constexpr uint64_t kMnMajor = smem_desc_sw128(0, Cfg::kBoxBytes, 1024);   // V
-      const uint64_t dq = kKmajor | (smem_u32(sm.q[s]) >> 4);
-      const uint64_t dk = kKmajor | (smem_u32(sm.k[0]) >> 4);
-      const uint64_t dv = kMnMajor | (smem_u32(sm.v[0]) >> 4);
-      const uint32_t dS = tbase + (s ? Cfg::kColS1 : Cfg::kColS0);
-      const uint32_t dO = tbase + (s ? Cfg::kColO1 : Cfg::kColO0);
-      int n_active = 0;
-      uint32_t pph = 0;
-      bool ok = mbar_wait(&sm.q_full, 0, abort);
-      tc_fence_after_sync();
-      for (int j = tile.lo; ok && j <= tile.hi; ++j) {
-        const uint32_t i = (uint32_t)(j - tile.lo);
-        const uint32_t kst = i % Cfg::kStagesK, kph = (i / Cfg::kStagesK) & 1u;
-        const uint32_t vst = i % Cfg::kStagesV, vph = (i / Cfg::kStagesV) & 1u;
-        const bool act = tile.active(s, j);
-        // every issuer waits for every tile before releasing it, so neither
-        // can run a whole ring ahead of the other
-        if (!(ok = mbar_wait(&sm.k_full[kst], kph, abort))) break;
-        tc_fence_after_sync();
-        // Sub-tile 1 issues S(j) only after sub-tile 0 has issued its own, so
-        // the two S products run one after the other and the two softmaxes
-        // are staggered by one S time instead of competing in lockstep.
-        if (s == 1 && act && tile.active(0, j) &&
-            !(ok = spin_until_ge(&sm.s0_issued, (int)i + 1, abort)))
-          break;
-        if (act) {
-          // S_s = Q_s K^T: K-major operands, 16 columns (32 bytes) of DH per MMA
-          const uint64_t b = dk + (uint64_t)(kst * (Cfg::kTileBytes >> 4));
-          mma_bf16_ss(dS, dq, b, idesc_qk, 0u);
-#pragma unroll
-          for (int kk = 1; kk < DH / 16; ++kk) {
-            const uint32_t off = ((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4;
-            mma_bf16_ss(dS, dq + off, b + off, idesc_qk, 1u);
-          }
-          mma_commit(&sm.s_full[s]);
-          if (s == 0) {
-            __threadfence_block();
-            *reinterpret_cast<volatile int*>(&sm.s0_issued) = (int)i + 1;
-          }
-        }
-        mma_commit(&sm.k_empty[kst]);
-        if (act) {
-          if (!(ok = mbar_wait(&sm.p_full[s], pph, abort))) break;
-          pph ^= 1;
-        }
-        if (!(ok = mbar_wait(&sm.v_full[vst], vph, abort))) break;
-        tc_fence_after_sync();
-        if (act) {
-          // O_s (+)= P_s V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
-          const uint64_t b = dv + (uint64_t)(vst * (Cfg::kTileBytes >> 4));
-          mma_bf16_ts(dO, dS, b, idesc_pv, n_active > 0 ? 1u : 0u);
-#pragma unroll
-          for (int kk = 1; kk < 8; ++kk) mma_bf16_ts(dO, dS + kk * 8, b + kk * (2048 >> 4), idesc_pv, 1u);
-          ++n_active;
-        }
-        mma_commit(&sm.v_empty[vst]);
-      }
-      if (ok && n_active > 0) mma_commit(&sm.o_final[s]);
-      // nothing of this thread's may still run on the tensor core at teardown
-      mma_commit(&sm.mma_done[s]);
-      mbar_wait_drain(&sm.mma_done[s], 0);
-    }
+    if (warp == Cfg::kWarpIssuer0)
+      prefill_issuer<DH, 0>(sm, tile, abort, lane);
+    else
+      prefill_issuer<DH, 1>(sm, tile, abort, lane);
   } else if (warp < 8) {
     // =================================================================== softmax + epilogue
     const int s = warp / 4;                 // sub-tile
