@@ -186,18 +186,20 @@ __device__ __forceinline__ void prefill_issuer(PrefillSmem<DH>& sm, const Prefil
     const uint32_t vi = (uint32_t)(g - 1), ki = (uint32_t)g;
     const uint32_t vst = vi % Cfg::kStagesV, vph = (vi / Cfg::kStagesV) & 1u;
     const uint32_t kst = ki % Cfg::kStagesK, kph = (ki / Cfg::kStagesK) & 1u;
-    if (do_pv) {
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_full[S], pph, abort)))) break;
-      pph ^= 1;
-    }
-    // every issuer waits for every tile before releasing it, so neither can
-    // run a whole ring ahead of the other
+    // Waits ordered so that the one usually completing last (this
+    // sub-tile's P, i.e. its softmax) comes last and the MMAs follow it at
+    // once.  Every issuer waits for every tile before releasing it, so
+    // neither can run a whole ring ahead of the other.
     if (g >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[vst], vph, abort))))
       break;
     if (g < n_tiles && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[kst], kph, abort))))
       break;
     // sub-tile 0 waits for sub-tile 1's group g-1, sub-tile 1 for sub-tile 0's group g
     if (!(ok = __all_sync(0xffffffffu, spin_until_ge(other, S ? g + 1 : g, abort)))) break;
+    if (do_pv) {
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_full[S], pph, abort)))) break;
+      pph ^= 1;
+    }
     tc_fence_after_sync();
     if (g >= 1) {   // P.V of the previous tile
       if (do_pv) {
