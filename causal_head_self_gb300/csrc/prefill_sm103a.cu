@@ -6,27 +6,27 @@ namespace chs {
 
 template <int DH>
 static cudaError_t launch_prefill_dh(const CUtensorMap& mq, const CUtensorMap& mk,
-                                     const CUtensorMap& mv, const CUtensorMap& mo,
-                                     const PrefillParams& prm, cudaStream_t stream) {
+                                     const CUtensorMap& mv, const PrefillParams& prm,
+                                     int num_sms, cudaStream_t stream) {
   constexpr size_t smem = prefill_smem_bytes<DH>();
   static_assert(smem <= 232448, "shared memory budget of one sm_103a CTA");
   cudaError_t e = cudaFuncSetAttribute(attn_prefill_sm103a<DH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)prm.num_qblocks * prm.B * prm.Hq;
-  attn_prefill_sm103a<DH><<<(unsigned)grid, PrefillCfg<DH>::kThreads, smem, stream>>>(mq, mk, mv,
-                                                                                     mo, prm);
+  // persistent: one CTA per SM (the shared memory allows no second), each
+  // walking its share of the work items
+  const int grid = prm.num_items < num_sms ? prm.num_items : num_sms;
+  attn_prefill_sm103a<DH><<<grid, PrefillCfg<DH>::kThreads, smem, stream>>>(mq, mk, mv, prm);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
                            int Hkv, int S, int Dh, int causal, int window, float scale_log2,
                            const DeviceInfo& dev, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv;
   if (!encode_bf16_map(&mq, q, Dh, S, (long long)B * Hq, 128) ||
       !encode_bf16_map(&mk, k, Dh, S, (long long)B * Hkv, 128) ||
-      !encode_bf16_map(&mv, v, Dh, S, (long long)B * Hkv, 128) ||
-      !encode_bf16_map(&mo, o, Dh, S, (long long)B * Hq, 32))
+      !encode_bf16_map(&mv, v, Dh, S, (long long)B * Hkv, 128))
     return cudaErrorInvalidValue;
   PrefillParams prm;
   prm.B = B;
@@ -37,9 +37,13 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o,
   prm.window = window;
   prm.scale_log2 = scale_log2;
   prm.num_qblocks = (S + 255) / 256;
+  const long long items = (long long)prm.num_qblocks * B * Hq;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  prm.num_items = (int)items;
+  prm.o = static_cast<__nv_bfloat16*>(o);
   prm.error_word = dev.error_word;
-  return Dh == 128 ? launch_prefill_dh<128>(mq, mk, mv, mo, prm, stream)
-                   : launch_prefill_dh<64>(mq, mk, mv, mo, prm, stream);
+  return Dh == 128 ? launch_prefill_dh<128>(mq, mk, mv, prm, dev.num_sms, stream)
+                   : launch_prefill_dh<64>(mq, mk, mv, prm, dev.num_sms, stream);
 }
 
 }  // namespace chs

@@ -11,19 +11,23 @@
 // online softmax that "多头注意力机制" (blog.euler0525.cn), section "Flash
 // Attention", and the textbook's section "Эффективные реализации" describe).
 //
-// One CTA owns 256 query rows of one (b, h): two 128-row sub-tiles that take
-// turns on the tensor core, so that the softmax of one overlaps the MMAs of
-// the other.  Roles (352 threads):
+// The kernel is persistent: one CTA per SM walks a list of work items, each
+// 256 query rows of one (b, h): two 128-row sub-tiles that take turns on the
+// tensor core, so that the softmax of one overlaps the MMAs of the other.
+// Items are handed out heaviest first (causal work grows with the query
+// block) in "snake" order over the CTAs, and the TMA producer runs ahead
+// into the next item (its Q and K/V tiles) while the current one finishes.
+// Roles (352 threads):
 //   warps 0-3  softmax + epilogue of sub-tile 0 (thread t owns row t, TMEM lane t)
 //   warps 4-7  softmax + epilogue of sub-tile 1
-//   warp  8    TMEM allocation; one thread issues the MMAs of sub-tile 0
-//   warp  9    one thread issues every TMA load (Q once, then K/V tiles)
-//   warp  10   one thread issues the MMAs of sub-tile 1
+//   warp  8    TMEM allocation; issues the MMAs of sub-tile 0
+//   warp  9    one thread issues every TMA load (Q per item, then K/V tiles)
+//   warp  10   issues the MMAs of sub-tile 1
 // A tcgen05.mma is accepted only about as fast as the tensor core executes
 // it, so time an issuing thread spends waiting on a barrier is tensor time
 // lost.  Two issuers, each owning one sub-tile's chain S(j) -> softmax ->
-// P.V(j) -> S(j+1), keep the tensor core fed while either waits; in-order
-// issue within a thread keeps S(j+1) from overwriting P(j) too early.
+// P.V(j) -> S(j+1), alternate MMA groups; in-order issue within a thread
+// keeps S(j+1) from overwriting P(j) too early.
 // With three warps on some SM sub-partitions, 168 registers per thread is the
 // most an 11-warp CTA gets; the softmax keeps a 128-score row plus a few
 // running values live within that.
@@ -42,6 +46,8 @@ struct PrefillParams {
   int window;   // > 0: also only if i - j < window
   float scale_log2;   // softmax scale * log2(e)
   int num_qblocks;    // ceil(S / 256)
+  int num_items;      // work items: num_qblocks * B * Hq
+  __nv_bfloat16* o;   // output [B, Hq, S, DH]
   int* error_word;    // set to a nonzero status when a wait gives up
 };
 
@@ -65,10 +71,10 @@ struct PrefillCfg {
 template <int DH>
 struct __align__(1024) PrefillSmem {
   using Cfg = PrefillCfg<DH>;
-  uint8_t q[2][Cfg::kTileBytes];          // Q sub-tiles; reused as output staging
+  uint8_t q[2][Cfg::kTileBytes];          // Q sub-tiles of the current item
   uint8_t k[Cfg::kStagesK][Cfg::kTileBytes];
   uint8_t v[Cfg::kStagesV][Cfg::kTileBytes];
-  uint64_t q_full;
+  uint64_t q_full[2], q_empty[2];       // Q sub-tile s loaded / its last S MMA done
   uint64_t k_full[Cfg::kStagesK], k_empty[Cfg::kStagesK];
   uint64_t v_full[Cfg::kStagesV], v_empty[Cfg::kStagesV];
   uint64_t s_full[2], p_full[2], o_final[2], mma_done[2];
@@ -77,9 +83,9 @@ struct __align__(1024) PrefillSmem {
   int groups_done[2];   // MMA groups each issuer has issued (orders the two issuers)
 };
 
-// Geometry of one CTA's work item.
+// Geometry of one work item.
 struct PrefillTile {
-  int q0;        // first query row of the CTA
+  int q0;        // first query row of the item
   int lo, hi;    // K/V tile range loaded (union over the two sub-tiles)
   int S, causal, window;
   __device__ __forceinline__ int row_first(int s) const { return q0 + 128 * s; }
@@ -92,6 +98,10 @@ struct PrefillTile {
     if (causal && c0 > row_last(s)) return false;
     if (window > 0 && c1 < row_first(s) - window + 1) return false;
     return true;
+  }
+  // offset from lo of the last tile sub-tile s sees (s must be valid)
+  __device__ __forceinline__ int last_group(int s) const {
+    return (causal ? min(hi, row_last(s) / 128) : hi) - lo;
   }
   // is any (row, key) pair of sub-tile s x tile j masked?
   __device__ __forceinline__ bool needs_mask(int s, int j) const {
@@ -130,6 +140,31 @@ __device__ __forceinline__ bool spin_until_ge(volatile int* p, int v, volatile i
   return true;
 }
 
+// Work item k of CTA c among G CTAs.  Items are numbered heaviest first
+// (query block descending, then (b, h)); round k of the CTAs takes items
+// [kG, (k+1)G) in forward order when k is even and backward when odd, so a
+// CTA that drew a heavy item in one round draws a light one in the next.
+__device__ __forceinline__ int prefill_item(int k, int c, int G) {
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+struct PrefillItem {
+  int b, h, bh, bh_kv;
+  PrefillTile tile;
+};
+
+__device__ __forceinline__ PrefillItem prefill_item_of(const PrefillParams& p, int w) {
+  PrefillItem it;
+  const int per_qb = p.B * p.Hq;
+  const int qb = p.num_qblocks - 1 - w / per_qb;
+  it.bh = w % per_qb;
+  it.b = it.bh / p.Hq;
+  it.h = it.bh % p.Hq;
+  it.bh_kv = it.b * p.Hkv + it.h / (p.Hq / p.Hkv);   // g(h) = floor(h / (H/G))
+  it.tile = prefill_tile_of(p, qb);
+  return it;
+}
+
 // Drain wait used at teardown: ignores the abort flag, bounded by time.
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -139,15 +174,17 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
-// One MMA issuer: the chain of sub-tile S (0 or 1), run by a whole warp that
-// stays converged; one elected lane issues each tcgen05 instruction.  All it
-// computes descends from compile-time constants, the CTA's shared-memory base
-// and loop counters, so descriptors and tensor-memory addresses stay in
-// uniform registers: a tcgen05.mma is accepted only about as fast as the
-// tensor core runs it, so every instruction between two of them is a bubble.
-// Wait results are made warp-uniform so the warp never diverges.
+
+// One MMA issuer: the chain of sub-tile S (0 or 1) over all of the CTA's work
+// items, run by a whole warp that stays converged; one elected lane issues
+// each tcgen05 instruction.  Descriptors and tensor-memory addresses descend
+// from compile-time constants, the CTA's shared-memory base and loop
+// counters, so they stay in uniform registers: a tcgen05.mma is accepted
+// only about as fast as the tensor core runs it, so every instruction
+// between two of them is a bubble.  Wait results are made warp-uniform so
+// the warp never diverges.
 template <int DH, int S>
-__device__ __forceinline__ void prefill_issuer(PrefillSmem<DH>& sm, const PrefillTile& tile,
+__device__ __forceinline__ void prefill_issuer(PrefillSmem<DH>& sm, const PrefillParams& p,
                                                volatile int* abort, int lane) {
   using Cfg = PrefillCfg<DH>;
   constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
@@ -164,199 +201,208 @@ __device__ __forceinline__ void prefill_issuer(PrefillSmem<DH>& sm, const Prefil
   // the CTA owns all 512 columns, so its allocation starts at column 0
   constexpr uint32_t dS = S ? Cfg::kColS1 : Cfg::kColS0;
   constexpr uint32_t dO = S ? Cfg::kColO1 : Cfg::kColO0;
-  // The work of each issuer is a sequence of groups: group g holds its P.V
-  // of tile lo+g-1 and its S of tile lo+g.  The tensor core runs
+  // The work of each issuer is a sequence of groups: in an item with tiles
+  // lo..hi, group g holds its P.V of tile lo+g-1 and its S of tile lo+g.
+  // The tensor core runs
   //   S0(lo) | PV1(-) S1(lo) | PV0(lo) S0(lo+1) | PV1(lo) S1(lo+1) | ...
   // i.e. group g of sub-tile 0, then group g of sub-tile 1, then group g+1
-  // of sub-tile 0: each softmax runs while the other sub-tile's two MMA
-  // groups keep the tensor core busy.  An issuer first waits for everything
-  // of its own (P, V, K), then for the other issuer's previous group (a
-  // counter in shared memory), so the tensor core idles only for that
-  // handover.
+  // of sub-tile 0, and on into the next item: each softmax runs while the
+  // other sub-tile's two MMA groups keep the tensor core busy.  An issuer
+  // first waits for everything of its own (V, K, then P), then for the other
+  // issuer's previous group (a counter in shared memory), so the tensor core
+  // idles only for that handover.  Group, K/V-ring and barrier-phase
+  // counters run on across items.
   volatile int* mine = &sm.groups_done[S];
   volatile int* other = &sm.groups_done[1 - S];
-  const int n_tiles = tile.hi - tile.lo + 1;
-  int n_active = 0;
-  uint32_t pph = 0;
-  bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0, abort));
-  tc_fence_after_sync();
-  for (int g = 0; ok && g <= n_tiles; ++g) {
-    const bool do_pv = g >= 1 && tile.active(S, tile.lo + g - 1);
-    const bool do_s = g < n_tiles && tile.active(S, tile.lo + g);
-    const uint32_t vi = (uint32_t)(g - 1), ki = (uint32_t)g;
-    const uint32_t vst = vi % Cfg::kStagesV, vph = (vi / Cfg::kStagesV) & 1u;
-    const uint32_t kst = ki % Cfg::kStagesK, kph = (ki / Cfg::kStagesK) & 1u;
-    // Waits ordered so that the one usually completing last (this
-    // sub-tile's P, i.e. its softmax) comes last and the MMAs follow it at
-    // once.  Every issuer waits for every tile before releasing it, so
-    // neither can run a whole ring ahead of the other.
-    if (g >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[vst], vph, abort))))
-      break;
-    if (g < n_tiles && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[kst], kph, abort))))
-      break;
-    // sub-tile 0 waits for sub-tile 1's group g-1, sub-tile 1 for sub-tile 0's group g
-    if (!(ok = __all_sync(0xffffffffu, spin_until_ge(other, S ? g + 1 : g, abort)))) break;
-    if (do_pv) {
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_full[S], pph, abort)))) break;
-      pph ^= 1;
+  uint32_t kv_base = 0;   // K/V tiles of the earlier items
+  int g_base = 0;         // groups of the earlier items
+  uint32_t pph = 0, qph = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int w = prefill_item(it, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    const PrefillTile tile = prefill_item_of(p, w).tile;
+    const int n_tiles = tile.hi - tile.lo + 1;
+    const bool valid = tile.valid(S);
+    // the group of this sub-tile's last S, after which its Q buffer is free
+    const int last_s = valid ? tile.last_group(S) : -1;
+    int n_active = 0;
+    if (valid) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[S], qph, abort));
+      qph ^= 1;
+      if (!ok) break;
     }
-    tc_fence_after_sync();
-    if (g >= 1) {   // P.V of the previous tile
+    for (int g = 0; g <= n_tiles; ++g) {
+      const int gg = g_base + g;
+      const bool do_pv = g >= 1 && tile.active(S, tile.lo + g - 1);
+      const bool do_s = g < n_tiles && tile.active(S, tile.lo + g);
+      const uint32_t vi = kv_base + (uint32_t)(g - 1), ki = kv_base + (uint32_t)g;
+      const uint32_t vst = vi % Cfg::kStagesV, vph = (vi / Cfg::kStagesV) & 1u;
+      const uint32_t kst = ki % Cfg::kStagesK, kph = (ki / Cfg::kStagesK) & 1u;
+      // Waits ordered so that the one usually completing last (this
+      // sub-tile's P, i.e. its softmax) comes last and the MMAs follow it at
+      // once.  Every issuer waits for every tile before releasing it, so
+      // neither can run a whole ring ahead of the other.
+      if (g >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[vst], vph, abort))))
+        break;
+      if (g < n_tiles && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[kst], kph, abort))))
+        break;
+      // sub-tile 0 waits for sub-tile 1's group gg-1, sub-tile 1 for sub-tile 0's group gg
+      if (!(ok = __all_sync(0xffffffffu, spin_until_ge(other, S ? gg + 1 : gg, abort)))) break;
       if (do_pv) {
-        // O_s (+)= P_s V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
-        const uint64_t b = dv + (uint64_t)(vst * (Cfg::kTileBytes >> 4));
-        mma_bf16_ts_warp(dO, dS, b, idesc_pv, n_active > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 1; kk < 8; ++kk) mma_bf16_ts_warp(dO, dS + kk * 8, b + kk * (2048 >> 4), idesc_pv, 1u);
-        ++n_active;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_full[S], pph, abort)))) break;
+        pph ^= 1;
       }
-      mma_commit_warp(&sm.v_empty[vst]);
-    }
-    if (g < n_tiles) {   // S of this tile
-      if (do_s) {
-        // S_s = Q_s K^T: K-major operands, 16 columns (32 bytes) of DH per MMA
-        const uint64_t b = dk + (uint64_t)(kst * (Cfg::kTileBytes >> 4));
-        mma_bf16_ss_warp(dS, dq, b, idesc_qk, 0u);
+      tc_fence_after_sync();
+      // The group is handed over to the other issuer two MMAs before its
+      // end: the other issuer's waits and fences then overlap the last
+      // MMAs of this group instead of leaving the tensor core idle.  (The
+      // counter only paces the two issuers; no data passes through it.)
+      auto publish = [&]() {
+        if (lane == 0) *mine = gg + 1;
+        __syncwarp();
+      };
+      if (g >= 1) {   // P.V of the previous tile
+        if (do_pv) {
+          // O_s (+)= P_s V: P from TMEM (8 columns = 16 keys per MMA), V MN-major.
+          // The first P.V of an item overwrites O_s: the epilogue of the
+          // previous item has read it, since these same softmax threads
+          // published P only after that read completed.
+          const uint64_t b = dv + (uint64_t)(vst * (Cfg::kTileBytes >> 4));
+          mma_bf16_ts_warp(dO, dS, b, idesc_pv, n_active > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 1; kk < DH / 16; ++kk) {
-          const uint32_t off = ((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4;
-          mma_bf16_ss_warp(dS, dq + off, b + off, idesc_qk, 1u);
+          for (int kk = 1; kk < 8; ++kk) {
+            if (kk == 6 && !do_s) publish();
+            mma_bf16_ts_warp(dO, dS + kk * 8, b + kk * (2048 >> 4), idesc_pv, 1u);
+          }
+          ++n_active;
         }
-        mma_commit_warp(&sm.s_full[S]);
+        mma_commit_warp(&sm.v_empty[vst]);
       }
-      mma_commit_warp(&sm.k_empty[kst]);
+      if (g < n_tiles) {   // S of this tile
+        if (do_s) {
+          // S_s = Q_s K^T: K-major operands, 16 columns (32 bytes) of DH per MMA
+          const uint64_t b = dk + (uint64_t)(kst * (Cfg::kTileBytes >> 4));
+          mma_bf16_ss_warp(dS, dq, b, idesc_qk, 0u);
+#pragma unroll
+          for (int kk = 1; kk < DH / 16; ++kk) {
+            if (kk == DH / 16 - 2) publish();
+            const uint32_t off = ((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4;
+            mma_bf16_ss_warp(dS, dq + off, b + off, idesc_qk, 1u);
+          }
+          mma_commit_warp(&sm.s_full[S]);
+        }
+        if (g == last_s) mma_commit_warp(&sm.q_empty[S]);
+        mma_commit_warp(&sm.k_empty[kst]);
+      }
+      if (!do_s && !do_pv) publish();
     }
-    __threadfence_block();
-    if (lane == 0) *mine = g + 1;
-    __syncwarp();
+    if (!ok) break;
+    if (n_active > 0) mma_commit_warp(&sm.o_final[S]);
+    kv_base += (uint32_t)n_tiles;
+    g_base += n_tiles + 1;
   }
-  if (ok && n_active > 0) mma_commit_warp(&sm.o_final[S]);
   // nothing of this thread's may still run on the tensor core at teardown
   mma_commit_warp(&sm.mma_done[S]);
   mbar_wait_drain(&sm.mma_done[S], 0);
 }
 
+// TMA producer (one thread): per work item, Q sub-tile 0, the first K tile,
+// Q sub-tile 1, then the K/V tiles in order.  A Q sub-tile is reloaded once
+// its issuer's last S MMA of the previous item is done, so the next item's
+// first tiles arrive while the current one finishes.
 template <int DH>
-__global__ void __launch_bounds__(352, 1)
-    attn_prefill_sm103a(const __grid_constant__ CUtensorMap map_q,
-                        const __grid_constant__ CUtensorMap map_k,
-                        const __grid_constant__ CUtensorMap map_v,
-                        const __grid_constant__ CUtensorMap map_o, const PrefillParams p) {
+__device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const PrefillParams& p,
+                                                 const CUtensorMap* map_q,
+                                                 const CUtensorMap* map_k,
+                                                 const CUtensorMap* map_v,
+                                                 volatile int* abort) {
   using Cfg = PrefillCfg<DH>;
-  using Smem = PrefillSmem<DH>;
-  extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~uintptr_t(1023));
-  volatile int* abort = &sm.abort_flag;
+  prefetch_tensormap(map_q);
+  prefetch_tensormap(map_k);
+  prefetch_tensormap(map_v);
+  const uint64_t keep = policy_evict_last();   // K/V tiles are re-read by other CTAs
+  uint32_t kst = 0, kph = 0, vst = 0, vph = 0;
+  uint32_t k_loaded = 0, k_par = 0, v_loaded = 0, v_par = 0;
+  uint32_t nq0 = 0, nq1 = 0;   // Q loads per sub-tile so far
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int w = prefill_item(it, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    const PrefillItem item = prefill_item_of(p, w);
+    const PrefillTile& tile = item.tile;
+    auto load_q = [&](int s, uint32_t& n) {
+      if (n > 0 && !mbar_wait(&sm.q_empty[s], (n - 1) & 1u, abort)) return false;
+      mbar_arrive_expect_tx(&sm.q_full[s], Cfg::kTileBytes);
+      for (int hf = 0; hf < Cfg::kHalves; ++hf)
+        tma_load_3d(sm.q[s] + hf * Cfg::kBoxBytes, map_q, &sm.q_full[s], hf * 64,
+                    tile.row_first(s), item.bh);
+      ++n;
+      return true;
+    };
+    if (!(ok = load_q(0, nq0))) break;
+    for (int j = tile.lo; j <= tile.hi; ++j) {
+      if (!(ok = mbar_wait(&sm.k_empty[kst], kph ^ 1, abort))) break;
+      mbar_arrive_expect_tx(&sm.k_full[kst], Cfg::kTileBytes);
+      for (int hf = 0; hf < Cfg::kHalves; ++hf)
+        tma_load_3d_hint(sm.k[kst] + hf * Cfg::kBoxBytes, map_k, &sm.k_full[kst], hf * 64,
+                         128 * j, item.bh_kv, keep);
+      k_loaded |= 1u << kst;
+      k_par = (k_par & ~(1u << kst)) | (kph << kst);
+      if (++kst == Cfg::kStagesK) { kst = 0; kph ^= 1; }
 
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
+      if (j == tile.lo && tile.valid(1) && !(ok = load_q(1, nq1))) break;
 
-  // ---- work item: heaviest query blocks first (causal work grows with qb)
-  const int per_qb = p.B * p.Hq;
-  const int qb = p.num_qblocks - 1 - (int)(blockIdx.x / per_qb);
-  const int bh = (int)(blockIdx.x % per_qb);
-  const int b = bh / p.Hq, h = bh % p.Hq;
-  const int g = h / (p.Hq / p.Hkv);          // g(h) = floor(h / (H/G))
-  const int bh_kv = b * p.Hkv + g;
-  const PrefillTile tile = prefill_tile_of(p, qb);
-
-  // ---- setup
-  if (threadIdx.x == 0) {
-    sm.abort_flag = 0;
-    sm.groups_done[0] = 0;
-    sm.groups_done[1] = 0;
-    mbar_init(&sm.q_full, 1);
-    // a K/V stage is free once both issuers' MMAs reading it are done
-    for (int i = 0; i < Cfg::kStagesK; ++i) { mbar_init(&sm.k_full[i], 1); mbar_init(&sm.k_empty[i], 2); }
-    for (int i = 0; i < Cfg::kStagesV; ++i) { mbar_init(&sm.v_full[i], 1); mbar_init(&sm.v_empty[i], 2); }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.p_full[s], 128);
-      mbar_init(&sm.o_final[s], 1);
+      if (!(ok = mbar_wait(&sm.v_empty[vst], vph ^ 1, abort))) break;
+      mbar_arrive_expect_tx(&sm.v_full[vst], Cfg::kTileBytes);
+      for (int hf = 0; hf < Cfg::kHalves; ++hf)
+        tma_load_3d_hint(sm.v[vst] + hf * Cfg::kBoxBytes, map_v, &sm.v_full[vst], hf * 64,
+                         128 * j, item.bh_kv, keep);
+      v_loaded |= 1u << vst;
+      v_par = (v_par & ~(1u << vst)) | (vph << vst);
+      if (++vst == Cfg::kStagesV) { vst = 0; vph ^= 1; }
     }
-    mbar_init(&sm.mma_done[0], 1);
-    mbar_init(&sm.mma_done[1], 1);
-    fence_mbarrier_init();
   }
-  if (warp == 8) {
-    tmem_alloc(&sm.tmem_base, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tbase = sm.tmem_base;
-  // all 512 columns are this CTA's, so the allocation starts at column 0;
-  // the MMA issuers rely on that (compile-time tensor-memory addresses)
-  if (threadIdx.x == 0 && tbase != 0) sm.abort_flag = 1;
+  // every copy this thread started has landed before the CTA may exit
+  if (nq0 > 0) mbar_wait_drain(&sm.q_full[0], (nq0 - 1) & 1u);
+  if (nq1 > 0) mbar_wait_drain(&sm.q_full[1], (nq1 - 1) & 1u);
+  for (int i = 0; i < Cfg::kStagesK; ++i)
+    if (k_loaded & (1u << i)) mbar_wait_drain(&sm.k_full[i], (k_par >> i) & 1u);
+  for (int i = 0; i < Cfg::kStagesV; ++i)
+    if (v_loaded & (1u << i)) mbar_wait_drain(&sm.v_full[i], (v_par >> i) & 1u);
+}
 
-  if (warp == Cfg::kWarpProducer) {
-    // =================================================================== TMA producer
-    if (lane == 0) {
-      prefetch_tensormap(&map_q);
-      prefetch_tensormap(&map_k);
-      prefetch_tensormap(&map_v);
-      const int nsub = tile.valid(1) ? 2 : 1;
-      mbar_arrive_expect_tx(&sm.q_full, nsub * Cfg::kTileBytes);
-      for (int s = 0; s < nsub; ++s)
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_3d(sm.q[s] + hf * Cfg::kBoxBytes, &map_q, &sm.q_full, hf * 64,
-                      tile.row_first(s), bh);
-      const uint64_t keep = policy_evict_last();   // K/V tiles are re-read by other CTAs
-      uint32_t kst = 0, kph = 0, vst = 0, vph = 0;
-      uint32_t k_loaded = 0, k_par = 0, v_loaded = 0, v_par = 0;
-      for (int j = tile.lo; j <= tile.hi; ++j) {
-        if (!mbar_wait(&sm.k_empty[kst], kph ^ 1, abort)) break;
-        mbar_arrive_expect_tx(&sm.k_full[kst], Cfg::kTileBytes);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_3d_hint(sm.k[kst] + hf * Cfg::kBoxBytes, &map_k, &sm.k_full[kst], hf * 64,
-                           128 * j, bh_kv, keep);
-        k_loaded |= 1u << kst;
-        k_par = (k_par & ~(1u << kst)) | (kph << kst);
-        if (++kst == Cfg::kStagesK) { kst = 0; kph ^= 1; }
-
-        if (!mbar_wait(&sm.v_empty[vst], vph ^ 1, abort)) break;
-        mbar_arrive_expect_tx(&sm.v_full[vst], Cfg::kTileBytes);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_3d_hint(sm.v[vst] + hf * Cfg::kBoxBytes, &map_v, &sm.v_full[vst], hf * 64,
-                           128 * j, bh_kv, keep);
-        v_loaded |= 1u << vst;
-        v_par = (v_par & ~(1u << vst)) | (vph << vst);
-        if (++vst == Cfg::kStagesV) { vst = 0; vph ^= 1; }
-      }
-      // every copy this thread started has landed before the CTA may exit
-      mbar_wait_drain(&sm.q_full, 0);
-      for (int i = 0; i < Cfg::kStagesK; ++i)
-        if (k_loaded & (1u << i)) mbar_wait_drain(&sm.k_full[i], (k_par >> i) & 1u);
-      for (int i = 0; i < Cfg::kStagesV; ++i)
-        if (v_loaded & (1u << i)) mbar_wait_drain(&sm.v_full[i], (v_par >> i) & 1u);
-    }
-  } else if (warp == Cfg::kWarpIssuer0 || warp == Cfg::kWarpIssuer1) {
-    // =================================================================== MMA issuers
-    if (warp == Cfg::kWarpIssuer0)
-      prefill_issuer<DH, 0>(sm, tile, abort, lane);
-    else
-      prefill_issuer<DH, 1>(sm, tile, abort, lane);
-  } else if (warp < 8) {
-    // =================================================================== softmax + epilogue
-    const int s = warp / 4;                 // sub-tile
-    const int wl = warp % 4;                // warp within the warpgroup = TMEM lane quarter
-    const int t = wl * 32 + lane;           // row within the sub-tile = TMEM lane
+// Softmax and epilogue of sub-tile s: thread t owns query row t of the
+// sub-tile (TMEM lane t) in every work item.  Per visible key tile: the
+// online softmax of "Online normalizer calculation for softmax" with a lazy
+// maximum; per item: O / l written straight from registers to global memory.
+template <int DH>
+__device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const PrefillParams& p,
+                                                uint32_t tbase, volatile int* abort, int warp,
+                                                int lane) {
+  using Cfg = PrefillCfg<DH>;
+  const int s = warp / 4;                 // sub-tile
+  const int wl = warp % 4;                // warp within the warpgroup = TMEM lane quarter
+  const int t = wl * 32 + lane;           // row within the sub-tile = TMEM lane
+  const uint32_t lane_addr = tbase + ((uint32_t)(wl * 32) << 16);
+  const uint32_t colS = lane_addr + (s ? Cfg::kColS1 : Cfg::kColS0);
+  const uint32_t colO = lane_addr + (s ? Cfg::kColO1 : Cfg::kColO0);
+  const float sl2 = p.scale_log2;
+  uint32_t ph = 0;   // bit 0: s_full phase, bit 1: o_final phase
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int w = prefill_item(it, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    const PrefillTile tile = prefill_item_of(p, w).tile;
+    if (!tile.valid(s)) continue;           // a ragged last block: no rows here
     const int row = tile.row_first(s) + t;  // absolute query row
-    const uint32_t lane_addr = tbase + ((uint32_t)(wl * 32) << 16);
-    const uint32_t colS = lane_addr + (s ? Cfg::kColS1 : Cfg::kColS0);
-    const uint32_t colO = lane_addr + (s ? Cfg::kColO1 : Cfg::kColO0);
-    const float sl2 = p.scale_log2;
 
     float m_run = -INFINITY;   // running max of scale*log2e*score (lazily updated)
     float l_run = 0.f;         // running sum of exp2(x - m_run)
-    int n_done = 0;
-    uint32_t sph = 0;
     for (int j = tile.lo; j <= tile.hi; ++j) {
       if (!tile.active(s, j)) continue;
-      if (!mbar_wait(&sm.s_full[s], sph, abort)) break;
-      sph ^= 1;
+      if (!(ok = mbar_wait(&sm.s_full[s], ph & 1u, abort))) break;
+      ph ^= 1u;
       tc_fence_after_sync();
 
       // scores, with each 32-column chunk's maximum from the load itself
@@ -404,11 +450,15 @@ __global__ void __launch_bounds__(352, 1)
       const float m_tile = mt * sl2;
       // lazy rescale: keep the old maximum unless the new one exceeds it by
       // more than 8 (weights stay <= 2^8); the result is exact either way
-      // because O and l are divided by the same sum at the end.
+      // because O and l are divided by the same sum at the end.  While
+      // m_run is -inf every weight so far was 0 (O and l are 0), so no
+      // rescale is needed; that also covers the item's first tile, whose
+      // first P.V overwrites O.
       const float m_new = fmaxf(m_run, m_tile);
-      const bool upd = (n_done == 0) || (m_new > m_run + 8.0f);
+      const bool fresh = m_run == -INFINITY;
+      const bool upd = fresh || (m_new > m_run + 8.0f);
       const float m_use = upd ? m_new : m_run;
-      const float corr = (upd && n_done > 0) ? ex2_approx(m_run - m_new) : 1.0f;
+      const float corr = (upd && !fresh) ? ex2_approx(m_run - m_new) : 1.0f;
       const float msub = (m_use == -INFINITY) ? 0.f : m_use;
       // P = exp2(x - m) as bf16 over the first 64 columns of S (the scores
       // die here, before O is touched, to keep register pressure down)
@@ -447,44 +497,93 @@ __global__ void __launch_bounds__(352, 1)
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&sm.p_full[s]);
-      ++n_done;
     }
+    if (!ok) break;
 
-    if (n_done > 0 && !*abort && mbar_wait(&sm.o_final[s], 0, abort)) {
-      tc_fence_after_sync();
-      // O / l -> bf16 -> this warp's 32 rows of the staging tile (Q buffer,
-      // 128-byte swizzled like the TMA box) -> TMA store
-      const float inv_l = 1.0f / l_run;
-      uint8_t* stg = sm.q[s];
+    // ---- epilogue: O / l -> bf16 -> row `row` of the output, 16 bytes at a time
+    if (!(ok = mbar_wait(&sm.o_final[s], (ph >> 1) & 1u, abort))) break;
+    ph ^= 2u;
+    tc_fence_after_sync();
+    const float inv_l = 1.0f / l_run;
+    const int bh = w % (p.B * p.Hq);
+    uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.S + row) * DH);
+    const bool store = row < p.S;
 #pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(colO + 32 * c, o);
-        tmem_ld_wait(o);
-        const int hf = (32 * c) / 64;
-        const int chunk0 = ((32 * c) % 64) / 8;
+    for (int c = 0; c < DH / 32; c += 2) {
+      uint32_t o0[32], o1[32];
+      tmem_ld_32x32b_x32(colO + 32 * c, o0);
+      tmem_ld_32x32b_x32(colO + 32 * c + 32, o1);
+      tmem_ld_wait(o0);
+      tmem_ld_wait(o1);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv_l, __uint_as_float(o[8 * q4 + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv_l, __uint_as_float(o[8 * q4 + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv_l, __uint_as_float(o[8 * q4 + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv_l, __uint_as_float(o[8 * q4 + 7]) * inv_l);
-          const int chunk = (chunk0 + q4) ^ (t & 7);
-          *reinterpret_cast<uint4*>(stg + hf * Cfg::kBoxBytes + t * 128 + chunk * 16) = w;
-        }
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const uint32_t* o = q8 < 4 ? o0 + 8 * q8 : o1 + 8 * (q8 - 4);
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
+        v.y = pack_bf16x2(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
+        v.z = pack_bf16x2(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
+        v.w = pack_bf16x2(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
+        if (store) dst[4 * c + q8] = v;
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && tile.row_first(s) + wl * 32 < p.S) {   // boxes wholly past S: nothing to store
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_store_3d(&map_o, stg + hf * Cfg::kBoxBytes + wl * 32 * 128, hf * 64,
-                       tile.row_first(s) + wl * 32, bh);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-      }
-      __syncwarp();
     }
+    // the next item's first P.V may overwrite O_s once these reads are done:
+    // the arrive on p_full that allows it follows tcgen05.wait::ld above
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(352, 1)
+    attn_prefill_sm103a(const __grid_constant__ CUtensorMap map_q,
+                        const __grid_constant__ CUtensorMap map_k,
+                        const __grid_constant__ CUtensorMap map_v, const PrefillParams p) {
+  using Cfg = PrefillCfg<DH>;
+  using Smem = PrefillSmem<DH>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  volatile int* abort = &sm.abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- setup (once per CTA; every barrier then runs on across work items)
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    sm.groups_done[0] = 0;
+    sm.groups_done[1] = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.p_full[s], 128);
+      mbar_init(&sm.o_final[s], 1);
+      mbar_init(&sm.mma_done[s], 1);
+    }
+    // a K/V stage is free once both issuers' MMAs reading it are done
+    for (int i = 0; i < Cfg::kStagesK; ++i) { mbar_init(&sm.k_full[i], 1); mbar_init(&sm.k_empty[i], 2); }
+    for (int i = 0; i < Cfg::kStagesV; ++i) { mbar_init(&sm.v_full[i], 1); mbar_init(&sm.v_empty[i], 2); }
+    fence_mbarrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = sm.tmem_base;
+  // all 512 columns are this CTA's, so the allocation starts at column 0;
+  // the MMA issuers rely on that (compile-time tensor-memory addresses)
+  if (tbase != 0) {
+    if (threadIdx.x == 0) sm.abort_flag = 1;
+  } else if (warp == Cfg::kWarpProducer) {
+    if (lane == 0) prefill_producer<DH>(sm, p, &map_q, &map_k, &map_v, abort);
+  } else if (warp == Cfg::kWarpIssuer0) {
+    prefill_issuer<DH, 0>(sm, p, abort, lane);
+  } else if (warp == Cfg::kWarpIssuer1) {
+    prefill_issuer<DH, 1>(sm, p, abort, lane);
+  } else if (warp < 8) {
+    prefill_softmax<DH>(sm, p, tbase, abort, warp, lane);
   }
 
   // ---- teardown (every thread gets here; all waits above are bounded)

@@ -60,6 +60,29 @@ def test_all_rows_small(B, Hq, Hkv, S, Dh, causal, window):
     assert_close(o.float().cpu().numpy(), ref, what=f"{(B, Hq, Hkv, S, Dh, causal, window)}")
 
 
+# More work items (256-row query blocks x heads) than SMs, so every CTA of the
+# persistent kernel runs several in a row: the barrier phases, ring positions
+# and tensor-memory accumulators carry from one item into the next.  Mixed
+# item sizes, a last block whose second 128-row half is empty (S % 256 <= 128)
+# or partly filled, GQA, windows, both head sizes.
+PERSISTENT = [
+    (3, 16, 4, 2900, 128, 1, 0),
+    (2, 24, 8, 3000, 64, 1, 700),
+    (2, 16, 16, 2000, 128, 0, 0),
+    (1, 160, 160, 256, 128, 1, 0),
+    (8, 40, 8, 130, 64, 1, 0),
+    (4, 20, 5, 1500, 128, 1, 129),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,Dh,causal,window", PERSISTENT)
+def test_all_rows_many_items_per_cta(B, Hq, Hkv, S, Dh, causal, window):
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, S, Dh, seed=3 * S + Dh + window)
+    o = gpu_fwd(q, k, v, causal, window)
+    ref = oracle.attention(q, k, v, causal=bool(causal), window=window)
+    assert_close(o.float().cpu().numpy(), ref, what=f"{(B, Hq, Hkv, S, Dh, causal, window)}")
+
+
 def test_explicit_scale():
     q, k, v = inputs.prefill_inputs(1, 2, 2, 200, 128, seed=5)
     o = gpu_fwd(q, k, v, 1, 0, scale=0.05)
