@@ -432,10 +432,14 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
         int khi = tile.S - 1;
         if (tile.causal) khi = min(khi, row);
         const int klo = tile.window > 0 ? row - tile.window + 1 : 0;
-        const int clo = klo - kv0, chi = khi - kv0;
+        // column c is visible iff c - clo, as unsigned, is <= chi - clo; an
+        // empty range moves clo far above every column, so nothing is kept
+        int clo = klo - kv0;
+        const int chi = khi - kv0;
+        const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
+        if (chi < clo) clo = 1 << 30;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c < clo || c > chi) x[c] = -INFINITY;
+        for (int c = 0; c < 128; ++c) x[c] = keep_if_le(x[c], (uint32_t)(c - clo), span);
         float mx[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) mx[i] = fmax3(x[i], x[4 + i], x[8 + i]);

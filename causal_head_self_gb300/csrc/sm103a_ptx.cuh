@@ -399,6 +399,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// x if off <= span (unsigned), else -inf: a predicated select, so that a
+// per-lane mask never becomes a divergent branch
+__device__ __forceinline__ float keep_if_le(float x, uint32_t off, uint32_t span) {
+  float d;
+  asm("{\n .reg .pred p;\n setp.le.u32 p, %1, %2;\n selp.f32 %0, %3, 0fFF800000, p;\n}"
+      : "=f"(d) : "r"(off), "r"(span), "f"(x));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
