@@ -48,6 +48,7 @@ struct PrefillParams {
   int num_qblocks;    // ceil(S / 256)
   int num_items;      // work items: num_qblocks * B * Hq
   __nv_bfloat16* o;   // output [B, Hq, S, DH]
+  int o_wide;         // o is 32-byte aligned: 32-byte stores
   int* error_word;    // set to a nonzero status when a wait gives up
 };
 
@@ -504,7 +505,8 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
     }
     if (!ok) break;
 
-    // ---- epilogue: O / l -> bf16 -> row `row` of the output, 16 bytes at a time
+    // ---- epilogue: O / l -> bf16 -> row `row` of the output, 32 bytes per
+    // store (16 when the output is only 16-byte aligned)
     if (!(ok = mbar_wait(&sm.o_final[s], (ph >> 1) & 1u, abort))) break;
     ph ^= 2u;
     tc_fence_after_sync();
@@ -520,14 +522,21 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
       tmem_ld_wait(o0);
       tmem_ld_wait(o1);
 #pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const uint32_t* o = q8 < 4 ? o0 + 8 * q8 : o1 + 8 * (q8 - 4);
-        uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
-        v.y = pack_bf16x2(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
-        v.z = pack_bf16x2(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
-        v.w = pack_bf16x2(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
-        if (store) dst[4 * c + q8] = v;
+      for (int q = 0; q < 4; ++q) {   // 16 columns each
+        const uint32_t* o = q < 2 ? o0 + 16 * q : o1 + 16 * (q - 2);
+        uint32_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          v[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+        if (store) {
+          uint4* d = dst + 2 * (2 * c + q);
+          if (p.o_wide) {
+            st_global_v8(d, v);
+          } else {
+            d[0] = make_uint4(v[0], v[1], v[2], v[3]);
+            d[1] = make_uint4(v[4], v[5], v[6], v[7]);
+          }
+        }
       }
     }
     // the next item's first P.V may overwrite O_s once these reads are done:

@@ -399,6 +399,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// one 32-byte global store (sm_100+); p must be 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                  "r"(w[6]), "r"(w[7]) : "memory");
+}
+
 // x if off <= span (unsigned), else -inf: a predicated select, so that a
 // per-lane mask never becomes a divergent branch
 __device__ __forceinline__ float keep_if_le(float x, uint32_t off, uint32_t span) {

@@ -83,6 +83,21 @@ def test_all_rows_many_items_per_cta(B, Hq, Hkv, S, Dh, causal, window):
     assert_close(o.float().cpu().numpy(), ref, what=f"{(B, Hq, Hkv, S, Dh, causal, window)}")
 
 
+def test_output_only_16_byte_aligned():
+    """The output may start on any 16-byte boundary (the kernel then stores
+    16 bytes at a time instead of 32); results are identical."""
+    q, k, v = inputs.prefill_inputs(2, 4, 2, 300, 128, seed=12)
+    d = torch.device("cuda")
+    q, k, v = q.to(d), k.to(d), v.to(d)
+    want = chs.attn_fwd(q, k, v)
+    buf = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device=d)
+    o = buf[8:].view(q.shape)
+    assert o.data_ptr() % 32 == 16
+    chs.attn_fwd(q, k, v, o)
+    assert chs.attn_status() == chs.ATTN_OK
+    assert torch.equal(o, want)
+
+
 def test_explicit_scale():
     q, k, v = inputs.prefill_inputs(1, 2, 2, 200, 128, seed=5)
     o = gpu_fwd(q, k, v, 1, 0, scale=0.05)
