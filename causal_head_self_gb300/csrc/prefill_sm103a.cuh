@@ -406,6 +406,44 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
       ph ^= 1u;
       tc_fence_after_sync();
 
+      if (tile.needs_mask(s, j)) {
+        // A boundary crosses this tile: overwrite the scores of the keys this
+        // row may not see with -inf in tensor memory, so the loads below and
+        // everything after them are those of an unmasked tile.  Visible keys
+        // of this row: [klo, khi] (absolute), as column offsets [clo, chi];
+        // column c is kept iff c - clo, as unsigned, is <= chi - clo (an
+        // empty range moves clo past every column).  A 32-column chunk that
+        // every row of the warp sees is left alone, one that none sees is
+        // filled without being read; only mixed chunks are read and masked
+        // (a predicated select, never a branch).  A rolled loop keeps this
+        // rarely run code small.
+        const int kv0 = 128 * j;
+        int khi = tile.S - 1;
+        if (tile.causal) khi = min(khi, row);
+        const int klo = tile.window > 0 ? row - tile.window + 1 : 0;
+        int clo = klo - kv0;
+        const int chi = khi - kv0;
+        const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
+        if (chi < clo) clo = 1 << 30;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          if (__all_sync(0xffffffffu, c0 >= clo && c0 + 31 <= chi)) continue;
+          uint32_t y[32];
+          if (__all_sync(0xffffffffu, c0 + 31 < clo || c0 > chi)) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) y[e] = 0xff800000u;   // -inf
+          } else {
+            tmem_ld_32x32b_x32(colS + c0, y);
+            tmem_ld_wait(y);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              y[e] = __float_as_uint(keep_if_le(__uint_as_float(y[e]), (uint32_t)(c0 + e - clo), span));
+          }
+          tmem_st_32x32b_x32(colS + c0, y);
+        }
+        tmem_st_wait();
+      }
+
       // scores, with each 32-column chunk's maximum from the load itself
       uint32_t r0[32], r1[32], r2[32], r3[32];
       float mc0, mc1, mc2, mc3;
@@ -425,33 +463,7 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
         x[64 + c] = __uint_as_float(r2[c]);
         x[96 + c] = __uint_as_float(r3[c]);
       }
-      float mt = fmaxf(fmaxf(mc0, mc1), fmaxf(mc2, mc3));
-      if (tile.needs_mask(s, j)) {
-        // visible keys of this row: [klo, khi] (absolute), as column offsets;
-        // the maximum is retaken over the visible keys only
-        const int kv0 = 128 * j;
-        int khi = tile.S - 1;
-        if (tile.causal) khi = min(khi, row);
-        const int klo = tile.window > 0 ? row - tile.window + 1 : 0;
-        // column c is visible iff c - clo, as unsigned, is <= chi - clo; an
-        // empty range moves clo far above every column, so nothing is kept
-        int clo = klo - kv0;
-        const int chi = khi - kv0;
-        const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
-        if (chi < clo) clo = 1 << 30;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = keep_if_le(x[c], (uint32_t)(c - clo), span);
-        float mx[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mx[i] = fmax3(x[i], x[4 + i], x[8 + i]);
-#pragma unroll
-        for (int c = 12; c < 124; c += 8)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], x[c + i], x[c + 4 + i]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], x[124 + i]);
-        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      }
+      const float mt = fmaxf(fmaxf(mc0, mc1), fmaxf(mc2, mc3));
       const float m_tile = mt * sl2;
       // lazy rescale: keep the old maximum unless the new one exceeds it by
       // more than 8 (weights stay <= 2^8); the result is exact either way
