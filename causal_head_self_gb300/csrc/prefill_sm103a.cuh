@@ -317,20 +317,17 @@ __device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const Pref
                                                  const CUtensorMap* map_q,
                                                  const CUtensorMap* map_k,
                                                  const CUtensorMap* map_v,
+                                                 const PrefillItem& first,
                                                  volatile int* abort) {
   using Cfg = PrefillCfg<DH>;
-  prefetch_tensormap(map_q);
-  prefetch_tensormap(map_k);
-  prefetch_tensormap(map_v);
   const uint64_t keep = policy_evict_last();   // K/V tiles are re-read by other CTAs
   uint32_t kst = 0, kph = 0, vst = 0, vph = 0;
   uint32_t k_loaded = 0, k_par = 0, v_loaded = 0, v_par = 0;
   uint32_t nq0 = 0, nq1 = 0;   // Q loads per sub-tile so far
   bool ok = true;
+  // the grid is no larger than the number of items, so every CTA has a first one
+  PrefillItem item = first;
   for (int it = 0; ok; ++it) {
-    const int w = prefill_item(it, blockIdx.x, gridDim.x);
-    if (w >= p.num_items) break;
-    const PrefillItem item = prefill_item_of(p, w);
     const PrefillTile& tile = item.tile;
     auto load_q = [&](int s, uint32_t& n) {
       if (n > 0 && !mbar_wait(&sm.q_empty[s], (n - 1) & 1u, abort)) return false;
@@ -363,6 +360,10 @@ __device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const Pref
       v_par = (v_par & ~(1u << vst)) | (vph << vst);
       if (++vst == Cfg::kStagesV) { vst = 0; vph ^= 1; }
     }
+    // decode the next item while this one's copies are in flight
+    const int w = prefill_item(it + 1, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    item = prefill_item_of(p, w);
   }
   // every copy this thread started has landed before the CTA may exit
   if (nq0 > 0) mbar_wait_drain(&sm.q_full[0], (nq0 - 1) & 1u);
@@ -572,6 +573,16 @@ __global__ void __launch_bounds__(352, 1)
   const int lane = threadIdx.x % 32;
 
   // ---- setup (once per CTA; every barrier then runs on across work items)
+  // The producer decodes its first item and prefetches the tensor maps
+  // first: the parameter reads and the integer divisions then overlap the
+  // barrier set-up and the tensor-memory allocation.
+  PrefillItem first{};
+  if (warp == Cfg::kWarpProducer && lane == 0) {
+    prefetch_tensormap(&map_q);
+    prefetch_tensormap(&map_k);
+    prefetch_tensormap(&map_v);
+    first = prefill_item_of(p, prefill_item(0, blockIdx.x, gridDim.x));
+  }
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
     sm.groups_done[0] = 0;
@@ -602,7 +613,7 @@ __global__ void __launch_bounds__(352, 1)
   if (tbase != 0) {
     if (threadIdx.x == 0) sm.abort_flag = 1;
   } else if (warp == Cfg::kWarpProducer) {
-    if (lane == 0) prefill_producer<DH>(sm, p, &map_q, &map_k, &map_v, abort);
+    if (lane == 0) prefill_producer<DH>(sm, p, &map_q, &map_k, &map_v, first, abort);
   } else if (warp == Cfg::kWarpIssuer0) {
     prefill_issuer<DH, 0>(sm, p, abort, lane);
   } else if (warp == Cfg::kWarpIssuer1) {
