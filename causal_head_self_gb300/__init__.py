@@ -2,11 +2,11 @@
 
 The compute path is the CUDA library ``libattn_sm103a.so`` (C ABI in
 ``include/attn.h``); this package is its thin Python binding.  ``attn_fwd``
-runs the tcgen05/TMA prefill kernel, ``attn_decode`` the split-KV decode and
-log-sum-exp combine kernels.  There is no CPU or PyTorch fallback: without the
+runs the tcgen05/TMA prefill kernel, ``attn_decode`` the split-KV decode kernel
+with its in-kernel log-sum-exp combine.  There is no CPU or PyTorch fallback: without the
 built library every call raises.
 """
 from ._binding import (ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_NO_MEMORY,  # noqa: F401
                        ATTN_ERR_SCRATCH_LIMIT, ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED, ATTN_OK,
-                       AttnError, attn_decode, attn_decode_noalloc, attn_fwd, attn_status,
-                       error_string, version)
+                       AttnError, attn_debug_inject_fault, attn_decode, attn_decode_noalloc,
+                       attn_fwd, attn_status, error_string, version)

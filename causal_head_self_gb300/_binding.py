@@ -26,7 +26,7 @@ ATTN_ERR_SCRATCH_LIMIT = 6
 
 # every symbol include/attn.h declares
 ABI_SYMBOLS = ("attn_fwd", "attn_decode", "attn_decode_noalloc", "attn_status",
-               "attn_error_string", "attn_version")
+               "attn_error_string", "attn_version", "attn_debug_inject_fault")
 
 _lib = None
 _lock = threading.Lock()
@@ -60,6 +60,8 @@ def load():
             lib.attn_error_string.argtypes = [i]
             lib.attn_version.restype = i
             lib.attn_version.argtypes = []
+            lib.attn_debug_inject_fault.restype = i
+            lib.attn_debug_inject_fault.argtypes = [i]
             _lib = lib
     return _lib
 
@@ -162,6 +164,15 @@ def attn_decode_noalloc(q, kcache, vcache, seqlens, o=None, *, window=0, scale=0
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_noalloc")
     return o
+
+
+def attn_debug_inject_fault(kind: int) -> None:
+    """Test hook (see include/attn.h): 0 none, 1 a prefill K tile is withheld,
+    2 a decode key block is withheld; later launches wait, give up and report
+    ATTN_ERR_TIMEOUT through attn_status()."""
+    rc = load().attn_debug_inject_fault(int(kind))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_debug_inject_fault")
 
 
 def attn_status(stream=None) -> int:

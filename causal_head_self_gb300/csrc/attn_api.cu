@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -87,6 +88,7 @@ int device_state(DeviceState** out) {
     st.info.device = dev;
     st.info.num_sms = sms;
     st.info.error_word = static_cast<int*>(word);
+    st.info.fault = 0;
     st.ready = true;
   }
   *out = &st;
@@ -143,6 +145,21 @@ const char* attn_error_string(int code) {
   }
 }
 
+// The test hook's current fault (attn_debug_inject_fault); 0 in normal use.
+static std::atomic<int> g_fault{0};
+
+static chs::DeviceInfo launch_info(const DeviceState* st) {
+  chs::DeviceInfo d = st->info;
+  d.fault = g_fault.load(std::memory_order_relaxed);
+  return d;
+}
+
+int attn_debug_inject_fault(int kind) {
+  if (kind < 0 || kind > 2) return ATTN_ERR_INVALID_ARG;
+  g_fault.store(kind, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
 int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int S,
              int Dh, int causal, int window, float scale, cudaStream_t stream) {
   if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
@@ -164,7 +181,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq
   int rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
   cudaError_t e = chs::launch_prefill(q, k, v, o, B, Hq, Hkv, S, Dh, causal, window, scale_log2,
-                                      st->info, stream);
+                                      launch_info(st), stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -211,7 +228,8 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
     counters = st->counters;
   }
   cudaError_t e = chs::launch_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, window,
-                                     scale_log2, plan, counters, partials, st->info, stream);
+                                     scale_log2, plan, counters, partials, launch_info(st),
+                                     stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -295,7 +313,7 @@ extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void
   if (cudaMemsetAsync(counters, 0, n_counters * sizeof(int), stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   cudaError_t e = chs::launch_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, window,
-                                     scale_log2, plan, counters, scratch + counter_bytes, st->info,
-                                     stream);
+                                     scale_log2, plan, counters, scratch + counter_bytes,
+                                     launch_info(st), stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -100,6 +100,7 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
   prm.chunk = plan.chunk;
   prm.scale_log2 = scale_log2;
   prm.error_word = dev.error_word;
+  prm.fault = dev.fault;
   return Dh == 128 ? launch_hpb<128>(prm, plan.heads_per_cta, stream)
                    : launch_hpb<64>(prm, plan.heads_per_cta, stream);
 }

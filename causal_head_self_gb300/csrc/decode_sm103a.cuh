@@ -43,6 +43,7 @@ struct DecodeParams {
   int nsplit, chunk;
   float scale_log2;
   int* error_word;
+  int fault;                // test hook: 2 = the first key block is never loaded
 };
 
 constexpr int kDecodeBlockKeys = 32;    // keys per pipeline stage
@@ -203,12 +204,14 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
       for (int blk = 0; blk < nblk; ++blk) {
         const int n = min(kDecodeBlockKeys, nkeys - blk * kDecodeBlockKeys);
         if (!mbar_wait(&sm.empty[st], ph ^ 1, abort)) break;
-        mbar_arrive_expect_tx(&sm.full[st], 2u * n * ROW);
-        const size_t off = (size_t)blk * kDecodeBlockKeys * ROW;
-        bulk_load(sm.k[st], kg + off, n * ROW, &sm.full[st], stream_once);
-        bulk_load(sm.v[st], vg + off, n * ROW, &sm.full[st], stream_once);
-        loaded |= 1u << st;
-        par = (par & ~(1u << st)) | (ph << st);
+        if (p.fault != 2 || blk != 0) {   // (the test hook withholds one block)
+          mbar_arrive_expect_tx(&sm.full[st], 2u * n * ROW);
+          const size_t off = (size_t)blk * kDecodeBlockKeys * ROW;
+          bulk_load(sm.k[st], kg + off, n * ROW, &sm.full[st], stream_once);
+          bulk_load(sm.v[st], vg + off, n * ROW, &sm.full[st], stream_once);
+          loaded |= 1u << st;
+          par = (par & ~(1u << st)) | (ph << st);
+        }
         if (++st == kDecodeStages) { st = 0; ph ^= 1; }
       }
       // every copy this thread started has landed before the CTA may exit

@@ -12,6 +12,7 @@ struct DeviceInfo {
   int device;
   int num_sms;
   int* error_word;   // device address of this device's latched error word
+  int fault;         // test hook passed to the kernels (attn_debug_inject_fault)
 };
 
 // Encode a 3-D tensor map over a contiguous [outer, rows, Dh] bf16 tensor:

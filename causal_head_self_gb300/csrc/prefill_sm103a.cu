@@ -43,6 +43,7 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o,
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.o_wide = (reinterpret_cast<uintptr_t>(o) & 31) == 0;
   prm.error_word = dev.error_word;
+  prm.fault = dev.fault;
   return Dh == 128 ? launch_prefill_dh<128>(mq, mk, mv, prm, dev.num_sms, stream)
                    : launch_prefill_dh<64>(mq, mk, mv, prm, dev.num_sms, stream);
 }

@@ -50,6 +50,7 @@ struct PrefillParams {
   __nv_bfloat16* o;   // output [B, Hq, S, DH]
   int o_wide;         // o is 32-byte aligned: 32-byte stores
   int* error_word;    // set to a nonzero status when a wait gives up
+  int fault;          // test hook: 1 = the first K tile is never loaded
 };
 
 template <int DH>
@@ -341,12 +342,14 @@ __device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const Pref
     if (!(ok = load_q(0, nq0))) break;
     for (int j = tile.lo; j <= tile.hi; ++j) {
       if (!(ok = mbar_wait(&sm.k_empty[kst], kph ^ 1, abort))) break;
-      mbar_arrive_expect_tx(&sm.k_full[kst], Cfg::kTileBytes);
-      for (int hf = 0; hf < Cfg::kHalves; ++hf)
-        tma_load_3d_hint(sm.k[kst] + hf * Cfg::kBoxBytes, map_k, &sm.k_full[kst], hf * 64,
-                         128 * j, item.bh_kv, keep);
-      k_loaded |= 1u << kst;
-      k_par = (k_par & ~(1u << kst)) | (kph << kst);
+      if (p.fault != 1 || it != 0 || j != tile.lo) {   // (the test hook withholds one tile)
+        mbar_arrive_expect_tx(&sm.k_full[kst], Cfg::kTileBytes);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+          tma_load_3d_hint(sm.k[kst] + hf * Cfg::kBoxBytes, map_k, &sm.k_full[kst], hf * 64,
+                           128 * j, item.bh_kv, keep);
+        k_loaded |= 1u << kst;
+        k_par = (k_par & ~(1u << kst)) | (kph << kst);
+      }
       if (++kst == Cfg::kStagesK) { kst = 0; kph ^= 1; }
 
       if (j == tile.lo && tile.valid(1) && !(ok = load_q(1, nq1))) break;

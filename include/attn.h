@@ -136,6 +136,25 @@ int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
  */
 int attn_status(cudaStream_t stream);
 
+/*
+ * attn_debug_inject_fault -- test hook for the failure path; the pages
+ * describe no such call.  Every later attn_fwd / attn_decode /
+ * attn_decode_noalloc launch in this process runs with the given fault until
+ * it is reset with kind 0:
+ *   0  none (the default)
+ *   1  attn_fwd: the producer never loads the first K tile of each CTA's
+ *      first work item, so the MMA issuers' bounded waits run out
+ *   2  attn_decode: the producer never loads the first key block of each CTA
+ * A faulted launch ends by itself after its waits give up (about 2 s): no
+ * GPU fault, trap or hang.  attn_status() then returns ATTN_ERR_TIMEOUT and
+ * clears it; the outputs of that launch are undefined, and the next launch
+ * without a fault is correct (the decode completion counters are left at
+ * zero).  Returns ATTN_OK, or ATTN_ERR_INVALID_ARG for an unknown kind.
+ * Not for production use: the setting is process-wide and unsynchronised
+ * with launches already queued.
+ */
+int attn_debug_inject_fault(int kind);
+
 /* attn_error_string -- a static, human-readable name for a status code. */
 const char* attn_error_string(int code);
 
