@@ -20,6 +20,15 @@ static cudaError_t launch_prefill_dh(const CUtensorMap& mq, const CUtensorMap& m
   return cudaGetLastError();
 }
 
+// Multiplier and shift for FastDiv (exact for dividends below 2^31).
+static FastDiv make_fast_div(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  const unsigned __int128 one = 1;
+  const uint64_t m = (uint64_t)(((one << (31 + l)) + d - 1) / d);
+  return FastDiv{(uint32_t)m, 31 + l, d};
+}
+
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
                            int Hkv, int S, int Dh, int causal, int window, float scale_log2,
                            const DeviceInfo& dev, cudaStream_t stream) {
@@ -44,6 +53,9 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o,
   prm.o_wide = (reinterpret_cast<uintptr_t>(o) & 31) == 0;
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
+  prm.div_bh = make_fast_div((uint32_t)(B * Hq));
+  prm.div_hq = make_fast_div((uint32_t)Hq);
+  prm.div_group = make_fast_div((uint32_t)(Hq / Hkv));
   return Dh == 128 ? launch_prefill_dh<128>(mq, mk, mv, prm, dev.num_sms, stream)
                    : launch_prefill_dh<64>(mq, mk, mv, prm, dev.num_sms, stream);
 }

@@ -40,6 +40,19 @@
 
 namespace chs {
 
+// Exact division of a non-negative int n < 2^31 by a fixed divisor d >= 1:
+// n / d == (n * m) >> (31 + l) with l = ceil(log2 d) and m = ceil(2^(31+l) / d)
+// (the rounding error n*(m*d - 2^(31+l)) / (d * 2^(31+l)) stays below 1/d).
+// The multiplier is made on the host; the device pays one wide multiply
+// instead of a division sequence.
+struct FastDiv {
+  uint32_t m, shift, d;
+  __device__ __forceinline__ int div(int n) const {
+    return (int)(((uint64_t)(uint32_t)n * m) >> shift);
+  }
+  __device__ __forceinline__ int mod(int n) const { return n - div(n) * (int)d; }
+};
+
 struct PrefillParams {
   int B, Hq, Hkv, S;
   int causal;   // 1: key j visible to query i only if j <= i
@@ -51,6 +64,9 @@ struct PrefillParams {
   int o_wide;         // o is 32-byte aligned: 32-byte stores
   int* error_word;    // set to a nonzero status when a wait gives up
   int fault;          // test hook: 1 = the first K tile is never loaded
+  FastDiv div_bh;     // by B * Hq (work items per query block)
+  FastDiv div_hq;     // by Hq
+  FastDiv div_group;  // by Hq / Hkv (query heads per K/V head)
 };
 
 template <int DH>
@@ -157,12 +173,12 @@ struct PrefillItem {
 
 __device__ __forceinline__ PrefillItem prefill_item_of(const PrefillParams& p, int w) {
   PrefillItem it;
-  const int per_qb = p.B * p.Hq;
-  const int qb = p.num_qblocks - 1 - w / per_qb;
-  it.bh = w % per_qb;
-  it.b = it.bh / p.Hq;
-  it.h = it.bh % p.Hq;
-  it.bh_kv = it.b * p.Hkv + it.h / (p.Hq / p.Hkv);   // g(h) = floor(h / (H/G))
+  const int blk = p.div_bh.div(w);
+  const int qb = p.num_qblocks - 1 - blk;
+  it.bh = w - blk * (int)p.div_bh.d;
+  it.b = p.div_hq.div(it.bh);
+  it.h = it.bh - it.b * p.Hq;
+  it.bh_kv = it.b * p.Hkv + p.div_group.div(it.h);   // g(h) = floor(h / (H/G))
   it.tile = prefill_tile_of(p, qb);
   return it;
 }
@@ -249,8 +265,13 @@ __device__ __forceinline__ void prefill_issuer(PrefillSmem<DH>& sm, const Prefil
         break;
       if (g < n_tiles && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[kst], kph, abort))))
         break;
-      // sub-tile 0 waits for sub-tile 1's group gg-1, sub-tile 1 for sub-tile 0's group gg
-      if (!(ok = __all_sync(0xffffffffu, spin_until_ge(other, S ? gg + 1 : gg, abort)))) break;
+      // sub-tile 0 waits for sub-tile 1's group gg-1, sub-tile 1 for sub-tile 0's group gg.
+      // Sub-tile 0 starts an item's first S without waiting: it then runs on
+      // the tensor core while sub-tile 1 finishes the previous item (its
+      // last, masked softmax and P.V), instead of after it.
+      if ((S == 1 || g > 0) &&
+          !(ok = __all_sync(0xffffffffu, spin_until_ge(other, S ? gg + 1 : gg, abort))))
+        break;
       if (do_pv) {
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_full[S], pph, abort)))) break;
         pph ^= 1;
@@ -527,7 +548,7 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
     ph ^= 2u;
     tc_fence_after_sync();
     const float inv_l = 1.0f / l_run;
-    const int bh = w % (p.B * p.Hq);
+    const int bh = p.div_bh.mod(w);
     uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.S + row) * DH);
     const bool store = row < p.S;
 #pragma unroll
