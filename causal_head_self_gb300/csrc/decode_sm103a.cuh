@@ -247,28 +247,40 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     float m_own = -INFINITY, l_own = 0.f;
     const int lane_off = (warp * KPW + kslot) * ROW + part * 16;   // this lane's chunk
 
-    // one warp step: KPS keys, one per key slot
-    auto step = [&](const uint8_t* kp, const uint8_t* vp, bool valid) {
-      uint4 kw = make_uint4(0, 0, 0, 0), vw = kw;
-      if (valid) {
-        kw = *reinterpret_cast<const uint4*>(kp);
-        vw = *reinterpret_cast<const uint4*>(vp);
-      }
-      float2 k2[4];
-      unpack_chunk(kw, k2);
-      float s[HPB];
+    // One block: this warp's KPW keys, KPS at a time (one per key slot), in
+    // three phases so that the NS independent keys of each phase overlap
+    // their latencies (loads, shuffle reductions, ex2) instead of running
+    // one dependent chain per key: all scores, then one lazy max update for
+    // the lot, then the weights and the V accumulation.
+    constexpr int NS = KPW / KPS;
+    auto do_block = [&](const uint8_t* kp, const uint8_t* vp, int n) {
+      float s_own[NS];
+      bool val[NS];
 #pragma unroll
-      for (int h = 0; h < HPB; ++h) {
-        float2 d = __fmul2_rn(q2[h][0], k2[0]);
+      for (int j = 0; j < NS; ++j) {
+        val[j] = warp * KPW + j * KPS + kslot < n;
+        uint4 kw = make_uint4(0, 0, 0, 0);
+        if (val[j]) kw = *reinterpret_cast<const uint4*>(kp + j * KPS * ROW);
+        float2 k2[4];
+        unpack_chunk(kw, k2);
+        float sh[HPB];
 #pragma unroll
-        for (int i = 1; i < 4; ++i) d = __ffma2_rn(q2[h][i], k2[i], d);
-        s[h] = d.x + d.y;
+        for (int h = 0; h < HPB; ++h) {
+          float2 d = __fmul2_rn(q2[h][0], k2[0]);
+#pragma unroll
+          for (int i = 1; i < 4; ++i) d = __ffma2_rn(q2[h][i], k2[i], d);
+          sh[h] = d.x + d.y;
+        }
+        s_own[j] = key_group_reduce_owned<HPB, LPK>(sh, lane);
       }
-      const float s_own = key_group_reduce_owned<HPB, LPK>(s, lane);
-      const bool grow = valid && s_own > m_own + 8.0f;
+      float smax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < NS; ++j)
+        if (val[j]) smax = fmaxf(smax, s_own[j]);
+      const bool grow = smax > m_own + 8.0f;
       if (__any_sync(0xffffffffu, grow)) {
-        const float corr = grow ? ex2_approx(m_own - s_own) : 1.0f;   // 0 for the first key
-        if (grow) m_own = s_own;
+        const float corr = grow ? ex2_approx(m_own - smax) : 1.0f;   // 0 for the first keys
+        if (grow) m_own = smax;
         l_own *= corr;
 #pragma unroll
         for (int h = 0; h < HPB; ++h) {
@@ -278,16 +290,25 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
           for (int i = 0; i < 4; ++i) acc[h][i] = __fmul2_rn(acc[h][i], c2);
         }
       }
-      const float p_own = valid ? ex2_approx(s_own - m_own) : 0.f;
-      l_own += p_own;
-      float2 v2[4];
-      unpack_chunk(vw, v2);
+      float p_own[NS];
 #pragma unroll
-      for (int h = 0; h < HPB; ++h) {
-        const float pw = __shfl_sync(0xffffffffu, p_own, key_group_owner<HPB, LPK>(h, lane));
-        const float2 p2 = make_float2(pw, pw);
+      for (int j = 0; j < NS; ++j) {
+        p_own[j] = val[j] ? ex2_approx(s_own[j] - m_own) : 0.f;
+        l_own += p_own[j];
+      }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[h][i] = __ffma2_rn(p2, v2[i], acc[h][i]);
+      for (int j = 0; j < NS; ++j) {
+        uint4 vw = make_uint4(0, 0, 0, 0);
+        if (val[j]) vw = *reinterpret_cast<const uint4*>(vp + j * KPS * ROW);
+        float2 v2[4];
+        unpack_chunk(vw, v2);
+#pragma unroll
+        for (int h = 0; h < HPB; ++h) {
+          const float pw = __shfl_sync(0xffffffffu, p_own[j], key_group_owner<HPB, LPK>(h, lane));
+          const float2 p2 = make_float2(pw, pw);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[h][i] = __ffma2_rn(p2, v2[i], acc[h][i]);
+        }
       }
     };
 
@@ -297,14 +318,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
       const int n = min(kDecodeBlockKeys, nkeys - blk * kDecodeBlockKeys);
       const uint8_t* kp = reinterpret_cast<const uint8_t*>(sm.k[st]) + lane_off;
       const uint8_t* vp = reinterpret_cast<const uint8_t*>(sm.v[st]) + lane_off;
-      if (n == kDecodeBlockKeys) {
-#pragma unroll
-        for (int j = 0; j < KPW / KPS; ++j) step(kp + j * KPS * ROW, vp + j * KPS * ROW, true);
-      } else {
-#pragma unroll
-        for (int j = 0; j < KPW / KPS; ++j)
-          step(kp + j * KPS * ROW, vp + j * KPS * ROW, warp * KPW + j * KPS + kslot < n);
-      }
+      if (n == kDecodeBlockKeys)
+        do_block(kp, vp, kDecodeBlockKeys);   // the common, full block (validity folds away)
+      else
+        do_block(kp, vp, n);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[st]);
       if (++st == kDecodeStages) { st = 0; ph ^= 1; }
