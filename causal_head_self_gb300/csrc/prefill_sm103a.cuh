@@ -515,7 +515,7 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
           const float2 xs = __ffma2_rn(make_float2(x[32 * c4 + 2 * e], x[32 * c4 + 2 * e + 1]),
                                        scale2, neg_m2);
           const float2 pp = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
-          ls[e & 1].x += pp.x; ls[e & 1].y += pp.y;
+          ls[e & 1] = __fadd2_rn(ls[e & 1], pp);
           pk[e] = pack_bf16x2(pp.x, pp.y);
         }
         tmem_st_32x32b_x16(colS + 16 * c4, pk);
