@@ -25,7 +25,7 @@ ATTN_ERR_NO_MEMORY = 5
 ATTN_ERR_SCRATCH_LIMIT = 6
 
 # every symbol include/attn.h declares
-ABI_SYMBOLS = ("attn_fwd", "attn_decode", "attn_decode_noalloc", "attn_status",
+ABI_SYMBOLS = ("attn_fwd", "attn_fwd_chunk", "attn_decode", "attn_decode_noalloc", "attn_status",
                "attn_error_string", "attn_version", "attn_debug_inject_fault")
 
 _lib = None
@@ -50,6 +50,8 @@ def load():
             vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             lib.attn_fwd.restype = i
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+            lib.attn_fwd_chunk.restype = i
+            lib.attn_fwd_chunk.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
             lib.attn_decode.restype = i
             lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
             lib.attn_decode_noalloc.restype = i
@@ -107,6 +109,32 @@ def attn_fwd(q, k, v, o=None, *, causal=True, window=0, scale=0.0, stream=None):
                          Dh, int(bool(causal)), int(window), float(scale), _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return o
+
+
+def attn_fwd_chunk(q, kcache, vcache, start_pos, o=None, *, causal=True, window=0, scale=0.0,
+                   stream=None):
+    """Prefill of one chunk against a KV cache.  q [B,Hq,Sq,Dh]; caches
+    [B,Hkv,Tmax,Dh] bf16 already holding the chunk's keys/values at rows
+    start_pos .. start_pos+Sq-1.  Query row r sits at position start_pos + r."""
+    _check_bf16("q", q, 4)
+    _check_bf16("kcache", kcache, 4)
+    _check_bf16("vcache", vcache, 4)
+    B, Hq, Sq, Dh = q.shape
+    Hkv, Tmax = kcache.shape[1], kcache.shape[2]
+    if tuple(kcache.shape) != (B, Hkv, Tmax, Dh) or vcache.shape != kcache.shape:
+        raise ValueError("the caches must be [B, Hkv, Tmax, Dh] matching q")
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _check_bf16("o", o, 4)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    rc = load().attn_fwd_chunk(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), o.data_ptr(), B,
+                               Hq, Hkv, Sq, Tmax, int(start_pos), Dh, int(bool(causal)),
+                               int(window), float(scale), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_chunk")
     return o
 
 

@@ -160,29 +160,48 @@ int attn_debug_inject_fault(int kind) {
   return ATTN_OK;
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int S,
-             int Dh, int causal, int window, float scale, cudaStream_t stream) {
-  if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+// Shared by attn_fwd and attn_fwd_chunk: queries at positions
+// start_pos .. start_pos + Sq - 1 against the first start_pos + Sq of Tkv
+// key/value rows per head.
+static int fwd_common(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                      int Hkv, int Sq, int Tkv, int start_pos, int Dh, int causal, int window,
+                      float scale, cudaStream_t stream) {
+  if (B < 0 || Sq < 0 || Tkv < 0 || start_pos < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)start_pos + Sq > Tkv) return ATTN_ERR_INVALID_ARG;
   if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (window < 0) window = 0;
   if (window > 0 && !causal) return ATTN_ERR_INVALID_ARG;
   float scale_log2 = 0.f;
   if (!resolve_scale(scale, Dh, &scale_log2)) return ATTN_ERR_INVALID_ARG;
-  if (B == 0 || S == 0) return ATTN_OK;
+  if (B == 0 || Sq == 0) return ATTN_OK;
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
-  const size_t qo_bytes = (size_t)B * Hq * S * Dh * 2, kv_bytes = (size_t)B * Hkv * S * Dh * 2;
-  if ((long long)B * Hq * ((S + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  const size_t qo_bytes = (size_t)B * Hq * Sq * Dh * 2, kv_bytes = (size_t)B * Hkv * Tkv * Dh * 2;
+  if ((long long)B * Hq * ((Sq + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, k, kv_bytes) ||
       overlaps(o, qo_bytes, v, kv_bytes))
     return ATTN_ERR_INVALID_ARG;
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
-  cudaError_t e = chs::launch_prefill(q, k, v, o, B, Hq, Hkv, S, Dh, causal, window, scale_log2,
-                                      launch_info(st), stream);
+  cudaError_t e = chs::launch_prefill(q, k, v, o, B, Hq, Hkv, Sq, Tkv, start_pos, Dh, causal,
+                                      window, scale_log2, launch_info(st), stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int S,
+             int Dh, int causal, int window, float scale, cudaStream_t stream) {
+  return fwd_common(q, k, v, o, B, Hq, Hkv, S, S, 0, Dh, causal, window, scale, stream);
+}
+
+int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* o, int B, int Hq,
+                   int Hkv, int Sq, int Tmax, int start_pos, int Dh, int causal, int window,
+                   float scale, cudaStream_t stream) {
+  if (Tmax < 1) return ATTN_ERR_INVALID_ARG;
+  return fwd_common(q, kcache, vcache, o, B, Hq, Hkv, Sq, Tmax, start_pos, Dh, causal, window,
+                    scale, stream);
 }
 
 int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens, void* o,

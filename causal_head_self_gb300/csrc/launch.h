@@ -20,9 +20,13 @@ struct DeviceInfo {
 bool encode_bf16_map(CUtensorMap* map, const void* base, int Dh, int rows, long long outer,
                      int box_rows);
 
+// Queries: Sq rows per (b, h), at positions start_pos .. start_pos + Sq - 1.
+// K, V: Tkv rows per (b, K/V head) in memory, of which the first
+// start_pos + Sq are visible (a plain prefill: Tkv = Sq, start_pos = 0).
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
-                           int Hkv, int S, int Dh, int causal, int window, float scale_log2,
-                           const DeviceInfo& dev, cudaStream_t stream);
+                           int Hkv, int Sq, int Tkv, int start_pos, int Dh, int causal,
+                           int window, float scale_log2, const DeviceInfo& dev,
+                           cudaStream_t stream);
 
 struct DecodePlan {
   int chunk;          // keys per split

@@ -30,22 +30,27 @@ static FastDiv make_fast_div(uint32_t d) {
 }
 
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
-                           int Hkv, int S, int Dh, int causal, int window, float scale_log2,
-                           const DeviceInfo& dev, cudaStream_t stream) {
+                           int Hkv, int Sq, int Tkv, int start_pos, int Dh, int causal,
+                           int window, float scale_log2, const DeviceInfo& dev,
+                           cudaStream_t stream) {
+  // K and V hold Tkv rows per head in memory; the chunk sees the first
+  // start_pos + Sq of them
   CUtensorMap mq, mk, mv;
-  if (!encode_bf16_map(&mq, q, Dh, S, (long long)B * Hq, 128) ||
-      !encode_bf16_map(&mk, k, Dh, S, (long long)B * Hkv, 128) ||
-      !encode_bf16_map(&mv, v, Dh, S, (long long)B * Hkv, 128))
+  if (!encode_bf16_map(&mq, q, Dh, Sq, (long long)B * Hq, 128) ||
+      !encode_bf16_map(&mk, k, Dh, Tkv, (long long)B * Hkv, 128) ||
+      !encode_bf16_map(&mv, v, Dh, Tkv, (long long)B * Hkv, 128))
     return cudaErrorInvalidValue;
   PrefillParams prm;
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
-  prm.S = S;
+  prm.Sq = Sq;
+  prm.Skv = start_pos + Sq;
+  prm.q_off = start_pos;
   prm.causal = causal;
   prm.window = window;
   prm.scale_log2 = scale_log2;
-  prm.num_qblocks = (S + 255) / 256;
+  prm.num_qblocks = (Sq + 255) / 256;
   const long long items = (long long)prm.num_qblocks * B * Hq;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   prm.num_items = (int)items;

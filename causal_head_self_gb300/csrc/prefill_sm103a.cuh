@@ -54,13 +54,16 @@ struct FastDiv {
 };
 
 struct PrefillParams {
-  int B, Hq, Hkv, S;
+  int B, Hq, Hkv;
+  int Sq;       // query rows per (b, h): the chunk
+  int Skv;      // keys visible to the chunk's last query: start position + Sq
+  int q_off;    // absolute position of query row 0 (the chunk's start position)
   int causal;   // 1: key j visible to query i only if j <= i
   int window;   // > 0: also only if i - j < window
   float scale_log2;   // softmax scale * log2(e)
-  int num_qblocks;    // ceil(S / 256)
+  int num_qblocks;    // ceil(Sq / 256)
   int num_items;      // work items: num_qblocks * B * Hq
-  __nv_bfloat16* o;   // output [B, Hq, S, DH]
+  __nv_bfloat16* o;   // output [B, Hq, Sq, DH]
   int o_wide;         // o is 32-byte aligned: 32-byte stores
   int* error_word;    // set to a nonzero status when a wait gives up
   int fault;          // test hook: 1 = the first K tile is never loaded
@@ -101,32 +104,37 @@ struct __align__(1024) PrefillSmem {
   int groups_done[2];   // MMA groups each issuer has issued (orders the two issuers)
 };
 
-// Geometry of one work item.
+// Geometry of one work item.  Query rows are counted within the chunk
+// (0..Sq-1); their positions in the sequence, which the masks compare with
+// key positions, are q_off higher.
 struct PrefillTile {
   int q0;        // first query row of the item
   int lo, hi;    // K/V tile range loaded (union over the two sub-tiles)
-  int S, causal, window;
+  int Sq, Skv, q_off, causal, window;
   __device__ __forceinline__ int row_first(int s) const { return q0 + 128 * s; }
-  __device__ __forceinline__ int row_last(int s) const { return min(q0 + 128 * s + 127, S - 1); }
-  __device__ __forceinline__ bool valid(int s) const { return q0 + 128 * s < S; }
+  __device__ __forceinline__ int pos_first(int s) const { return q_off + q0 + 128 * s; }
+  __device__ __forceinline__ int pos_last(int s) const {
+    return q_off + min(q0 + 128 * s + 127, Sq - 1);
+  }
+  __device__ __forceinline__ bool valid(int s) const { return q0 + 128 * s < Sq; }
   // does sub-tile s see any key of tile j?
   __device__ __forceinline__ bool active(int s, int j) const {
     if (!valid(s)) return false;
-    const int c0 = 128 * j, c1 = min(128 * j + 127, S - 1);
-    if (causal && c0 > row_last(s)) return false;
-    if (window > 0 && c1 < row_first(s) - window + 1) return false;
+    const int c0 = 128 * j, c1 = min(128 * j + 127, Skv - 1);
+    if (causal && c0 > pos_last(s)) return false;
+    if (window > 0 && c1 < pos_first(s) - window + 1) return false;
     return true;
   }
   // offset from lo of the last tile sub-tile s sees (s must be valid)
   __device__ __forceinline__ int last_group(int s) const {
-    return (causal ? min(hi, row_last(s) / 128) : hi) - lo;
+    return (causal ? min(hi, pos_last(s) / 128) : hi) - lo;
   }
   // is any (row, key) pair of sub-tile s x tile j masked?
   __device__ __forceinline__ bool needs_mask(int s, int j) const {
     const int c0 = 128 * j, c1 = 128 * j + 127;
-    if (c1 >= S) return true;
-    if (causal && c1 > row_first(s)) return true;
-    if (window > 0 && c0 < row_last(s) - window + 1) return true;
+    if (c1 >= Skv) return true;
+    if (causal && c1 > pos_first(s)) return true;
+    if (window > 0 && c0 < pos_last(s) - window + 1) return true;
     return false;
   }
 };
@@ -134,13 +142,15 @@ struct PrefillTile {
 __device__ __forceinline__ PrefillTile prefill_tile_of(const PrefillParams& p, int qb) {
   PrefillTile t;
   t.q0 = qb * 256;
-  t.S = p.S;
+  t.Sq = p.Sq;
+  t.Skv = p.Skv;
+  t.q_off = p.q_off;
   t.causal = p.causal;
   t.window = p.window;
-  const int nkv = (p.S + 127) / 128;
-  const int last_row = min(t.q0 + 255, p.S - 1);
-  t.hi = p.causal ? min(nkv - 1, last_row / 128) : nkv - 1;
-  t.lo = (p.causal && p.window > 0) ? max(0, t.q0 - p.window + 1) / 128 : 0;
+  const int nkv = (p.Skv + 127) / 128;
+  const int last_pos = p.q_off + min(t.q0 + 255, p.Sq - 1);
+  t.hi = p.causal ? min(nkv - 1, last_pos / 128) : nkv - 1;
+  t.lo = (p.causal && p.window > 0) ? max(0, p.q_off + t.q0 - p.window + 1) / 128 : 0;
   return t;
 }
 
@@ -421,7 +431,7 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
     if (w >= p.num_items) break;
     const PrefillTile tile = prefill_item_of(p, w).tile;
     if (!tile.valid(s)) continue;           // a ragged last block: no rows here
-    const int row = tile.row_first(s) + t;  // absolute query row
+    const int row = tile.pos_first(s) + t;  // this thread's query position
 
     float m_run = -INFINITY;   // running max of scale*log2e*score (lazily updated)
     float l_run = 0.f;         // running sum of exp2(x - m_run)
@@ -443,7 +453,7 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
         // (a predicated select, never a branch).  A rolled loop keeps this
         // rarely run code small.
         const int kv0 = 128 * j;
-        int khi = tile.S - 1;
+        int khi = tile.Skv - 1;
         if (tile.causal) khi = min(khi, row);
         const int klo = tile.window > 0 ? row - tile.window + 1 : 0;
         int clo = klo - kv0;
@@ -549,8 +559,9 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
     tc_fence_after_sync();
     const float inv_l = 1.0f / l_run;
     const int bh = p.div_bh.mod(w);
-    uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.S + row) * DH);
-    const bool store = row < p.S;
+    const int orow = tile.row_first(s) + t;  // output row within the chunk
+    uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.Sq + orow) * DH);
+    const bool store = orow < p.Sq;
 #pragma unroll
     for (int c = 0; c < DH / 32; c += 2) {
       uint32_t o0[32], o1[32];

@@ -73,6 +73,29 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq
              int S, int Dh, int causal, int window, float scale, cudaStream_t stream);
 
 /*
+ * attn_fwd_chunk -- prefill of one chunk against a KV cache ("Механизм
+ * внимания", section "Prefill и decode": a long prompt may be fed in chunks;
+ * the chunk's keys and values are written into the cache first, then its
+ * queries attend to everything cached before them and to the chunk).
+ *   q       [B, Hq, Sq, Dh]     the chunk's queries        (device, bf16, read)
+ *   kcache  [B, Hkv, Tmax, Dh]  cached keys                (device, bf16, read)
+ *   vcache  [B, Hkv, Tmax, Dh]  cached values              (device, bf16, read)
+ *   o       [B, Hq, Sq, Dh]     output                     (device, bf16, written;
+ *                                                           must not overlap the others)
+ *   start_pos  position of the chunk's first token; the chunk's own keys
+ *              are cache rows start_pos .. start_pos + Sq - 1, and only rows
+ *              [0, start_pos + Sq) are read (0 <= start_pos, start_pos + Sq <= Tmax).
+ * Query row r sits at position start_pos + r and, with causal = 1, sees keys
+ * 0 .. start_pos + r (the window, if any, as in attn_fwd); with causal = 0
+ * every key 0 .. start_pos + Sq - 1.  start_pos = 0 and Tmax = Sq is exactly
+ * attn_fwd (the same kernel and bits).  Errors and the empty case (B == 0 or
+ * Sq == 0) as in attn_fwd.
+ */
+int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* o, int B, int Hq,
+                   int Hkv, int Sq, int Tmax, int start_pos, int Dh, int causal, int window,
+                   float scale, cudaStream_t stream);
+
+/*
  * attn_decode -- one KV-cache decode step ("Механизм внимания", section
  * "Prefill и decode": the new token's key and value are appended to the
  * cache first, then its query meets every cached key, its own included).
