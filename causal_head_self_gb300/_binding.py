@@ -25,7 +25,8 @@ ATTN_ERR_NO_MEMORY = 5
 ATTN_ERR_SCRATCH_LIMIT = 6
 
 # every symbol include/attn.h declares
-ABI_SYMBOLS = ("attn_fwd", "attn_fwd_chunk", "attn_decode", "attn_decode_noalloc", "attn_status",
+ABI_SYMBOLS = ("attn_fwd", "attn_fwd_chunk", "attn_decode", "attn_decode_ring", "attn_decode_noalloc",
+               "attn_status",
                "attn_error_string", "attn_version", "attn_debug_inject_fault")
 
 _lib = None
@@ -54,6 +55,8 @@ def load():
             lib.attn_fwd_chunk.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
             lib.attn_decode.restype = i
             lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+            lib.attn_decode_ring.restype = i
+            lib.attn_decode_ring.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
             lib.attn_decode_noalloc.restype = i
             lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
             lib.attn_status.restype = i
@@ -162,6 +165,34 @@ def attn_decode(q, kcache, vcache, seqlens, o=None, *, window=0, scale=0.0, stre
                             _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode")
+    return o
+
+
+def attn_decode_ring(q, kcache, vcache, seqlens, o=None, *, window=0, scale=0.0, stream=None):
+    """Decode step over a rolling-buffer cache [B,Hkv,C,Dh]: position t of
+    sequence b at row t % C; seqlens [B] int32 = tokens so far (see
+    include/attn.h)."""
+    _check_bf16("q", q, 4)
+    _check_bf16("kcache", kcache, 4)
+    _check_bf16("vcache", vcache, 4)
+    B, Hq, one, Dh = q.shape
+    Hkv, C = kcache.shape[1], kcache.shape[2]
+    if one != 1 or tuple(kcache.shape) != (B, Hkv, C, Dh) or vcache.shape != kcache.shape:
+        raise ValueError("q must be [B,Hq,1,Dh] and the caches [B,Hkv,C,Dh]")
+    if (not isinstance(seqlens, torch.Tensor) or seqlens.dtype != torch.int32 or not seqlens.is_cuda
+            or seqlens.numel() != B or not seqlens.is_contiguous()):
+        raise TypeError("seqlens must be a contiguous CUDA int32 tensor of B entries")
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _check_bf16("o", o, 4)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    rc = load().attn_decode_ring(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                 seqlens.data_ptr(), o.data_ptr(), B, Hq, Hkv, C, Dh, int(window),
+                                 float(scale), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_ring")
     return o
 
 

@@ -204,12 +204,14 @@ int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* 
                     scale, stream);
 }
 
-int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens, void* o,
-                int B, int Hq, int Hkv, int Tmax, int Dh, int window, float scale,
-                cudaStream_t stream) {
+// Shared by attn_decode (ring = 0) and attn_decode_ring (ring = 1).
+static int decode_common(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                         void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window, int ring,
+                         float scale, cudaStream_t stream) {
   if (B < 0 || Tmax < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
   if (window < 0) window = 0;
+  if (ring && window > Tmax) return ATTN_ERR_INVALID_ARG;   // the ring holds Tmax positions
   float scale_log2 = 0.f;
   if (!resolve_scale(scale, Dh, &scale_log2)) return ATTN_ERR_INVALID_ARG;
   if (B == 0) return ATTN_OK;
@@ -247,9 +249,22 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
     counters = st->counters;
   }
   cudaError_t e = chs::launch_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, window,
-                                     scale_log2, plan, counters, partials, launch_info(st),
+                                     ring, scale_log2, plan, counters, partials, launch_info(st),
                                      stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens, void* o,
+                int B, int Hq, int Hkv, int Tmax, int Dh, int window, float scale,
+                cudaStream_t stream) {
+  return decode_common(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, window, 0, scale,
+                       stream);
+}
+
+int attn_decode_ring(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                     void* o, int B, int Hq, int Hkv, int C, int Dh, int window, float scale,
+                     cudaStream_t stream) {
+  return decode_common(q, kcache, vcache, seqlens, o, B, Hq, Hkv, C, Dh, window, 1, scale, stream);
 }
 
 int attn_status(cudaStream_t stream) {
@@ -332,7 +347,7 @@ extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void
   if (cudaMemsetAsync(counters, 0, n_counters * sizeof(int), stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   cudaError_t e = chs::launch_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, window,
-                                     scale_log2, plan, counters, scratch + counter_bytes,
+                                     0, scale_log2, plan, counters, scratch + counter_bytes,
                                      launch_info(st), stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

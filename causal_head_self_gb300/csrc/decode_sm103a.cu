@@ -77,7 +77,7 @@ static cudaError_t launch_hpb(const DecodeParams& prm, int hpb, cudaStream_t str
 
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int* seqlens,
                           void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,
-                          float scale_log2, const DecodePlan& plan, int* counters,
+                          int ring, float scale_log2, const DecodePlan& plan, int* counters,
                           void* partials, const DeviceInfo& dev, cudaStream_t stream) {
   DecodeParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
@@ -101,6 +101,7 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
   prm.scale_log2 = scale_log2;
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
+  prm.ring = ring;
   return Dh == 128 ? launch_hpb<128>(prm, plan.heads_per_cta, stream)
                    : launch_hpb<64>(prm, plan.heads_per_cta, stream);
 }

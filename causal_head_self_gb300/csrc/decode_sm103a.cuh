@@ -44,6 +44,7 @@ struct DecodeParams {
   float scale_log2;
   int* error_word;
   int fault;                // test hook: 2 = the first key block is never loaded
+  int ring;                 // 1: the Tmax cache rows are a ring, position t at row t % Tmax
 };
 
 constexpr int kDecodeBlockKeys = 32;    // keys per pipeline stage
@@ -64,12 +65,33 @@ struct __align__(128) DecodeSmem {
   int is_last;
 };
 
-// keys [k_begin, k_end) of split `split`, for a sequence of L keys
-__device__ __forceinline__ void decode_split_range(int L, int window, int split, int chunk,
+// The visible key positions of a sequence of L tokens are [lo, L); splits
+// are `chunk` positions wide, counted from `base`.  A linear cache counts
+// them from position 0 (fixed split boundaries); a ring, whose positions
+// grow without bound, from lo.
+struct DecodeSpan {
+  int lo, base;
+};
+
+__device__ __forceinline__ DecodeSpan decode_span(const DecodeParams& p, int L) {
+  DecodeSpan d;
+  if (p.ring) {
+    const int w = p.window > 0 ? p.window : p.Tmax;   // <= Tmax, checked on the host
+    d.lo = max(0, L - w);
+    d.base = d.lo;
+  } else {
+    d.lo = p.window > 0 ? max(0, L - p.window) : 0;
+    d.base = 0;
+  }
+  return d;
+}
+
+// keys [k_begin, k_end) of split `split`
+__device__ __forceinline__ void decode_split_range(const DecodeSpan& d, int L, int split, int chunk,
                                                    int& k_begin, int& k_end) {
-  const int lo = window > 0 ? max(0, L - window) : 0;
-  k_begin = max(split * chunk, lo);
-  k_end = min((split + 1) * chunk, L);
+  // (64-bit: a ring's positions may come close to 2^31)
+  k_begin = (int)max((long long)d.base + (long long)split * chunk, (long long)d.lo);
+  k_end = (int)min((long long)d.base + (long long)(split + 1) * chunk, (long long)L);
 }
 
 // bf16 pair (low half = lower-addressed element) -> float2
@@ -167,7 +189,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   const int b = blockIdx.z;
   const int hq0 = g * (p.Hq / p.Hkv) + hsub * HPB;   // first query head of this CTA
   const int L = p.seqlens[b];
-  if (L < 1 || L > p.Tmax) {
+  if (L < 1 || (!p.ring && L > p.Tmax)) {
     // a sequence length outside [1, Tmax]: zero output, latch the error
     if (split == 0) {
       for (int i = threadIdx.x; i < HPB * DH; i += blockDim.x)
@@ -177,7 +199,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     return;
   }
   int k_begin, k_end;
-  decode_split_range(L, p.window, split, p.chunk, k_begin, k_end);
+  const DecodeSpan span = decode_span(p, L);
+  decode_split_range(span, L, split, p.chunk, k_begin, k_end);
   if (k_begin >= k_end) return;      // this split holds no visible key
   const int nkeys = k_end - k_begin;
   const int nblk = (nkeys + kDecodeBlockKeys - 1) / kDecodeBlockKeys;
@@ -196,22 +219,33 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   if (warp == kDecodeConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const size_t row0 = ((size_t)b * p.Hkv + g) * p.Tmax + k_begin;
-      const uint8_t* kg = reinterpret_cast<const uint8_t*>(p.kc) + row0 * ROW;
-      const uint8_t* vg = reinterpret_cast<const uint8_t*>(p.vc) + row0 * ROW;
+      const size_t head0 = ((size_t)b * p.Hkv + g) * p.Tmax;   // row 0 of this head
+      const uint8_t* kg = reinterpret_cast<const uint8_t*>(p.kc) + head0 * ROW;
+      const uint8_t* vg = reinterpret_cast<const uint8_t*>(p.vc) + head0 * ROW;
       const uint64_t stream_once = policy_evict_first();
+      // cache row of the block's first key (a linear cache never wraps)
+      int row = p.ring ? k_begin % p.Tmax : k_begin;
       uint32_t st = 0, ph = 0, loaded = 0, par = 0;
       for (int blk = 0; blk < nblk; ++blk) {
         const int n = min(kDecodeBlockKeys, nkeys - blk * kDecodeBlockKeys);
         if (!mbar_wait(&sm.empty[st], ph ^ 1, abort)) break;
         if (p.fault != 2 || blk != 0) {   // (the test hook withholds one block)
           mbar_arrive_expect_tx(&sm.full[st], 2u * n * ROW);
-          const size_t off = (size_t)blk * kDecodeBlockKeys * ROW;
-          bulk_load(sm.k[st], kg + off, n * ROW, &sm.full[st], stream_once);
-          bulk_load(sm.v[st], vg + off, n * ROW, &sm.full[st], stream_once);
+          // a block that runs past the end of a ring continues at row 0
+          const int n1 = min(n, p.Tmax - row);
+          bulk_load(sm.k[st], kg + (size_t)row * ROW, n1 * ROW, &sm.full[st], stream_once);
+          bulk_load(sm.v[st], vg + (size_t)row * ROW, n1 * ROW, &sm.full[st], stream_once);
+          if (n1 < n) {   // (offsets in bytes: the stage arrays hold bf16 elements)
+            bulk_load(reinterpret_cast<uint8_t*>(sm.k[st]) + n1 * ROW, kg, (n - n1) * ROW,
+                      &sm.full[st], stream_once);
+            bulk_load(reinterpret_cast<uint8_t*>(sm.v[st]) + n1 * ROW, vg, (n - n1) * ROW,
+                      &sm.full[st], stream_once);
+          }
           loaded |= 1u << st;
           par = (par & ~(1u << st)) | (ph << st);
         }
+        row += n;
+        if (row >= p.Tmax) row -= p.Tmax;
         if (++st == kDecodeStages) { st = 0; ph ^= 1; }
       }
       // every copy this thread started has landed before the CTA may exit
@@ -368,8 +402,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     }
     named_bar_sync(1, 32 * kDecodeConsumerWarps);
 
-    const int lo = p.window > 0 ? max(0, L - p.window) : 0;
-    const int s_first = lo / p.chunk, s_last = (L - 1) / p.chunk;
+    const int s_first = (span.lo - span.base) / p.chunk, s_last = (L - 1 - span.base) / p.chunk;
     const bool single = s_first == s_last;   // the whole key range is this CTA's
     // merge the warps: this CTA's result for each (head, d)
     for (int idx = threadIdx.x; idx < HPB * DH; idx += 32 * kDecodeConsumerWarps) {

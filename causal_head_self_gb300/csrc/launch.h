@@ -44,9 +44,11 @@ size_t decode_partials_bytes(int B, int Hq, int Dh, const DecodePlan& plan);
 // buffer that only ever holds counters stays valid across calls and shapes.
 size_t decode_counter_count(int B, int Hq, int Hkv, const DecodePlan& plan);
 
+// ring = 1: the Tmax cache rows of a head hold position t at row t % Tmax
+// (the last Tmax positions of an unbounded sequence).
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int* seqlens,
                           void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,
-                          float scale_log2, const DecodePlan& plan, int* counters,
+                          int ring, float scale_log2, const DecodePlan& plan, int* counters,
                           void* partials, const DeviceInfo& dev, cudaStream_t stream);
 
 }  // namespace chs

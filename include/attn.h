@@ -122,6 +122,26 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
                 cudaStream_t stream);
 
 /*
+ * attn_decode_ring -- the decode step over a rolling-buffer cache
+ * ("Механизм внимания", section "Скользящее окно": with a window the cache
+ * need only hold the last W positions, and a ring buffer does that).
+ *   kcache, vcache [B, Hkv, C, Dh]: position t of sequence b is at row t % C
+ *                  (the last min(seqlens[b], C) positions are held).
+ *   seqlens [B]    tokens of sequence b so far, own token included (>= 1,
+ *                  any size below 2^31 - C); the query sits at position
+ *                  seqlens[b] - 1.
+ *   window         W <= C: keys [seqlens[b] - W, seqlens[b]) are visible;
+ *                  window <= 0 means W = C (every held position).
+ *                  window > C is ATTN_ERR_INVALID_ARG.
+ * Other arguments, the workspace and the errors as in attn_decode.  While a
+ * sequence has not wrapped (seqlens[b] <= C) and window <= 0 the result is
+ * bit-identical to attn_decode on the same buffers.
+ */
+int attn_decode_ring(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                     void* o, int B, int Hq, int Hkv, int C, int Dh, int window, float scale,
+                     cudaStream_t stream);
+
+/*
  * attn_decode_noalloc -- the same decode step as attn_decode (same arguments,
  * same result up to rounding, same errors), for callers that must not
  * allocate device memory.  The pages describe no such call; it exists for
