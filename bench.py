@@ -224,6 +224,27 @@ def time_oracle(prefill_host, decode_host, w_p, w_d, prefill_heads=None, decode_
 
 # ------------------------------------------------------------------ arms
 
+# ------------------------------------------------------------------ ranks (N > 1)
+
+def rank_seed(seed, rank):
+    """Weak scaling: every rank runs its own, independent batch."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(values, world, device=None):
+    """The slowest rank's times (the job ends when it does); identity at N=1."""
+    if world <= 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(work_per_rank, seconds_slowest, world):
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return work_per_rank * world / seconds_slowest
+
+
 def run_reference(args, rank, world):
     """The oracle on the host cores, as the reference arm."""
     if rank != 0:
@@ -272,10 +293,10 @@ def run_gpu(args, rank, world, local_rank):
     w_p, w_d = inputs.WORKLOADS[PREFILL], inputs.WORKLOADS[DECODE]
     # weak scaling: every rank runs its own batch (seeds differ per rank)
     qh, kh, vh = inputs.prefill_inputs(w_p["B"], w_p["Hq"], w_p["Hkv"], w_p["S"], w_p["Dh"],
-                                       w_p["seed"] + 1000 * rank)
+                                       rank_seed(w_p["seed"], rank))
     qdh, kch, vch, slh = inputs.decode_inputs(w_d["B"], w_d["Hq"], w_d["Hkv"], w_d["Tmax"],
                                               w_d["Dh"], w_d["lmin"], w_d["lmax"],
-                                              w_d["seed"] + 1000 * rank)
+                                              rank_seed(w_d["seed"], rank))
     q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
     o = torch.empty_like(q)
     qd, kc, vc, sl = qdh.to(dev), kch.to(dev), vch.to(dev), slh.to(dev)
@@ -320,10 +341,7 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device error in the timed region: {status}")
     t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3   # seconds
     t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
-    if world > 1:
-        t = torch.tensor([t_pre, t_dec, t_wall], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_pre, t_dec, t_wall = t.tolist()
+    t_pre, t_dec, t_wall = max_over_ranks([t_pre, t_dec, t_wall], world, dev)
 
     # ---------------------------------------------------------- end to end (host buffers)
     e2e_steps = max(3, min(20, args.steps))
@@ -356,10 +374,7 @@ def run_gpu(args, rank, world, local_rank):
     if chs.attn_status() != chs.ATTN_OK:
         raise RuntimeError("device error in the end-to-end loop")
     tp_e2e, td_e2e = statistics.mean(e2e_p), statistics.mean(e2e_d)
-    if world > 1:
-        t = torch.tensor([tp_e2e, td_e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tp_e2e, td_e2e = t.tolist()
+    tp_e2e, td_e2e = max_over_ranks([tp_e2e, td_e2e], world, dev)
     if rank != 0:
         return None
 
@@ -395,7 +410,7 @@ def run_gpu(args, rank, world, local_rank):
                "seconds": sec, "decode_value": d_gbs, "decode_unit": "GB/s"}
 
     return {
-        "impl": "gb300", "metric": METRIC, "value": pre_tflops * world, "unit": "TFLOP/s",
+        "impl": "gb300", "metric": METRIC, "value": job_rate(pf, pre_launch, world) / 1e12, "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": (t_pre + t_dec) / K * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -410,16 +425,16 @@ def run_gpu(args, rank, world, local_rank):
                          "prefill_bf16_sustained": pre_tflops / peaks["bf16_tflops_sustained"],
                          "decode_hbm": dec_gbs / peaks["hbm_gbs"],
                          "decode_hbm_8TBps_spec": dec_gbs / 8000.0, "peaks": peak_src},
-        "decode": {"value": dec_gbs * world, "unit": "GB/s",
+        "decode": {"value": job_rate(db, dec_launch, world) / 1e9, "unit": "GB/s",
                    "tokens_per_s": w_d["B"] * world / dec_launch,
                    "tflops": dfl / dec_launch / 1e12 * world, "ms_per_launch": dec_launch * 1e3},
         "roofline": dominant,
         "rooflines": {"prefill": roof_p, "decode": roof_d},
         "cpu_baseline": cpu,
-        "e2e": {"value": pf / tp_e2e / 1e12 * world, "unit": "TFLOP/s",
+        "e2e": {"value": job_rate(pf, tp_e2e, world) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (qh, kh, vh)),
                 "d2h_bytes_per_step": o.numel() * o.element_size(),
-                "decode": {"value": db / td_e2e / 1e9 * world, "unit": "GB/s",
+                "decode": {"value": job_rate(db, td_e2e, world) / 1e9, "unit": "GB/s",
                            "h2d_bytes_per_step": sum(x.numel() * x.element_size()
                                                      for x in (qdh, kch, vch, slh)),
                            "d2h_bytes_per_step": od.numel() * od.element_size()}},
