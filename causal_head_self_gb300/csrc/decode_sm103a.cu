@@ -5,21 +5,21 @@
 namespace chs {
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int Tmax, int Dh, int num_sms) {
-  (void)Dh;
   DecodePlan plan;
+  const long long bk = Dh == 64 ? decode_block_keys<64>() : decode_block_keys<128>();
   const int group = Hq / Hkv;
   plan.heads_per_cta = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
   const long long ctas_per_split = (long long)B * Hkv * (group / plan.heads_per_cta);
   // aim for about eight waves of resident CTAs over the whole cache, in
-  // whole 32-key blocks, between 256 and 4096 keys per split, <= 64 splits
+  // whole blocks, between 256 and 4096 keys per split, <= 64 splits
   const long long want = 8LL * kDecodeCtasPerSm * num_sms;
   long long per_split_keys = (long long)Tmax * ctas_per_split / (want > 0 ? want : 1);
-  long long chunk = (per_split_keys + kDecodeBlockKeys - 1) / kDecodeBlockKeys * kDecodeBlockKeys;
+  long long chunk = (per_split_keys + bk - 1) / bk * bk;
   if (chunk < 256) chunk = 256;
   if (chunk > 4096) chunk = 4096;
   long long nsplit = (Tmax + chunk - 1) / chunk;
   if (nsplit > 64) {
-    chunk = ((Tmax + 63) / 64 + kDecodeBlockKeys - 1) / kDecodeBlockKeys * kDecodeBlockKeys;
+    chunk = ((Tmax + 63) / 64 + bk - 1) / bk * bk;
     nsplit = (Tmax + chunk - 1) / chunk;
   }
   plan.chunk = (int)chunk;
@@ -63,7 +63,7 @@ static cudaError_t launch_dh(const DecodeParams& prm, cudaStream_t stream) {
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   const int groups = (prm.Hq / prm.Hkv) / HPB;
-  dim3 grid(prm.nsplit, prm.Hkv * groups, prm.B);
+  dim3 grid(prm.Hkv * groups, prm.nsplit, prm.B);
   kernel<<<grid, kDecodeThreads, smem, stream>>>(prm);
   return cudaGetLastError();
 }

@@ -7,7 +7,7 @@
 // sections "KV-кэш", "Prefill и decode" and "Скользящее окно").  The step reads
 // the whole cache for little arithmetic, so it is bound by HBM bandwidth.
 //
-// One kernel, grid (nsplit, Hkv * groups, B).  A CTA takes `chunk` keys of one
+// One kernel, grid (Hkv * groups, nsplit, B).  A CTA takes `chunk` keys of one
 // (b, K/V head) and the HPB query heads of that head's GQA group it holds, so
 // each cached byte is read from HBM once per group.  One producer thread
 // streams 32-key blocks of K and V into a four-stage shared-memory ring with
@@ -47,7 +47,12 @@ struct DecodeParams {
   int ring;                 // 1: the Tmax cache rows are a ring, position t at row t % Tmax
 };
 
-constexpr int kDecodeBlockKeys = 32;    // keys per pipeline stage
+constexpr int kDecodeBlockKeys = 32;    // keys per pipeline stage at Dh = 128
+// Keys per pipeline stage: 8 KiB of K and 8 KiB of V per stage at either head
+// size, so that as many bytes are in flight (at Dh = 64, 32-key stages kept
+// too few bytes in flight to cover the HBM latency).
+template <int DH>
+__host__ __device__ constexpr int decode_block_keys() { return kDecodeBlockKeys * 128 / DH; }
 constexpr int kDecodeStages = 4;
 constexpr int kDecodeConsumerWarps = 4;
 constexpr int kDecodeThreads = 32 * (kDecodeConsumerWarps + 1);
@@ -55,8 +60,8 @@ constexpr int kDecodeCtasPerSm = 3;
 
 template <int DH, int HPB>
 struct __align__(128) DecodeSmem {
-  __nv_bfloat16 k[kDecodeStages][kDecodeBlockKeys * DH];
-  __nv_bfloat16 v[kDecodeStages][kDecodeBlockKeys * DH];
+  __nv_bfloat16 k[kDecodeStages][decode_block_keys<DH>() * DH];
+  __nv_bfloat16 v[kDecodeStages][decode_block_keys<DH>() * DH];
   float red_o[kDecodeConsumerWarps][HPB][DH];
   float red_m[kDecodeConsumerWarps][HPB];
   float red_l[kDecodeConsumerWarps][HPB];
@@ -174,7 +179,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     attn_decode_sm103a(const DecodeParams p) {
   constexpr int LPK = DH / 8;           // lanes per key (one 16-byte chunk each)
   constexpr int KPS = 32 / LPK;         // keys per warp step
-  constexpr int KPW = kDecodeBlockKeys / kDecodeConsumerWarps;   // keys per warp per block
+  constexpr int BK = decode_block_keys<DH>();   // keys per block
+  constexpr int KPW = BK / kDecodeConsumerWarps;   // keys per warp per block
   constexpr int ROW = DH * 2;           // bytes per cached row
   using Smem = DecodeSmem<DH, HPB>;
   extern __shared__ uint8_t smem_raw[];
@@ -182,10 +188,13 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
                                       ~uintptr_t(127));
   volatile int* abort = &sm.abort_flag;
 
-  const int split = blockIdx.x;
+  // grid (head groups, splits, B): the CTAs of one split -- the query-head
+  // groups that read the same K/V rows when Hq / Hkv exceeds 4 (MQA) -- are
+  // launched side by side, so the rows come from L2 after the first read
+  const int split = blockIdx.y;
   const int groups = (p.Hq / p.Hkv) / HPB;
-  const int g = blockIdx.y / groups;
-  const int hsub = blockIdx.y % groups;
+  const int g = blockIdx.x / groups;
+  const int hsub = blockIdx.x % groups;
   const int b = blockIdx.z;
   const int hq0 = g * (p.Hq / p.Hkv) + hsub * HPB;   // first query head of this CTA
   const int L = p.seqlens[b];
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   decode_split_range(span, L, split, p.chunk, k_begin, k_end);
   if (k_begin >= k_end) return;      // this split holds no visible key
   const int nkeys = k_end - k_begin;
-  const int nblk = (nkeys + kDecodeBlockKeys - 1) / kDecodeBlockKeys;
+  const int nblk = (nkeys + BK - 1) / BK;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
       int row = p.ring ? k_begin % p.Tmax : k_begin;
       uint32_t st = 0, ph = 0, loaded = 0, par = 0;
       for (int blk = 0; blk < nblk; ++blk) {
-        const int n = min(kDecodeBlockKeys, nkeys - blk * kDecodeBlockKeys);
+        const int n = min(BK, nkeys - blk * BK);
         if (!mbar_wait(&sm.empty[st], ph ^ 1, abort)) break;
         if (p.fault != 2 || blk != 0) {   // (the test hook withholds one block)
           mbar_arrive_expect_tx(&sm.full[st], 2u * n * ROW);
@@ -349,11 +358,11 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     uint32_t st = 0, ph = 0;
     for (int blk = 0; blk < nblk; ++blk) {
       if (!mbar_wait(&sm.full[st], ph, abort)) break;
-      const int n = min(kDecodeBlockKeys, nkeys - blk * kDecodeBlockKeys);
+      const int n = min(BK, nkeys - blk * BK);
       const uint8_t* kp = reinterpret_cast<const uint8_t*>(sm.k[st]) + lane_off;
       const uint8_t* vp = reinterpret_cast<const uint8_t*>(sm.v[st]) + lane_off;
-      if (n == kDecodeBlockKeys)
-        do_block(kp, vp, kDecodeBlockKeys);   // the common, full block (validity folds away)
+      if (n == BK)
+        do_block(kp, vp, BK);   // the common, full block (validity folds away)
       else
         do_block(kp, vp, n);
       __syncwarp();
@@ -435,7 +444,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
       // the last CTA of this (b, K/V head, group) to get here merges all splits
       __threadfence();
       named_bar_sync(1, 32 * kDecodeConsumerWarps);
-      int* counter = p.counters + (size_t)b * gridDim.y + blockIdx.y;
+      int* counter = p.counters + (size_t)b * gridDim.x + blockIdx.x;
       if (threadIdx.x == 0) {
         const int prev = atomicAdd(counter, 1);
         sm.is_last = prev == s_last - s_first;
