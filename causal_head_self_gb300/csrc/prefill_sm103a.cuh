@@ -80,7 +80,7 @@ struct PrefillCfg {
   static constexpr int kHalves = DH / 64;            // 128-byte swizzle boxes across DH
   static constexpr int kBoxBytes = 128 * 64 * 2;     // one 128 x 64 bf16 box
   static constexpr int kTileBytes = kHalves * kBoxBytes;
-  static constexpr int kStagesK = DH == 128 ? 3 : 4;
+  static constexpr int kStagesK = DH == 128 ? 2 : 4;
   static constexpr int kStagesV = DH == 128 ? 2 : 4;
   static constexpr int kThreads = 352;
   static constexpr int kWarpProducer = 9;
