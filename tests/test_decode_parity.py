@@ -94,3 +94,20 @@ def test_workload_decode_b16_all_rows():
     o = gpu_decode(q, kc, vc, sl, window=w["window"])
     ref = oracle.decode(q, kc, vc, sl, window=w["window"])
     assert_close(o.float().cpu().numpy(), ref, what=name)
+
+
+def test_empty_batch_is_a_no_op():
+    d = torch.device("cuda")
+    q = torch.empty((0, 8, 1, 128), dtype=torch.bfloat16, device=d)
+    kc = torch.empty((0, 2, 64, 128), dtype=torch.bfloat16, device=d)
+    sl = torch.empty((0,), dtype=torch.int32, device=d)
+    o = chs.attn_decode(q, kc, kc.clone(), sl)
+    assert o.shape == q.shape
+    assert chs.attn_status() == chs.ATTN_OK
+
+
+def test_many_sequences_with_one_key_each():
+    """B = 300 sequences of one cached key: the output is that key's value."""
+    q, kc, vc, sl = inputs.decode_inputs(300, 4, 1, 32, 64, 1, 1, seed=52)
+    o = gpu_decode(q, kc, vc, sl).cpu()
+    assert torch.equal(o, vc[:, :1].repeat_interleave(4, dim=1)[:, :, :1])

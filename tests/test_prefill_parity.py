@@ -186,3 +186,21 @@ def test_workload_mha_s4096_noncausal_sampled():
 
 def test_workload_gqa_s32768_window_sampled():
     _full("prefill_gqa_b1_h32kv8_s32768_d128_w4096", 64, (0, 4095, 4096, 4097, 8191, 32767))
+
+
+def test_empty_batch_or_sequence_is_a_no_op():
+    d = torch.device("cuda")
+    for shape_q, shape_kv in (((0, 4, 16, 128), (0, 2, 16, 128)), ((2, 4, 0, 128), (2, 2, 0, 128))):
+        q = torch.empty(shape_q, dtype=torch.bfloat16, device=d)
+        k = torch.empty(shape_kv, dtype=torch.bfloat16, device=d)
+        o = chs.attn_fwd(q, k, k.clone())
+        assert o.shape == q.shape
+    assert chs.attn_status() == chs.ATTN_OK
+
+
+def test_many_tiny_items_all_rows():
+    """300 work items of a handful of rows each: every CTA runs two, on
+    ragged single tiles."""
+    q, k, v = inputs.prefill_inputs(50, 6, 2, 5, 128, seed=51)
+    o = gpu_fwd(q, k, v, 1, 0)
+    assert_close(o.float().cpu().numpy(), oracle.attention(q, k, v, causal=True))
