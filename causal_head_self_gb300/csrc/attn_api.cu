@@ -155,7 +155,7 @@ static chs::DeviceInfo launch_info(const DeviceState* st) {
 }
 
 int attn_debug_inject_fault(int kind) {
-  if (kind < 0 || kind > 2) return ATTN_ERR_INVALID_ARG;
+  if (kind < 0 || kind > 3) return ATTN_ERR_INVALID_ARG;
   g_fault.store(kind, std::memory_order_relaxed);
   return ATTN_OK;
 }
@@ -229,6 +229,23 @@ static int decode_common(const void* q, const void* kcache, const void* vcache, 
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
+  if (!ring && Hq / Hkv >= chs::kDecodeTcMinGroup) {
+    // many query heads per cached byte: the tensor-core path (a contraction)
+    const chs::DecodePlan plan = chs::plan_decode_tc(B, Hq, Hkv, Tmax, st->info.num_sms);
+    if ((long long)B * Hkv * ((Hq / Hkv + 127) / 128) > 65535) return ATTN_ERR_INVALID_ARG;
+    void* partials = nullptr;
+    {
+      std::lock_guard<std::mutex> lock(g_mutex);
+      rc = grow_buffer(&st->partials, &st->partials_bytes,
+                       chs::decode_partials_bytes(B, Hq, Dh, plan), false, stream);
+      if (rc != ATTN_OK) return rc;
+      partials = st->partials;
+    }
+    cudaError_t e = chs::launch_decode_tc(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh,
+                                          window, scale_log2, plan, partials, launch_info(st),
+                                          stream);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
   const chs::DecodePlan plan = chs::plan_decode(B, Hq, Hkv, Tmax, Dh, st->info.num_sms);
   if ((long long)Hkv * ((Hq / Hkv) / plan.heads_per_cta) > 65535) return ATTN_ERR_INVALID_ARG;
   const size_t need_partials = chs::decode_partials_bytes(B, Hq, Dh, plan);

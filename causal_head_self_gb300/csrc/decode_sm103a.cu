@@ -1,5 +1,6 @@
 // decode_sm103a.cu -- split planning and host launchers of the decode kernels.
 #include "decode_sm103a.cuh"
+#include "decode_tc_sm103a.cuh"
 #include "launch.h"
 
 namespace chs {
@@ -104,6 +105,79 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
   prm.ring = ring;
   return Dh == 128 ? launch_hpb<128>(prm, plan.heads_per_cta, stream)
                    : launch_hpb<64>(prm, plan.heads_per_cta, stream);
+}
+
+// ---------------------------------------------------------------- tensor-core path
+
+DecodePlan plan_decode_tc(int B, int Hq, int Hkv, int Tmax, int num_sms) {
+  DecodePlan plan;
+  const int group = Hq / Hkv;
+  plan.heads_per_cta = group < 128 ? group : 128;
+  const long long units = (long long)B * Hkv * ((group + 127) / 128);
+  // about three waves of one CTA per SM, whole 128-key tiles, 256..8192 keys
+  // per split, at most 64 splits
+  const long long want = 3LL * num_sms;
+  long long chunk = ((long long)Tmax * units / (want > 0 ? want : 1) + 127) / 128 * 128;
+  if (chunk < 256) chunk = 256;
+  if (chunk > 8192) chunk = 8192;
+  long long nsplit = (Tmax + chunk - 1) / chunk;
+  if (nsplit > 64) {
+    chunk = ((Tmax + 63) / 64 + 127) / 128 * 128;
+    nsplit = (Tmax + chunk - 1) / chunk;
+  }
+  plan.chunk = (int)chunk;
+  plan.nsplit = (int)nsplit;
+  return plan;
+}
+
+template <int DH>
+static cudaError_t launch_tc_dh(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                const DecodeTcParams& prm, cudaStream_t stream) {
+  constexpr size_t smem = decode_tc_smem_bytes<DH>();
+  static_assert(smem <= 232448, "shared memory budget of one sm_103a CTA");
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_sm103a<DH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(prm.nsplit, prm.B * prm.Hkv * prm.row_blocks);
+  attn_decode_tc_sm103a<DH><<<grid, DecodeTcCfg<DH>::kThreads, smem, stream>>>(mq, mk, mv, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_decode_tc_combine<DH><<<prm.B * prm.Hq, DH, 0, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, const int* seqlens,
+                             void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,
+                             float scale_log2, const DecodePlan& plan, void* partials,
+                             const DeviceInfo& dev, cudaStream_t stream) {
+  const int G = Hq / Hkv;
+  CUtensorMap mq, mk, mv;
+  if (!encode_bf16_map(&mq, q, Dh, G, (long long)B * Hkv, 128) ||
+      !encode_bf16_map(&mk, kc, Dh, Tmax, (long long)B * Hkv, 128) ||
+      !encode_bf16_map(&mv, vc, Dh, Tmax, (long long)B * Hkv, 128))
+    return cudaErrorInvalidValue;
+  DecodeTcParams prm;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.G = G;
+  prm.Tmax = Tmax;
+  prm.window = window;
+  prm.nsplit = plan.nsplit;
+  prm.chunk = plan.chunk;
+  prm.row_blocks = (G + 127) / 128;
+  prm.scale_log2 = scale_log2;
+  prm.seqlens = seqlens;
+  const DecodePartialsLayout w = partials_layout(B, Hq, Dh, plan);
+  uint8_t* ws = static_cast<uint8_t*>(partials);
+  prm.o_part = reinterpret_cast<float*>(ws + w.o_off);
+  prm.m_part = reinterpret_cast<float*>(ws + w.m_off);
+  prm.l_part = reinterpret_cast<float*>(ws + w.l_off);
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.error_word = dev.error_word;
+  prm.fault = dev.fault;
+  return Dh == 128 ? launch_tc_dh<128>(mq, mk, mv, prm, stream)
+                   : launch_tc_dh<64>(mq, mk, mv, prm, stream);
 }
 
 }  // namespace chs

@@ -1,0 +1,430 @@
+// decode_tc_sm103a.cuh -- the decode step for large query-head groups on the
+// 5th-generation tensor cores (sm_103a).
+//
+// When many query heads share one K/V head (MQA, or GQA with 8 or more heads
+// per group), a decode step is no longer a pure stream: every cached byte
+// meets Hq / Hkv query rows, 64 FLOP per byte for a group of 32, and the
+// CUDA-core decode kernel becomes bound by its arithmetic.  Packed together,
+// the group's query rows form a real contraction: S = Q K^T with the group's
+// heads as the M dimension (up to 128 per CTA; fewer rows leave the rest of
+// the tile unused), 128 keys as N, Dh as K, and O = P V.  So this path is the
+// prefill pipeline reduced to one 128-row sub-tile without a causal mask: a
+// TMA producer streams 128-key K and V tiles of one split of the cache, one
+// warp issues tcgen05.mma (S and P.V accumulate in tensor memory), and the
+// softmax warps (only those holding real rows) run the online softmax with a
+// lazy maximum.  Each CTA writes fp32 partials (o unnormalised, m, l) of its
+// split; a small combine kernel merges the splits per (b, query head) with
+// the same log-sum-exp algebra as the CUDA-core decode.
+//
+// Key tiles are placed so that the split's last tile ends at its last key:
+// tile j starts at position k_end - 128 * (n - j), and only the first tile
+// can reach below k_begin (into earlier, valid cache rows, or below 0 where
+// the copy fills zeros).  Those columns are masked to -inf, so their weights
+// are exactly 0 and every V row the MMA reads is a written cache row (or a
+// zero row): rows past seqlens[b] are never read.
+//
+// Every wait is bounded (sm103a_ptx.cuh): a lost arrival ends the CTA with
+// ATTN_ERR_TIMEOUT latched instead of a hang.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "sm103a_ptx.cuh"
+
+namespace chs {
+
+struct DecodeTcParams {
+  int B, Hq, Hkv, G, Tmax, window;
+  int nsplit, chunk;        // chunk: keys per split, a multiple of 128
+  int row_blocks;           // ceil(G / 128): CTAs per (b, K/V head, split)
+  float scale_log2;
+  const int* seqlens;       // [B], device
+  float* o_part;            // [B, Hq, nsplit, DH]  unnormalised
+  float* m_part;            // [B, Hq, nsplit]      (log2 domain)
+  float* l_part;            // [B, Hq, nsplit]
+  __nv_bfloat16* o;         // [B, Hq, 1, DH]
+  int* error_word;
+  int fault;                // test hook: 3 = the first K tile is never loaded
+};
+
+template <int DH>
+struct DecodeTcCfg {
+  static constexpr int kHalves = DH / 64;
+  static constexpr int kBoxBytes = 128 * 64 * 2;     // one 128 x 64 bf16 box
+  static constexpr int kTileBytes = kHalves * kBoxBytes;
+  static constexpr int kStages = 2;                  // K ring and V ring
+  static constexpr int kThreads = 192;               // warps 0-3 softmax, 4 producer, 5 MMA
+  static constexpr int kWarpProducer = 4, kWarpIssuer = 5;
+  static constexpr uint32_t kCols = 256;             // S [0,128), O [128,128+DH)
+  static constexpr uint32_t kColS = 0, kColO = 128;
+};
+
+template <int DH>
+struct __align__(1024) DecodeTcSmem {
+  using Cfg = DecodeTcCfg<DH>;
+  uint8_t q[Cfg::kTileBytes];
+  uint8_t k[Cfg::kStages][Cfg::kTileBytes];
+  uint8_t v[Cfg::kStages][Cfg::kTileBytes];
+  uint64_t q_full;
+  uint64_t k_full[Cfg::kStages], k_empty[Cfg::kStages];
+  uint64_t v_full[Cfg::kStages], v_empty[Cfg::kStages];
+  uint64_t s_full, p_full, o_final, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// The keys of split `split` of a sequence of L keys: [k_begin, k_end).
+__device__ __forceinline__ void decode_tc_range(int L, int window, int split, int chunk,
+                                                int& k_begin, int& k_end) {
+  const int lo = window > 0 ? max(0, L - window) : 0;
+  k_begin = max(split * chunk, lo);
+  k_end = min((split + 1) * chunk, L);
+}
+
+// Drain wait used at teardown: ignores the abort flag, bounded by time.
+__device__ __forceinline__ void mbar_wait_drain_tc(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// TMA producer (one thread): the CTA's 128 query rows once, then the split's
+// K and V tiles through two-stage rings.
+template <int DH>
+__device__ __forceinline__ void decode_tc_producer(DecodeTcSmem<DH>& sm, const DecodeTcParams& p,
+                                                   const CUtensorMap* map_q,
+                                                   const CUtensorMap* map_k,
+                                                   const CUtensorMap* map_v, int bg, int rb,
+                                                   int origin, int ntiles, volatile int* abort) {
+  using Cfg = DecodeTcCfg<DH>;
+  const uint64_t once = policy_evict_first();   // each cached row is read by one CTA
+  mbar_arrive_expect_tx(&sm.q_full, Cfg::kTileBytes);
+  for (int hf = 0; hf < Cfg::kHalves; ++hf)
+    tma_load_3d(sm.q + hf * Cfg::kBoxBytes, map_q, &sm.q_full, hf * 64, 128 * rb, bg);
+  uint32_t k_loaded = 0, k_par = 0, v_loaded = 0, v_par = 0;
+  for (int j = 0; j < ntiles; ++j) {
+    const int st = j % Cfg::kStages;
+    const uint32_t ph = (uint32_t)(j / Cfg::kStages) & 1u;
+    const int row = origin + 128 * j;   // may be negative for the first tile: zeros
+    if (!mbar_wait(&sm.k_empty[st], ph ^ 1u, abort)) break;
+    if (p.fault != 3 || j != 0) {   // (the test hook withholds one tile)
+      mbar_arrive_expect_tx(&sm.k_full[st], Cfg::kTileBytes);
+      for (int hf = 0; hf < Cfg::kHalves; ++hf)
+        tma_load_3d_hint(sm.k[st] + hf * Cfg::kBoxBytes, map_k, &sm.k_full[st], hf * 64, row, bg,
+                         once);
+      k_loaded |= 1u << st;
+      k_par = (k_par & ~(1u << st)) | (ph << st);
+    }
+    if (!mbar_wait(&sm.v_empty[st], ph ^ 1u, abort)) break;
+    mbar_arrive_expect_tx(&sm.v_full[st], Cfg::kTileBytes);
+    for (int hf = 0; hf < Cfg::kHalves; ++hf)
+      tma_load_3d_hint(sm.v[st] + hf * Cfg::kBoxBytes, map_v, &sm.v_full[st], hf * 64, row, bg,
+                       once);
+    v_loaded |= 1u << st;
+    v_par = (v_par & ~(1u << st)) | (ph << st);
+  }
+  // every copy this thread started has landed before the CTA may exit
+  mbar_wait_drain_tc(&sm.q_full, 0);
+  for (int i = 0; i < Cfg::kStages; ++i) {
+    if (k_loaded & (1u << i)) mbar_wait_drain_tc(&sm.k_full[i], (k_par >> i) & 1u);
+    if (v_loaded & (1u << i)) mbar_wait_drain_tc(&sm.v_full[i], (v_par >> i) & 1u);
+  }
+}
+
+// MMA issuer (one converged warp, one elected lane per instruction):
+// S(0), then per tile j: P.V(j) once the softmax has written P(j), and S(j+1)
+// after it (S(j+1) overwrites the columns P(j) lives in; the tensor core runs
+// one thread's MMAs in order).
+template <int DH>
+__device__ __forceinline__ void decode_tc_issuer(DecodeTcSmem<DH>& sm, uint32_t tbase, int ntiles,
+                                                 volatile int* abort) {
+  using Cfg = DecodeTcCfg<DH>;
+  constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t idesc_pv = idesc_bf16_f32(128, DH, false, true);
+  constexpr uint64_t kKmajor = smem_desc_sw128(0, 16, 1024);                // Q, K
+  constexpr uint64_t kMnMajor = smem_desc_sw128(0, Cfg::kBoxBytes, 1024);   // V
+  const uint64_t dq = kKmajor | (smem_u32(sm.q) >> 4);
+  const uint64_t dk = kKmajor | (smem_u32(sm.k[0]) >> 4);
+  const uint64_t dv = kMnMajor | (smem_u32(sm.v[0]) >> 4);
+  const uint32_t dS = tbase + Cfg::kColS, dO = tbase + Cfg::kColO;
+  auto issue_s = [&](int j) -> bool {
+    const int st = j % Cfg::kStages;
+    const uint32_t ph = (uint32_t)(j / Cfg::kStages) & 1u;
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.k_full[st], ph, abort))) return false;
+    tc_fence_after_sync();
+    const uint64_t b = dk + (uint64_t)(st * (Cfg::kTileBytes >> 4));
+#pragma unroll
+    for (int kk = 0; kk < DH / 16; ++kk) {
+      const uint32_t off = ((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4;
+      mma_bf16_ss_warp(dS, dq + off, b + off, idesc_qk, kk > 0 ? 1u : 0u);
+    }
+    mma_commit_warp(&sm.s_full);
+    mma_commit_warp(&sm.k_empty[st]);
+    return true;
+  };
+  bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0, abort));
+  if (ok) ok = issue_s(0);
+  for (int j = 0; ok && j < ntiles; ++j) {
+    const int st = j % Cfg::kStages;
+    const uint32_t ph = (uint32_t)(j / Cfg::kStages) & 1u;
+    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], ph, abort)))) break;
+    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_full, (uint32_t)j & 1u, abort)))) break;
+    tc_fence_after_sync();
+    // O (+)= P V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
+    const uint64_t b = dv + (uint64_t)(st * (Cfg::kTileBytes >> 4));
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_bf16_ts_warp(dO, dS + kk * 8, b + kk * (2048 >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+    mma_commit_warp(&sm.v_empty[st]);
+    if (j + 1 < ntiles) ok = issue_s(j + 1);
+  }
+  if (ok) mma_commit_warp(&sm.o_final);
+  // nothing of this warp's may still run on the tensor core at teardown
+  mma_commit_warp(&sm.mma_done);
+  mbar_wait_drain_tc(&sm.mma_done, 0);
+}
+
+// Softmax of the CTA's query rows (thread t owns row t, TMEM lane t): per
+// 128-key tile the online softmax of "Online normalizer calculation for
+// softmax" with a lazy maximum, as in the prefill; at the end, the row's
+// unnormalised o, its maximum m and sum l go to the split's partials.
+template <int DH>
+__device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const DecodeTcParams& p,
+                                                  uint32_t tbase, int warp, int lane, int b,
+                                                  int head0, int rows, int split, int clo0,
+                                                  int ntiles, volatile int* abort) {
+  using Cfg = DecodeTcCfg<DH>;
+  const int t = warp * 32 + lane;
+  const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+  const uint32_t colS = lane_addr + Cfg::kColS, colO = lane_addr + Cfg::kColO;
+  const float sl2 = p.scale_log2;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool ok = true;
+  for (int j = 0; j < ntiles; ++j) {
+    if (!(ok = mbar_wait(&sm.s_full, (uint32_t)j & 1u, abort))) break;
+    tc_fence_after_sync();
+    if (j == 0 && clo0 > 0) {
+      // the first tile reaches below the split: its first clo0 columns are
+      // not this split's keys (a whole-warp chunk below them is filled
+      // without being read; the chunk that straddles is read and masked)
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        if (c0 >= clo0) break;
+        uint32_t y[32];
+        if (c0 + 31 < clo0) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) y[e] = 0xff800000u;   // -inf
+        } else {
+          tmem_ld_32x32b_x32(colS + c0, y);
+          tmem_ld_wait(y);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            y[e] = __float_as_uint(keep_if_le(__uint_as_float(y[e]), (uint32_t)(c0 + e - clo0),
+                                              (uint32_t)(127 - clo0)));
+        }
+        tmem_st_32x32b_x32(colS + c0, y);
+      }
+      tmem_st_wait();
+    }
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    float mc0, mc1, mc2, mc3;
+    tmem_ld_max_32x32b_x32(colS + 0, r0, mc0);
+    tmem_ld_max_32x32b_x32(colS + 32, r1, mc1);
+    tmem_ld_max_32x32b_x32(colS + 64, r2, mc2);
+    tmem_ld_max_32x32b_x32(colS + 96, r3, mc3);
+    tmem_ld_wait(r0, mc0);
+    tmem_ld_wait(r1, mc1);
+    tmem_ld_wait(r2, mc2);
+    tmem_ld_wait(r3, mc3);
+    float x[128];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      x[c] = __uint_as_float(r0[c]);
+      x[32 + c] = __uint_as_float(r1[c]);
+      x[64 + c] = __uint_as_float(r2[c]);
+      x[96 + c] = __uint_as_float(r3[c]);
+    }
+    const float m_tile = fmaxf(fmaxf(mc0, mc1), fmaxf(mc2, mc3)) * sl2;
+    // lazy maximum (raised only past +8 in log2 units; exact either way)
+    const float m_new = fmaxf(m_run, m_tile);
+    const bool fresh = m_run == -INFINITY;
+    const bool upd = fresh || (m_new > m_run + 8.0f);
+    const float m_use = upd ? m_new : m_run;
+    const float corr = (upd && !fresh) ? ex2_approx(m_run - m_new) : 1.0f;
+    const float msub = (m_use == -INFINITY) ? 0.f : m_use;
+    const float2 scale2 = make_float2(sl2, sl2), neg_m2 = make_float2(-msub, -msub);
+    float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float2 xs = __ffma2_rn(make_float2(x[32 * c4 + 2 * e], x[32 * c4 + 2 * e + 1]),
+                                     scale2, neg_m2);
+        const float2 pp = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
+        ls[e & 1] = __fadd2_rn(ls[e & 1], pp);
+        pk[e] = pack_bf16x2(pp.x, pp.y);
+      }
+      tmem_st_32x32b_x16(colS + 16 * c4, pk);   // P over the first 64 columns of S
+    }
+    const float lsum = (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
+    // a raised maximum rescales the row's O (P.V of the earlier tiles is
+    // done: the S just waited for was issued after it)
+    if (__any_sync(0xffffffffu, corr != 1.0f)) {
+#pragma unroll 1
+      for (int c = 0; c < DH / 16; ++c) {
+        uint32_t o[16];
+        tmem_ld_32x32b_x16(colO + 16 * c, o);
+        tmem_ld_wait(o);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+        tmem_st_32x32b_x16(colO + 16 * c, o);
+      }
+    }
+    l_run = l_run * corr + lsum;
+    m_run = m_use;
+    tmem_st_wait();
+    tc_fence_before_sync();
+    mbar_arrive(&sm.p_full);
+  }
+  if (!ok || !mbar_wait(&sm.o_final, 0, abort)) return;
+  tc_fence_after_sync();
+  const bool real = t < rows;
+  const size_t ps = ((size_t)b * p.Hq + head0 + t) * p.nsplit + split;
+  float4* dst = reinterpret_cast<float4*>(p.o_part + ps * DH);
+#pragma unroll 1
+  for (int c = 0; c < DH / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(colO + 32 * c, o);
+    tmem_ld_wait(o);
+    if (real) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        dst[8 * c + e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                     __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+    }
+  }
+  if (real) {
+    p.m_part[ps] = m_run;
+    p.l_part[ps] = l_run;
+  }
+}
+
+// grid (nsplit, B * Hkv * row_blocks): one split of one (b, K/V head) for up
+// to 128 of its group's query heads.
+template <int DH>
+__global__ void __launch_bounds__(192, 1)
+    attn_decode_tc_sm103a(const __grid_constant__ CUtensorMap map_q,
+                          const __grid_constant__ CUtensorMap map_k,
+                          const __grid_constant__ CUtensorMap map_v, const DecodeTcParams p) {
+  using Cfg = DecodeTcCfg<DH>;
+  using Smem = DecodeTcSmem<DH>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  volatile int* abort = &sm.abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  const int split = blockIdx.x;
+  const int rb = blockIdx.y % p.row_blocks;
+  const int bg = blockIdx.y / p.row_blocks;   // b * Hkv + g
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int L = p.seqlens[b];
+  if (L < 1 || L > p.Tmax) return;            // the combine kernel reports it
+  int k_begin, k_end;
+  decode_tc_range(L, p.window, split, p.chunk, k_begin, k_end);
+  if (k_begin >= k_end) return;               // no visible key in this split
+  const int ntiles = (k_end - k_begin + 127) / 128;
+  const int origin = k_end - 128 * ntiles;    // position of the first tile's first key
+  const int rows = min(128, p.G - 128 * rb);  // real query rows of this CTA
+  const int active_warps = (rows + 31) / 32;
+
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    mbar_init(&sm.q_full, 1);
+    for (int i = 0; i < Cfg::kStages; ++i) {
+      mbar_init(&sm.k_full[i], 1);
+      mbar_init(&sm.k_empty[i], 1);
+      mbar_init(&sm.v_full[i], 1);
+      mbar_init(&sm.v_empty[i], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.p_full, 32 * active_warps);
+    mbar_init(&sm.o_final, 1);
+    mbar_init(&sm.mma_done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == Cfg::kWarpIssuer) {
+    tmem_alloc(&sm.tmem_base, Cfg::kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = sm.tmem_base;
+
+  if (warp == Cfg::kWarpProducer) {
+    if (lane == 0) {
+      prefetch_tensormap(&map_q);
+      prefetch_tensormap(&map_k);
+      prefetch_tensormap(&map_v);
+      decode_tc_producer<DH>(sm, p, &map_q, &map_k, &map_v, bg, rb, origin, ntiles, abort);
+    }
+  } else if (warp == Cfg::kWarpIssuer) {
+    decode_tc_issuer<DH>(sm, tbase, ntiles, abort);
+  } else if (warp < active_warps) {
+    decode_tc_softmax<DH>(sm, p, tbase, warp, lane, b, g * p.G + 128 * rb, rows, split,
+                          k_begin - origin, ntiles, abort);
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == Cfg::kWarpIssuer) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, Cfg::kCols);
+  }
+  if (threadIdx.x == 0 && sm.abort_flag) atomicExch(p.error_word, 4);   // ATTN_ERR_TIMEOUT
+}
+
+// Merge the splits of one (b, query head): o = sum_s 2^(m_s - M) o_s /
+// sum_s 2^(m_s - M) l_s with M the largest m_s (the online-softmax merge),
+// in split order.  One block of DH threads per (b, query head).
+template <int DH>
+__global__ void __launch_bounds__(DH) attn_decode_tc_combine(const DecodeTcParams p) {
+  const int bh = blockIdx.x;
+  const int b = bh / p.Hq;
+  const int d = threadIdx.x;
+  const int L = p.seqlens[b];
+  if (L < 1 || L > p.Tmax) {
+    // a sequence length outside [1, Tmax]: zero output, latch the error
+    p.o[(size_t)bh * DH + d] = __float2bfloat16(0.f);
+    if (d == 0) atomicExch(p.error_word, 1);   // ATTN_ERR_INVALID_ARG
+    return;
+  }
+  const int lo = p.window > 0 ? max(0, L - p.window) : 0;
+  const int s_first = lo / p.chunk, s_last = (L - 1) / p.chunk;
+  const float* mp = p.m_part + (size_t)bh * p.nsplit;
+  const float* lp = p.l_part + (size_t)bh * p.nsplit;
+  const float* op = p.o_part + (size_t)bh * p.nsplit * DH;
+  float M = -INFINITY;
+  for (int s = s_first; s <= s_last; ++s) M = fmaxf(M, mp[s]);
+  float o = 0.f, l = 0.f;
+  for (int s = s_first; s <= s_last; ++s) {
+    const float f = ex2_approx(mp[s] - M);
+    o = fmaf(f, op[(size_t)s * DH + d], o);
+    l = fmaf(f, lp[s], l);
+  }
+  p.o[(size_t)bh * DH + d] = __float2bfloat16(o / l);
+}
+
+template <int DH>
+constexpr size_t decode_tc_smem_bytes() {
+  return sizeof(DecodeTcSmem<DH>) + 1024;   // + alignment slack
+}
+
+}  // namespace chs

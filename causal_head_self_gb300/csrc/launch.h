@@ -51,4 +51,14 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
                           int ring, float scale_log2, const DecodePlan& plan, int* counters,
                           void* partials, const DeviceInfo& dev, cudaStream_t stream);
 
+// Tensor-core decode for large query-head groups (Hq / Hkv >= kDecodeTcMinGroup):
+// splits of whole 128-key tiles, one CTA per (split, b, K/V head, 128 heads),
+// then a combine kernel.  Linear caches only.
+constexpr int kDecodeTcMinGroup = 8;
+DecodePlan plan_decode_tc(int B, int Hq, int Hkv, int Tmax, int num_sms);
+cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, const int* seqlens,
+                             void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,
+                             float scale_log2, const DecodePlan& plan, void* partials,
+                             const DeviceInfo& dev, cudaStream_t stream);
+
 }  // namespace chs

@@ -110,6 +110,9 @@ int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* 
  * [max(0, seqlens[b] - window), seqlens[b]) (all of them when window <= 0).
  * A seqlens entry outside [1, Tmax] zeroes that sequence's output and latches
  * ATTN_ERR_INVALID_ARG for attn_status().
+ * With Hq / Hkv >= 8 (MQA-like groups) the step runs on the tensor cores
+ * (the group's query heads packed as the rows of one contraction with each
+ * key tile) followed by a small combine kernel; otherwise on the CUDA cores.
  * The split-KV partials live in a library-owned device workspace, allocated
  * on first use per device and grown on demand (cudaMalloc): make the first
  * call with the largest shape outside any CUDA graph capture.  Calls on one
@@ -187,7 +190,10 @@ int attn_status(cudaStream_t stream);
  *   0  none (the default)
  *   1  attn_fwd: the producer never loads the first K tile of each CTA's
  *      first work item, so the MMA issuers' bounded waits run out
- *   2  attn_decode: the producer never loads the first key block of each CTA
+ *   2  attn_decode (CUDA-core path): the producer never loads the first key
+ *      block of each CTA
+ *   3  attn_decode (tensor-core path, Hq / Hkv >= 8): the producer never loads
+ *      the first K tile of each CTA
  * A faulted launch ends by itself after its waits give up (about 2 s): no
  * GPU fault, trap or hang.  attn_status() then returns ATTN_ERR_TIMEOUT and
  * clears it; the outputs of that launch are undefined, and the next launch
