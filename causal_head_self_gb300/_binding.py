@@ -227,8 +227,8 @@ def attn_decode_noalloc(q, kcache, vcache, seqlens, o=None, *, window=0, scale=0
 
 def attn_debug_inject_fault(kind: int) -> None:
     """Test hook (see include/attn.h): 0 none, 1 a prefill K tile is withheld,
-    2 a decode key block is withheld; later launches wait, give up and report
-    ATTN_ERR_TIMEOUT through attn_status()."""
+    2 a decode key block (CUDA-core path), 3 a decode K tile (tensor-core path);
+    later launches wait, give up and report ATTN_ERR_TIMEOUT through attn_status()."""
     rc = load().attn_debug_inject_fault(int(kind))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_debug_inject_fault")

@@ -114,12 +114,13 @@ DecodePlan plan_decode_tc(int B, int Hq, int Hkv, int Tmax, int num_sms) {
   const int group = Hq / Hkv;
   plan.heads_per_cta = group < 128 ? group : 128;
   const long long units = (long long)B * Hkv * ((group + 127) / 128);
-  // about three waves of one CTA per SM, whole 128-key tiles, 256..8192 keys
-  // per split, at most 64 splits
-  const long long want = 3LL * num_sms;
+  // about one wave of one CTA per SM (measured: a CTA's start-up costs more
+  // than the imbalance of longer splits), whole 128-key tiles, 256..32768
+  // keys per split, at most 64 splits
+  const long long want = 1LL * num_sms;
   long long chunk = ((long long)Tmax * units / (want > 0 ? want : 1) + 127) / 128 * 128;
   if (chunk < 256) chunk = 256;
-  if (chunk > 8192) chunk = 8192;
+  if (chunk > 32768) chunk = 32768;
   long long nsplit = (Tmax + chunk - 1) / chunk;
   if (nsplit > 64) {
     chunk = ((Tmax + 63) / 64 + 127) / 128 * 128;

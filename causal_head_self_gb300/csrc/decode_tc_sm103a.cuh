@@ -57,8 +57,8 @@ struct DecodeTcCfg {
   static constexpr int kStages = 2;                  // K ring and V ring
   static constexpr int kThreads = 192;               // warps 0-3 softmax, 4 producer, 5 MMA
   static constexpr int kWarpProducer = 4, kWarpIssuer = 5;
-  static constexpr uint32_t kCols = 256;             // S [0,128), O [128,128+DH)
-  static constexpr uint32_t kColS = 0, kColO = 128;
+  static constexpr uint32_t kCols = 512;             // S0 [0,128), S1 [128,256), O [256,256+DH)
+  static constexpr uint32_t kColS = 0, kColO = 256;  // S buffer b at kColS + 128 b
 };
 
 template <int DH>
@@ -70,7 +70,7 @@ struct __align__(1024) DecodeTcSmem {
   uint64_t q_full;
   uint64_t k_full[Cfg::kStages], k_empty[Cfg::kStages];
   uint64_t v_full[Cfg::kStages], v_empty[Cfg::kStages];
-  uint64_t s_full, p_full, o_final, mma_done;
+  uint64_t s_full[2], p_full[2], pv_done, o_final, mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -135,10 +135,12 @@ __device__ __forceinline__ void decode_tc_producer(DecodeTcSmem<DH>& sm, const D
   }
 }
 
-// MMA issuer (one converged warp, one elected lane per instruction):
-// S(0), then per tile j: P.V(j) once the softmax has written P(j), and S(j+1)
-// after it (S(j+1) overwrites the columns P(j) lives in; the tensor core runs
-// one thread's MMAs in order).
+// MMA issuer (one converged warp, one elected lane per instruction).  S is
+// double-buffered in tensor memory: S(j+1) is computed while the softmax
+// works on S(j), so the softmax warps go from one tile to the next without
+// waiting for the tensor core.  Order: S(0), S(1), then per tile j: P.V(j)
+// once P(j) is written, and S(j+2) into the buffer P(j) lived in (the tensor
+// core runs one thread's MMAs in order, so S(j+2) follows P.V(j)).
 template <int DH>
 __device__ __forceinline__ void decode_tc_issuer(DecodeTcSmem<DH>& sm, uint32_t tbase, int ntiles,
                                                  volatile int* abort) {
@@ -150,37 +152,43 @@ __device__ __forceinline__ void decode_tc_issuer(DecodeTcSmem<DH>& sm, uint32_t 
   const uint64_t dq = kKmajor | (smem_u32(sm.q) >> 4);
   const uint64_t dk = kKmajor | (smem_u32(sm.k[0]) >> 4);
   const uint64_t dv = kMnMajor | (smem_u32(sm.v[0]) >> 4);
-  const uint32_t dS = tbase + Cfg::kColS, dO = tbase + Cfg::kColO;
+  const uint32_t dO = tbase + Cfg::kColO;
   auto issue_s = [&](int j) -> bool {
     const int st = j % Cfg::kStages;
     const uint32_t ph = (uint32_t)(j / Cfg::kStages) & 1u;
     if (!__all_sync(0xffffffffu, mbar_wait(&sm.k_full[st], ph, abort))) return false;
     tc_fence_after_sync();
+    const uint32_t dS = tbase + Cfg::kColS + 128u * (uint32_t)(j & 1);
     const uint64_t b = dk + (uint64_t)(st * (Cfg::kTileBytes >> 4));
 #pragma unroll
     for (int kk = 0; kk < DH / 16; ++kk) {
       const uint32_t off = ((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4;
       mma_bf16_ss_warp(dS, dq + off, b + off, idesc_qk, kk > 0 ? 1u : 0u);
     }
-    mma_commit_warp(&sm.s_full);
+    mma_commit_warp(&sm.s_full[j & 1]);
     mma_commit_warp(&sm.k_empty[st]);
     return true;
   };
   bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0, abort));
   if (ok) ok = issue_s(0);
+  if (ok && ntiles > 1) ok = issue_s(1);
   for (int j = 0; ok && j < ntiles; ++j) {
     const int st = j % Cfg::kStages;
     const uint32_t ph = (uint32_t)(j / Cfg::kStages) & 1u;
     if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], ph, abort)))) break;
-    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_full, (uint32_t)j & 1u, abort)))) break;
+    if (!(ok = __all_sync(0xffffffffu,
+                          mbar_wait(&sm.p_full[j & 1], (uint32_t)(j >> 1) & 1u, abort))))
+      break;
     tc_fence_after_sync();
     // O (+)= P V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
+    const uint32_t dP = tbase + Cfg::kColS + 128u * (uint32_t)(j & 1);
     const uint64_t b = dv + (uint64_t)(st * (Cfg::kTileBytes >> 4));
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      mma_bf16_ts_warp(dO, dS + kk * 8, b + kk * (2048 >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+      mma_bf16_ts_warp(dO, dP + kk * 8, b + kk * (2048 >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+    mma_commit_warp(&sm.pv_done);
     mma_commit_warp(&sm.v_empty[st]);
-    if (j + 1 < ntiles) ok = issue_s(j + 1);
+    if (j + 2 < ntiles) ok = issue_s(j + 2);
   }
   if (ok) mma_commit_warp(&sm.o_final);
   // nothing of this warp's may still run on the tensor core at teardown
@@ -200,13 +208,14 @@ __device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const De
   using Cfg = DecodeTcCfg<DH>;
   const int t = warp * 32 + lane;
   const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
-  const uint32_t colS = lane_addr + Cfg::kColS, colO = lane_addr + Cfg::kColO;
+  const uint32_t colO = lane_addr + Cfg::kColO;
   const float sl2 = p.scale_log2;
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
   for (int j = 0; j < ntiles; ++j) {
-    if (!(ok = mbar_wait(&sm.s_full, (uint32_t)j & 1u, abort))) break;
+    if (!(ok = mbar_wait(&sm.s_full[j & 1], (uint32_t)(j >> 1) & 1u, abort))) break;
     tc_fence_after_sync();
+    const uint32_t colS = lane_addr + Cfg::kColS + 128u * (uint32_t)(j & 1);
     if (j == 0 && clo0 > 0) {
       // the first tile reaches below the split: its first clo0 columns are
       // not this split's keys (a whole-warp chunk below them is filled
@@ -272,9 +281,12 @@ __device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const De
       tmem_st_32x32b_x16(colS + 16 * c4, pk);   // P over the first 64 columns of S
     }
     const float lsum = (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
-    // a raised maximum rescales the row's O (P.V of the earlier tiles is
-    // done: the S just waited for was issued after it)
+    // a raised maximum rescales the row's O, once P.V of the previous tile
+    // has written it (S(j) was issued before P.V(j-1): wait for it; P.V(j)
+    // cannot run before this tile's P is published below)
     if (__any_sync(0xffffffffu, corr != 1.0f)) {
+      if (j > 0 && !(ok = mbar_wait(&sm.pv_done, (uint32_t)(j - 1) & 1u, abort))) break;
+      tc_fence_after_sync();
 #pragma unroll 1
       for (int c = 0; c < DH / 16; ++c) {
         uint32_t o[16];
@@ -289,7 +301,7 @@ __device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const De
     m_run = m_use;
     tmem_st_wait();
     tc_fence_before_sync();
-    mbar_arrive(&sm.p_full);
+    mbar_arrive(&sm.p_full[j & 1]);
   }
   if (!ok || !mbar_wait(&sm.o_final, 0, abort)) return;
   tc_fence_after_sync();
@@ -352,8 +364,11 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&sm.v_full[i], 1);
       mbar_init(&sm.v_empty[i], 1);
     }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 32 * active_warps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.p_full[i], 32 * active_warps);
+    }
+    mbar_init(&sm.pv_done, 1);
     mbar_init(&sm.o_final, 1);
     mbar_init(&sm.mma_done, 1);
     fence_mbarrier_init();
