@@ -209,7 +209,7 @@ static int decode_common(const void* q, const void* kcache, const void* vcache, 
                          void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window, int ring,
                          float scale, cudaStream_t stream) {
   if (B < 0 || Tmax < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Dh != 64 && Dh != 128 && Dh != 256) return ATTN_ERR_UNSUPPORTED;
   if (window < 0) window = 0;
   if (ring && window > Tmax) return ATTN_ERR_INVALID_ARG;   // the ring holds Tmax positions
   float scale_log2 = 0.f;
@@ -229,7 +229,7 @@ static int decode_common(const void* q, const void* kcache, const void* vcache, 
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
-  if (!ring && Hq / Hkv >= chs::kDecodeTcMinGroup) {
+  if (!ring && Dh <= 128 && Hq / Hkv >= chs::kDecodeTcMinGroup) {
     // many query heads per cached byte: the tensor-core path (a contraction)
     const chs::DecodePlan plan = chs::plan_decode_tc(B, Hq, Hkv, Tmax, st->info.num_sms);
     if ((long long)B * Hkv * ((Hq / Hkv + 127) / 128) > 65535) return ATTN_ERR_INVALID_ARG;
@@ -321,7 +321,7 @@ extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void
                                    const int* seqlens, void* o, int B, int Hq, int Hkv, int Tmax,
                                    int Dh, int window, float scale, cudaStream_t stream) {
   if (B < 0 || Tmax < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Dh != 64 && Dh != 128 && Dh != 256) return ATTN_ERR_UNSUPPORTED;
   if (window < 0) window = 0;
   float scale_log2 = 0.f;
   if (!resolve_scale(scale, Dh, &scale_log2)) return ATTN_ERR_INVALID_ARG;

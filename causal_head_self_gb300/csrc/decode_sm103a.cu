@@ -7,7 +7,9 @@ namespace chs {
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int Tmax, int Dh, int num_sms) {
   DecodePlan plan;
-  const long long bk = Dh == 64 ? decode_block_keys<64>() : decode_block_keys<128>();
+  const long long bk = Dh == 64    ? decode_block_keys<64>()
+                       : Dh == 256 ? decode_block_keys<256>()
+                                   : decode_block_keys<128>();
   const int group = Hq / Hkv;
   plan.heads_per_cta = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
   const long long ctas_per_split = (long long)B * Hkv * (group / plan.heads_per_cta);
@@ -103,6 +105,7 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
   prm.ring = ring;
+  if (Dh == 256) return launch_hpb<256>(prm, plan.heads_per_cta, stream);
   return Dh == 128 ? launch_hpb<128>(prm, plan.heads_per_cta, stream)
                    : launch_hpb<64>(prm, plan.heads_per_cta, stream);
 }

@@ -19,7 +19,9 @@
  *     ("多头注意力机制" (blog.euler0525.cn), section "Multi-head Attention":
  *     heads moved ahead of the sequence axis).  All tensor pointers are
  *     DEVICE pointers, 16-byte aligned.  The caller owns every tensor.
- *   - Dh must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise).
+ *   - Dh must be 64 or 128 for the prefill entry points and 64, 128 or 256
+ *     (the Gemma head size) for the decode ones (ATTN_ERR_UNSUPPORTED
+ *     otherwise).
  *   - Hq % Hkv == 0 is required (ATTN_ERR_INVALID_ARG otherwise).
  *   - scale == 0 selects 1/sqrt(Dh), the textbook's choice (divide by the
  *     square root of the HEAD size, not the model width); a positive scale is
@@ -49,7 +51,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,  /* bad shape, pointer, alignment, aliasing, scale or window */
-  ATTN_ERR_UNSUPPORTED = 2,  /* a head size other than 64 or 128 */
+  ATTN_ERR_UNSUPPORTED = 2,  /* a head size the entry point does not take */
   ATTN_ERR_CUDA = 3,         /* a CUDA runtime or launch error */
   ATTN_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (reported by attn_status) */
   ATTN_ERR_NO_MEMORY = 5,    /* the decode workspace could not be allocated */
@@ -110,7 +112,7 @@ int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* 
  * [max(0, seqlens[b] - window), seqlens[b]) (all of them when window <= 0).
  * A seqlens entry outside [1, Tmax] zeroes that sequence's output and latches
  * ATTN_ERR_INVALID_ARG for attn_status().
- * With Hq / Hkv >= 8 (MQA-like groups) the step runs on the tensor cores
+ * With Hq / Hkv >= 8 (MQA-like groups) and Dh <= 128 the step runs on the tensor cores
  * (the group's query heads packed as the rows of one contraction with each
  * key tile) followed by a small combine kernel; otherwise on the CUDA cores.
  * The split-KV partials live in a library-owned device workspace, allocated

@@ -111,3 +111,16 @@ def test_many_sequences_with_one_key_each():
     q, kc, vc, sl = inputs.decode_inputs(300, 4, 1, 32, 64, 1, 1, seed=52)
     o = gpu_decode(q, kc, vc, sl).cpu()
     assert torch.equal(o, vc[:, :1].repeat_interleave(4, dim=1)[:, :, :1])
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tmax,lmin,lmax,window", [
+    (3, 8, 2, 3000, 1, 3000, 0),
+    (2, 16, 1, 1000, 900, 1000, 300),   # MQA at Dh 256 stays on the CUDA cores
+    (2, 4, 4, 700, 1, 700, 0),
+])
+def test_head_size_256(B, Hq, Hkv, Tmax, lmin, lmax, window):
+    """Dh = 256 (the Gemma head size): 16-key pipeline stages, a whole warp per key."""
+    q, kc, vc, sl = inputs.decode_inputs(B, Hq, Hkv, Tmax, 256, lmin, lmax, seed=Tmax + 256)
+    o = gpu_decode(q, kc, vc, sl, window=window)
+    ref = oracle.decode(q, kc, vc, sl, window=window)
+    assert_close(o.float().cpu().numpy(), ref, what=f"Dh 256 {(B, Hq, Hkv, Tmax, window)}")

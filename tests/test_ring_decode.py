@@ -53,6 +53,7 @@ CASES = [
     (2, 8, 4, 777, 128, [10000, 777 * 2], 500),        # ring not a multiple of a block
     (2, 8, 2, 640, 128, [639, 7001], 640),             # window == ring
     (1, 2, 2, 33, 128, [1000], 0),                     # a ring barely larger than a block
+    (2, 8, 2, 500, 256, [1234, 499], 0),               # Dh 256: 16-key stages
 ]
 
 
