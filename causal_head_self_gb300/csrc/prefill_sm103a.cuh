@@ -159,6 +159,7 @@ __device__ __forceinline__ bool spin_until_ge(volatile int* p, int v, volatile i
   if (*p >= v) return true;
   const uint64_t t0 = globaltimer_ns();
   while (*p < v) {
+    __nanosleep(20);   // leave issue slots to the softmax warps of this sub-partition
     if (*abort) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort = 1;
