@@ -13,6 +13,17 @@ static cudaError_t launch_prefill_dh(const CUtensorMap& mq, const CUtensorMap& m
   cudaError_t e = cudaFuncSetAttribute(attn_prefill_sm103a<DH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  // The warpgroups' register rebalance assumes the kernel was compiled to the
+  // full kRegsLaunch registers per thread; with fewer, the increase could
+  // wait forever, so refuse to launch.
+  static int regs = -1;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_prefill_sm103a<DH>);
+    if (e != cudaSuccess) return e;
+    regs = fa.numRegs;
+  }
+  if (regs < PrefillCfg<DH>::kRegsLaunch) return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM (the shared memory allows no second), each
   // walking its share of the work items
   const int grid = prm.num_items < num_sms ? prm.num_items : num_sms;

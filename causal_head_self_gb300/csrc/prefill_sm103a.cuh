@@ -17,7 +17,7 @@
 // Items are handed out heaviest first (causal work grows with the query
 // block) in "snake" order over the CTAs, and the TMA producer runs ahead
 // into the next item (its Q and K/V tiles) while the current one finishes.
-// Roles (352 threads):
+// Roles (384 threads):
 //   warps 0-3  softmax + epilogue of sub-tile 0 (thread t owns row t, TMEM lane t)
 //   warps 4-7  softmax + epilogue of sub-tile 1
 //   warp  8    TMEM allocation; issues the MMAs of sub-tile 0
@@ -82,7 +82,13 @@ struct PrefillCfg {
   static constexpr int kTileBytes = kHalves * kBoxBytes;
   static constexpr int kStagesK = DH == 128 ? 2 : 4;
   static constexpr int kStagesV = DH == 128 ? 2 : 4;
-  static constexpr int kThreads = 352;
+  static constexpr int kThreads = 384;   // 12 warps: three warpgroups
+  // Registers per thread after the warpgroups rebalance (setmaxnreg): the
+  // control warpgroup (warps 8-11) drops to kRegsControl, the two softmax
+  // warpgroups rise to kRegsSoftmax.  The sum stays within the launch's
+  // 384 x kRegsLaunch registers (the launcher checks the compiled count).
+  static constexpr int kRegsLaunch = 168, kRegsControl = 80, kRegsSoftmax = 208;
+  static_assert(4 * kRegsControl + 8 * kRegsSoftmax <= 12 * kRegsLaunch, "register split");
   static constexpr int kWarpProducer = 9;
   // warp issuing the MMAs of sub-tile s: 8 + 2 s (different sub-partitions)
   static constexpr int kWarpIssuer0 = 8, kWarpIssuer1 = 10;
@@ -594,7 +600,7 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
 }
 
 template <int DH>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_prefill_sm103a(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v, const PrefillParams p) {
@@ -646,16 +652,24 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t tbase = sm.tmem_base;
   // all 512 columns are this CTA's, so the allocation starts at column 0;
   // the MMA issuers rely on that (compile-time tensor-memory addresses)
-  if (tbase != 0) {
-    if (threadIdx.x == 0) sm.abort_flag = 1;
-  } else if (warp == Cfg::kWarpProducer) {
-    if (lane == 0) prefill_producer<DH>(sm, p, &map_q, &map_k, &map_v, first, abort);
-  } else if (warp == Cfg::kWarpIssuer0) {
-    prefill_issuer<DH, 0>(sm, p, abort, lane);
-  } else if (warp == Cfg::kWarpIssuer1) {
-    prefill_issuer<DH, 1>(sm, p, abort, lane);
-  } else if (warp < 8) {
-    prefill_softmax<DH>(sm, p, tbase, abort, warp, lane);
+  // Warpgroup-wide register rebalance (every warp of a warpgroup executes
+  // it), inside each role's branch so that the compiler gives the softmax
+  // code the larger budget.
+  if (tbase != 0 && threadIdx.x == 0) sm.abort_flag = 1;
+  if (warp >= 8) {
+    setmaxnreg_dec<Cfg::kRegsControl>();
+    if (tbase == 0) {
+      if (warp == Cfg::kWarpProducer) {
+        if (lane == 0) prefill_producer<DH>(sm, p, &map_q, &map_k, &map_v, first, abort);
+      } else if (warp == Cfg::kWarpIssuer0) {
+        prefill_issuer<DH, 0>(sm, p, abort, lane);
+      } else if (warp == Cfg::kWarpIssuer1) {
+        prefill_issuer<DH, 1>(sm, p, abort, lane);
+      }
+    }
+  } else {
+    setmaxnreg_inc<Cfg::kRegsSoftmax>();
+    if (tbase == 0) prefill_softmax<DH>(sm, p, tbase, abort, warp, lane);
   }
 
   // ---- teardown (every thread gets here; all waits above are bounded)
