@@ -55,15 +55,18 @@ size_t decode_counter_count(int B, int Hq, int Hkv, const DecodePlan& plan) {
 }
 
 template <int DH, int HPB>
-static cudaError_t launch_dh(const DecodeParams& prm, cudaStream_t stream) {
+static cudaError_t launch_dh(const DecodeParams& prm, int device, cudaStream_t stream) {
   constexpr size_t smem = decode_smem_bytes<DH, HPB>();
   auto kernel = attn_decode_sm103a<DH, HPB>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  // as much shared memory as the SM has, so that several CTAs fit
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           (int)cudaSharedmemCarveoutMaxShared);
+  static std::atomic<int> configured[kMaxDevices];
+  cudaError_t e = configure_once(configured, device, [kernel] {
+    cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (r != cudaSuccess) return r;
+    // as much shared memory as the SM has, so that several CTAs fit
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared);
+  });
   if (e != cudaSuccess) return e;
   const int groups = (prm.Hq / prm.Hkv) / HPB;
   dim3 grid(prm.Hkv * groups, prm.nsplit, prm.B);
@@ -72,10 +75,10 @@ static cudaError_t launch_dh(const DecodeParams& prm, cudaStream_t stream) {
 }
 
 template <int DH>
-static cudaError_t launch_hpb(const DecodeParams& prm, int hpb, cudaStream_t stream) {
-  if (hpb == 4) return launch_dh<DH, 4>(prm, stream);
-  if (hpb == 2) return launch_dh<DH, 2>(prm, stream);
-  return launch_dh<DH, 1>(prm, stream);
+static cudaError_t launch_hpb(const DecodeParams& prm, int hpb, int device, cudaStream_t stream) {
+  if (hpb == 4) return launch_dh<DH, 4>(prm, device, stream);
+  if (hpb == 2) return launch_dh<DH, 2>(prm, device, stream);
+  return launch_dh<DH, 1>(prm, device, stream);
 }
 
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int* seqlens,
@@ -105,9 +108,9 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
   prm.ring = ring;
-  if (Dh == 256) return launch_hpb<256>(prm, plan.heads_per_cta, stream);
-  return Dh == 128 ? launch_hpb<128>(prm, plan.heads_per_cta, stream)
-                   : launch_hpb<64>(prm, plan.heads_per_cta, stream);
+  if (Dh == 256) return launch_hpb<256>(prm, plan.heads_per_cta, dev.device, stream);
+  return Dh == 128 ? launch_hpb<128>(prm, plan.heads_per_cta, dev.device, stream)
+                   : launch_hpb<64>(prm, plan.heads_per_cta, dev.device, stream);
 }
 
 // ---------------------------------------------------------------- tensor-core path
@@ -136,11 +139,14 @@ DecodePlan plan_decode_tc(int B, int Hq, int Hkv, int Tmax, int num_sms) {
 
 template <int DH>
 static cudaError_t launch_tc_dh(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                                const DecodeTcParams& prm, cudaStream_t stream) {
+                                const DecodeTcParams& prm, int device, cudaStream_t stream) {
   constexpr size_t smem = decode_tc_smem_bytes<DH>();
   static_assert(smem <= 232448, "shared memory budget of one sm_103a CTA");
-  cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_sm103a<DH>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<int> configured[kMaxDevices];
+  cudaError_t e = configure_once(configured, device, [] {
+    return cudaFuncSetAttribute(attn_decode_tc_sm103a<DH>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
   if (e != cudaSuccess) return e;
   dim3 grid(prm.nsplit, prm.B * prm.Hkv * prm.row_blocks);
   attn_decode_tc_sm103a<DH><<<grid, DecodeTcCfg<DH>::kThreads, smem, stream>>>(mq, mk, mv, prm);
@@ -180,8 +186,8 @@ cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, cons
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
-  return Dh == 128 ? launch_tc_dh<128>(mq, mk, mv, prm, stream)
-                   : launch_tc_dh<64>(mq, mk, mv, prm, stream);
+  return Dh == 128 ? launch_tc_dh<128>(mq, mk, mv, prm, dev.device, stream)
+                   : launch_tc_dh<64>(mq, mk, mv, prm, dev.device, stream);
 }
 
 }  // namespace chs

@@ -2,11 +2,25 @@
 // translation units.  Not part of the public ABI (see include/attn.h).
 #pragma once
 
+#include <atomic>
+
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
 namespace chs {
+
+// Kernel attributes (shared-memory size, carveout) are set once per device:
+// `flags` is a per-kernel array of kMaxDevices entries.
+constexpr int kMaxDevices = 64;
+template <typename F>
+inline cudaError_t configure_once(std::atomic<int>* flags, int device, F&& set) {
+  const bool tracked = device >= 0 && device < kMaxDevices;
+  if (tracked && flags[device].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = set();
+  if (e == cudaSuccess && tracked) flags[device].store(1, std::memory_order_release);
+  return e;
+}
 
 struct DeviceInfo {
   int device;

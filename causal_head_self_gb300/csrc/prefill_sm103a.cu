@@ -7,11 +7,14 @@ namespace chs {
 template <int DH>
 static cudaError_t launch_prefill_dh(const CUtensorMap& mq, const CUtensorMap& mk,
                                      const CUtensorMap& mv, const PrefillParams& prm,
-                                     int num_sms, cudaStream_t stream) {
+                                     int num_sms, int device, cudaStream_t stream) {
   constexpr size_t smem = prefill_smem_bytes<DH>();
   static_assert(smem <= 232448, "shared memory budget of one sm_103a CTA");
-  cudaError_t e = cudaFuncSetAttribute(attn_prefill_sm103a<DH>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<int> configured[kMaxDevices];
+  cudaError_t e = configure_once(configured, device, [] {
+    return cudaFuncSetAttribute(attn_prefill_sm103a<DH>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
   if (e != cudaSuccess) return e;
   // The warpgroups' register rebalance assumes the kernel was compiled to the
   // full kRegsLaunch registers per thread; with fewer, the increase could
@@ -72,8 +75,8 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o,
   prm.div_bh = make_fast_div((uint32_t)(B * Hq));
   prm.div_hq = make_fast_div((uint32_t)Hq);
   prm.div_group = make_fast_div((uint32_t)(Hq / Hkv));
-  return Dh == 128 ? launch_prefill_dh<128>(mq, mk, mv, prm, dev.num_sms, stream)
-                   : launch_prefill_dh<64>(mq, mk, mv, prm, dev.num_sms, stream);
+  return Dh == 128 ? launch_prefill_dh<128>(mq, mk, mv, prm, dev.num_sms, dev.device, stream)
+                   : launch_prefill_dh<64>(mq, mk, mv, prm, dev.num_sms, dev.device, stream);
 }
 
 }  // namespace chs
