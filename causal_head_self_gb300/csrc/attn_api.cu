@@ -115,9 +115,11 @@ bool resolve_scale(float scale, int Dh, float* scale_log2) {
 namespace chs {
 
 bool encode_bf16_map(CUtensorMap* map, const void* base, int Dh, int rows, long long outer,
-                     int box_rows) {
+                     int box_rows, int stride_rows) {
+  if (stride_rows == 0) stride_rows = rows;
+  if (rows < 1 || stride_rows < rows) return false;
   cuuint64_t dims[3] = {(cuuint64_t)Dh, (cuuint64_t)rows, (cuuint64_t)outer};
-  cuuint64_t strides[2] = {(cuuint64_t)Dh * 2, (cuuint64_t)Dh * 2 * (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)Dh * 2, (cuuint64_t)Dh * 2 * (cuuint64_t)stride_rows};
   cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t elem[3] = {1, 1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
@@ -169,7 +171,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, int 
   if (B < 0 || Sq < 0 || Tkv < 0 || start_pos < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
     return ATTN_ERR_INVALID_ARG;
   if ((long long)start_pos + Sq > Tkv) return ATTN_ERR_INVALID_ARG;
-  if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Dh != 64 && Dh != 128 && Dh != 256) return ATTN_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (window < 0) window = 0;
   if (window > 0 && !causal) return ATTN_ERR_INVALID_ARG;
@@ -179,7 +181,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, int 
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
   const size_t qo_bytes = (size_t)B * Hq * Sq * Dh * 2, kv_bytes = (size_t)B * Hkv * Tkv * Dh * 2;
-  if ((long long)B * Hq * ((Sq + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * Hq * ((Sq + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, k, kv_bytes) ||
       overlaps(o, qo_bytes, v, kv_bytes))
     return ATTN_ERR_INVALID_ARG;

@@ -29,10 +29,13 @@ struct DeviceInfo {
   int fault;         // test hook passed to the kernels (attn_debug_inject_fault)
 };
 
-// Encode a 3-D tensor map over a contiguous [outer, rows, Dh] bf16 tensor:
-// dims {Dh, rows, outer}, 128-byte swizzle, box {64, box_rows, 1}.
+// Encode a 3-D tensor map over a [outer, stride_rows, Dh] bf16 tensor of
+// which the first `rows` rows per outer index are visible: dims {Dh, rows,
+// outer}, 128-byte swizzle, box {64, box_rows, 1}.  Rows at or past `rows`
+// are never read; a box reaching past them is zero-filled
+// (stride_rows = 0 means stride_rows = rows).
 bool encode_bf16_map(CUtensorMap* map, const void* base, int Dh, int rows, long long outer,
-                     int box_rows);
+                     int box_rows, int stride_rows = 0);
 
 // Queries: Sq rows per (b, h), at positions start_pos .. start_pos + Sq - 1.
 // K, V: Tkv rows per (b, K/V head) in memory, of which the first

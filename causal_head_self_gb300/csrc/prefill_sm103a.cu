@@ -1,5 +1,6 @@
 // prefill_sm103a.cu -- host launcher of the tcgen05 prefill kernel.
 #include "launch.h"
+#include "prefill256_sm103a.cuh"
 #include "prefill_sm103a.cuh"
 
 namespace chs {
@@ -43,23 +44,73 @@ static FastDiv make_fast_div(uint32_t d) {
   return FastDiv{(uint32_t)m, 31 + l, d};
 }
 
+// Head size 256: one 128-row sub-tile per work item, 64-key tiles.
+static cudaError_t launch_prefill256(const void* q, const void* k, const void* v, void* o, int B,
+                                     int Hq, int Hkv, int Sq, int Tkv, int start_pos, int causal,
+                                     int window, float scale_log2, const DeviceInfo& dev,
+                                     cudaStream_t stream) {
+  using Cfg = Prefill256Cfg;
+  const int Skv = start_pos + Sq;
+  CUtensorMap mq, mk, mv;
+  if (!encode_bf16_map(&mq, q, Cfg::DH, Sq, (long long)B * Hq, 128) ||
+      !encode_bf16_map(&mk, k, Cfg::DH, Skv, (long long)B * Hkv, Cfg::kKeys, Tkv) ||
+      !encode_bf16_map(&mv, v, Cfg::DH, Skv, (long long)B * Hkv, Cfg::kKeys, Tkv))
+    return cudaErrorInvalidValue;
+  Prefill256Params prm;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.q_off = start_pos;
+  prm.causal = causal;
+  prm.window = window;
+  prm.scale_log2 = scale_log2;
+  prm.num_qblocks = (Sq + 127) / 128;
+  prm.per_qb = B * Hq;
+  prm.group = Hq / Hkv;
+  const long long items = (long long)prm.num_qblocks * B * Hq;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  prm.num_items = (int)items;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.o_wide = (reinterpret_cast<uintptr_t>(o) & 31) == 0;
+  prm.error_word = dev.error_word;
+  prm.fault = dev.fault;
+  constexpr size_t smem = prefill256_smem_bytes();
+  static_assert(smem <= 232448, "shared memory budget of one sm_103a CTA");
+  static std::atomic<int> configured[kMaxDevices];
+  cudaError_t e = configure_once(configured, dev.device, [] {
+    return cudaFuncSetAttribute(attn_prefill256_sm103a,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
+  const int grid = prm.num_items < dev.num_sms ? prm.num_items : dev.num_sms;
+  attn_prefill256_sm103a<<<grid, Cfg::kThreads, smem, stream>>>(mq, mk, mv, prm);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
                            int Hkv, int Sq, int Tkv, int start_pos, int Dh, int causal,
                            int window, float scale_log2, const DeviceInfo& dev,
                            cudaStream_t stream) {
+  if (Dh == 256)
+    return launch_prefill256(q, k, v, o, B, Hq, Hkv, Sq, Tkv, start_pos, causal, window,
+                             scale_log2, dev, stream);
   // K and V hold Tkv rows per head in memory; the chunk sees the first
-  // start_pos + Sq of them
+  // start_pos + Sq of them, and the maps cover only those (the last key
+  // tile's rows past them are zero-filled, never read from the cache)
+  const int Skv = start_pos + Sq;
   CUtensorMap mq, mk, mv;
   if (!encode_bf16_map(&mq, q, Dh, Sq, (long long)B * Hq, 128) ||
-      !encode_bf16_map(&mk, k, Dh, Tkv, (long long)B * Hkv, 128) ||
-      !encode_bf16_map(&mv, v, Dh, Tkv, (long long)B * Hkv, 128))
+      !encode_bf16_map(&mk, k, Dh, Skv, (long long)B * Hkv, 128, Tkv) ||
+      !encode_bf16_map(&mv, v, Dh, Skv, (long long)B * Hkv, 128, Tkv))
     return cudaErrorInvalidValue;
   PrefillParams prm;
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
   prm.Sq = Sq;
-  prm.Skv = start_pos + Sq;
+  prm.Skv = Skv;
   prm.q_off = start_pos;
   prm.causal = causal;
   prm.window = window;

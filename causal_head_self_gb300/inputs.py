@@ -27,6 +27,12 @@ WORKLOADS = {
     # causal GQA prefill (32 query heads over 8 K/V heads) with a 4096-key sliding window
     "prefill_gqa_b1_h32kv8_s32768_d128_w4096": dict(kind="prefill", B=1, Hq=32, Hkv=8, S=32768,
                                                     Dh=128, causal=True, window=4096, seed=3),
+    # causal GQA prefill at head size 256 (16 query heads over 8 K/V heads),
+    # without and with a 4096-key sliding window
+    "prefill_gqa_b1_h16kv8_s8192_d256": dict(kind="prefill", B=1, Hq=16, Hkv=8, S=8192, Dh=256,
+                                             causal=True, window=0, seed=6),
+    "prefill_gqa_b1_h16kv8_s8192_d256_w4096": dict(kind="prefill", B=1, Hq=16, Hkv=8, S=8192,
+                                                   Dh=256, causal=True, window=4096, seed=6),
     # one decode step for 16 sequences against caches of 16384..32768 keys
     "decode_gqa_b16_h32kv8_t32768_d128": dict(kind="decode", B=16, Hq=32, Hkv=8, Tmax=32768,
                                               Dh=128, lmin=16384, lmax=32768, window=0, seed=4),

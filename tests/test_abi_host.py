@@ -59,7 +59,7 @@ def fwd(lib, *args, ptrs=P, scale=0.0):
     ((1, 4, 0, 16, 128, 1, 0), _binding.ATTN_ERR_INVALID_ARG),   # no K/V head
     ((-1, 4, 4, 16, 128, 1, 0), _binding.ATTN_ERR_INVALID_ARG),  # negative batch
     ((1, 4, 4, 16, 96, 1, 0), _binding.ATTN_ERR_UNSUPPORTED),    # head size
-    ((1, 4, 4, 16, 256, 1, 0), _binding.ATTN_ERR_UNSUPPORTED),
+    ((1, 4, 4, 16, 512, 1, 0), _binding.ATTN_ERR_UNSUPPORTED),
     ((1, 4, 4, 16, 128, 0, 8), _binding.ATTN_ERR_INVALID_ARG),   # window without causal
     ((1, 4, 4, 16, 128, 2, 0), _binding.ATTN_ERR_INVALID_ARG),   # causal flag not 0/1
     ((0, 4, 4, 16, 128, 1, 0), _binding.ATTN_OK),                # empty batch: no-op

@@ -117,3 +117,17 @@ def test_chunk_rejects_a_chunk_past_the_cache():
     with pytest.raises(chs.AttnError) as e:
         chs.attn_fwd_chunk(q.to(d), kc.to(d), vc.to(d), 201)
     assert e.value.code == chs.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("Dh", [64, 128])
+def test_cache_rows_past_the_chunk_are_never_read(Dh):
+    """Cache rows at or past start_pos + Sq hold NaN: the last key tile
+    reaches past them (start_pos + Sq is not a multiple of the tile) but the
+    output must not see them."""
+    B, Hq, Hkv, Sq, Tmax, start = 2, 4, 2, 150, 900, 333
+    q, kc, vc = _chunk_inputs(B, Hq, Hkv, Sq, Tmax, Dh, seed=36 + Dh)
+    ref = _oracle_chunk(q, kc, vc, start, 1, 0)
+    kc[:, :, start + Sq:] = float("nan")
+    vc[:, :, start + Sq:] = float("nan")
+    o = _gpu_chunk(q, kc, vc, start, 1, 0)
+    assert_close(o.float().cpu().numpy(), ref, what="NaN past the chunk")
