@@ -19,9 +19,8 @@
  *     ("多头注意力机制" (blog.euler0525.cn), section "Multi-head Attention":
  *     heads moved ahead of the sequence axis).  All tensor pointers are
  *     DEVICE pointers, 16-byte aligned.  The caller owns every tensor.
- *   - Dh must be 64 or 128 for the prefill entry points and 64, 128 or 256
- *     (the Gemma head size) for the decode ones (ATTN_ERR_UNSUPPORTED
- *     otherwise).
+ *   - Dh must be 64, 128 or 256 (the Gemma head size) for every entry
+ *     point (ATTN_ERR_UNSUPPORTED otherwise).
  *   - Hq % Hkv == 0 is required (ATTN_ERR_INVALID_ARG otherwise).
  *   - scale == 0 selects 1/sqrt(Dh), the textbook's choice (divide by the
  *     square root of the HEAD size, not the model width); a positive scale is
