@@ -25,9 +25,9 @@ ATTN_ERR_NO_MEMORY = 5
 ATTN_ERR_SCRATCH_LIMIT = 6
 
 # every symbol include/attn.h declares
-ABI_SYMBOLS = ("attn_fwd", "attn_fwd_chunk", "attn_decode", "attn_decode_ring", "attn_decode_noalloc",
-               "attn_status",
-               "attn_error_string", "attn_version", "attn_debug_inject_fault")
+ABI_SYMBOLS = ("attn_fwd", "attn_fwd_lse", "attn_fwd_chunk", "attn_bwd", "attn_decode",
+               "attn_decode_ring", "attn_decode_noalloc", "attn_status", "attn_error_string",
+               "attn_version", "attn_debug_inject_fault")
 
 _lib = None
 _lock = threading.Lock()
@@ -51,6 +51,10 @@ def load():
             vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             lib.attn_fwd.restype = i
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+            lib.attn_fwd_lse.restype = i
+            lib.attn_fwd_lse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+            lib.attn_bwd.restype = i
+            lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
             lib.attn_fwd_chunk.restype = i
             lib.attn_fwd_chunk.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
             lib.attn_decode.restype = i
@@ -113,6 +117,66 @@ def attn_fwd(q, k, v, o=None, *, causal=True, window=0, scale=0.0, stream=None):
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return o
+
+
+def attn_fwd_lse(q, k, v, o=None, lse=None, *, causal=True, window=0, scale=0.0, stream=None):
+    """attn_fwd that also returns each row's log-sum-exp lse [B,Hq,S] fp32
+    (natural log of the softmax normaliser).  Returns (o, lse)."""
+    _check_bf16("q", q, 4)
+    _check_bf16("k", k, 4)
+    _check_bf16("v", v, 4)
+    B, Hq, S, Dh = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, S, Dh) or tuple(v.shape) != (B, Hkv, S, Dh):
+        raise ValueError("k and v must be [B, Hkv, S, Dh] matching q")
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _check_bf16("o", o, 4)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    elif (lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, S) or not lse.is_cuda
+          or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous CUDA float32 [B, Hq, S] tensor")
+    rc = load().attn_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), B, Hq, Hkv, S, Dh, int(bool(causal)), int(window),
+                             float(scale), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_lse")
+    return o, lse
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq=None, dk=None, dv=None, *, causal=True, window=0,
+             scale=0.0, stream=None):
+    """Backward pass of attn_fwd_lse: (dq, dk, dv) from q, k, v, its output o,
+    its lse and dout = dL/do (all as attn_fwd_lse took / returned them)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_bf16(name, t, 4)
+    B, Hq, S, Dh = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, S, Dh) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, S, Dh] matching q")
+    if o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("o and dout must have q's shape")
+    if (lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, S) or not lse.is_cuda
+            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous CUDA float32 [B, Hq, S] tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _check_bf16(name, t, 4)
+        if t.shape != ref.shape:
+            raise ValueError(f"{name} must have the shape of its input")
+    rc = load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv,
+                         S, Dh, int(bool(causal)), int(window), float(scale),
+                         _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_chunk(q, kcache, vcache, start_pos, o=None, *, causal=True, window=0, scale=0.0,

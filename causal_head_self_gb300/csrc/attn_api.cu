@@ -31,6 +31,9 @@ struct DeviceState {
   size_t partials_bytes = 0;
   int* counters = nullptr;
   size_t counters_n = 0;
+  // backward workspace: per-row log-sum-exp (log2 units) and D = dO . o
+  void* bwd_ws = nullptr;
+  size_t bwd_ws_bytes = 0;
 };
 
 // Grow a device buffer (never inside a stream capture); zero it if asked.
@@ -165,9 +168,9 @@ int attn_debug_inject_fault(int kind) {
 // Shared by attn_fwd and attn_fwd_chunk: queries at positions
 // start_pos .. start_pos + Sq - 1 against the first start_pos + Sq of Tkv
 // key/value rows per head.
-static int fwd_common(const void* q, const void* k, const void* v, void* o, int B, int Hq,
-                      int Hkv, int Sq, int Tkv, int start_pos, int Dh, int causal, int window,
-                      float scale, cudaStream_t stream) {
+static int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int Sq, int Tkv, int start_pos, int Dh, int causal,
+                      int window, float scale, cudaStream_t stream) {
   if (B < 0 || Sq < 0 || Tkv < 0 || start_pos < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
     return ATTN_ERR_INVALID_ARG;
   if ((long long)start_pos + Sq > Tkv) return ATTN_ERR_INVALID_ARG;
@@ -185,25 +188,39 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, int 
   if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, k, kv_bytes) ||
       overlaps(o, qo_bytes, v, kv_bytes))
     return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr) {
+    const size_t lse_bytes = (size_t)B * Hq * Sq * 4;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3) != 0 || overlaps(lse, lse_bytes, o, qo_bytes) ||
+        overlaps(lse, lse_bytes, q, qo_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
+        overlaps(lse, lse_bytes, v, kv_bytes))
+      return ATTN_ERR_INVALID_ARG;
+  }
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
-  cudaError_t e = chs::launch_prefill(q, k, v, o, B, Hq, Hkv, Sq, Tkv, start_pos, Dh, causal,
+  cudaError_t e = chs::launch_prefill(q, k, v, o, lse, B, Hq, Hkv, Sq, Tkv, start_pos, Dh, causal,
                                       window, scale_log2, launch_info(st), stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int S,
              int Dh, int causal, int window, float scale, cudaStream_t stream) {
-  return fwd_common(q, k, v, o, B, Hq, Hkv, S, S, 0, Dh, causal, window, scale, stream);
+  return fwd_common(q, k, v, o, nullptr, B, Hq, Hkv, S, S, 0, Dh, causal, window, scale, stream);
+}
+
+int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int S, int Dh, int causal, int window, float scale,
+                 cudaStream_t stream) {
+  if (lse == nullptr && B > 0 && S > 0) return ATTN_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, S, S, 0, Dh, causal, window, scale, stream);
 }
 
 int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* o, int B, int Hq,
                    int Hkv, int Sq, int Tmax, int start_pos, int Dh, int causal, int window,
                    float scale, cudaStream_t stream) {
   if (Tmax < 1) return ATTN_ERR_INVALID_ARG;
-  return fwd_common(q, kcache, vcache, o, B, Hq, Hkv, Sq, Tmax, start_pos, Dh, causal, window,
-                    scale, stream);
+  return fwd_common(q, kcache, vcache, o, nullptr, B, Hq, Hkv, Sq, Tmax, start_pos, Dh, causal,
+                    window, scale, stream);
 }
 
 // Shared by attn_decode (ring = 0) and attn_decode_ring (ring = 1).
@@ -270,6 +287,52 @@ static int decode_common(const void* q, const void* kcache, const void* vcache, 
   cudaError_t e = chs::launch_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, window,
                                      ring, scale_log2, plan, counters, partials, launch_info(st),
                                      stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dh,
+             int causal, int window, float scale, cudaStream_t stream) {
+  if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (window < 0) window = 0;
+  if (window > 0 && !causal) return ATTN_ERR_INVALID_ARG;
+  float scale_log2 = 0.f;
+  if (!resolve_scale(scale, Dh, &scale_log2)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return ATTN_OK;
+  const void* in[] = {q, k, v, o, dout};
+  void* out[] = {dq, dk, dv};
+  for (const void* x : in)
+    if (!x || !aligned16(x)) return ATTN_ERR_INVALID_ARG;
+  for (const void* x : out)
+    if (!x || !aligned16(x)) return ATTN_ERR_INVALID_ARG;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * Hq * ((S + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  const size_t qb = (size_t)B * Hq * S * Dh * 2, kb = (size_t)B * Hkv * S * Dh * 2;
+  const size_t in_bytes[] = {qb, kb, kb, qb, qb};
+  const size_t out_bytes[] = {qb, kb, kb};
+  for (int a = 0; a < 3; ++a) {
+    for (int b = 0; b < 5; ++b)
+      if (overlaps(out[a], out_bytes[a], in[b], in_bytes[b])) return ATTN_ERR_INVALID_ARG;
+    if (overlaps(out[a], out_bytes[a], lse, (size_t)B * Hq * S * 4)) return ATTN_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlaps(out[a], out_bytes[a], out[b], out_bytes[b])) return ATTN_ERR_INVALID_ARG;
+  }
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != ATTN_OK) return rc;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    rc = grow_buffer(&st->bwd_ws, &st->bwd_ws_bytes, chs::bwd_workspace_bytes(B, Hq, S), false,
+                     stream);
+    if (rc != ATTN_OK) return rc;
+    ws = st->bwd_ws;
+  }
+  const float sc = scale == 0.f ? (float)(1.0 / std::sqrt((double)Dh)) : scale;
+  cudaError_t e = chs::launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, static_cast<float*>(ws), B,
+                                  Hq, Hkv, S, Dh, causal, window, sc, launch_info(st), stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

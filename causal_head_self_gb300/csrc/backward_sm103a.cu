@@ -1,0 +1,83 @@
+// backward_sm103a.cu -- host launcher of the backward pass: D and lse2 per
+// row, then the dK/dV pass and the dQ pass on the same stream.
+#include "backward_sm103a.cuh"
+#include "launch.h"
+
+namespace chs {
+
+template <int DH>
+static cudaError_t launch_bwd_dh(const CUtensorMap& mq, const CUtensorMap& mk,
+                                 const CUtensorMap& mv, const CUtensorMap& mdo, const BwdParams& prm,
+                                 const void* o, const void* dout, const float* lse, float* lse2,
+                                 float* delta, const DeviceInfo& dev, cudaStream_t stream) {
+  constexpr size_t smem_kv = bwd_dkdv_smem_bytes<DH>(), smem_q = bwd_dq_smem_bytes<DH>();
+  static_assert(smem_kv <= 232448 && smem_q <= 232448, "shared memory budget of one sm_103a CTA");
+  static std::atomic<int> configured[kMaxDevices];
+  cudaError_t e = configure_once(configured, dev.device, [] {
+    cudaError_t r = cudaFuncSetAttribute(attn_bwd_dkdv<DH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(attn_bwd_dq<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_q);
+  });
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)prm.B * prm.Hq * prm.S_pad;
+  attn_bwd_prep<DH><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2,
+      delta, rows, prm.S, prm.S_pad);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // persistent passes: one CTA per SM (their shared memory allows no second)
+  BwdParams pk = prm;
+  pk.num_items = prm.nblk * prm.B * prm.Hkv;
+  const int grid_kv = pk.num_items < dev.num_sms ? pk.num_items : dev.num_sms;
+  attn_bwd_dkdv<DH><<<grid_kv, BwdCfg<DH>::kThreads, smem_kv, stream>>>(mq, mk, mv, mdo, pk);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  BwdParams pq = prm;
+  pq.num_items = prm.nblk * prm.B * prm.Hq;
+  const int grid_q = pq.num_items < dev.num_sms ? pq.num_items : dev.num_sms;
+  attn_bwd_dq<DH><<<grid_q, BwdCfg<DH>::kThreads, smem_q, stream>>>(mq, mk, mv, mdo, pq);
+  return cudaGetLastError();
+}
+
+size_t bwd_workspace_bytes(int B, int Hq, int S) {
+  const size_t S_pad = ((size_t)S + 127) / 128 * 128;
+  return 2 * (size_t)B * Hq * S_pad * sizeof(float);
+}
+
+cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       float* workspace, int B, int Hq, int Hkv, int S, int Dh, int causal,
+                       int window, float scale, const DeviceInfo& dev, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_bf16_map(&mq, q, Dh, S, (long long)B * Hq, 128) ||
+      !encode_bf16_map(&mdo, dout, Dh, S, (long long)B * Hq, 128) ||
+      !encode_bf16_map(&mk, k, Dh, S, (long long)B * Hkv, 128) ||
+      !encode_bf16_map(&mv, v, Dh, S, (long long)B * Hkv, 128))
+    return cudaErrorInvalidValue;
+  BwdParams prm{};
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.S = S;
+  prm.causal = causal;
+  prm.window = window;
+  prm.scale = scale;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  prm.nblk = (S + 127) / 128;
+  prm.S_pad = prm.nblk * 128;
+  prm.group = Hq / Hkv;
+  if ((long long)prm.nblk * B * Hq > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (((long long)B * Hq * prm.S_pad + 7) / 8 > 0x7fffffffLL) return cudaErrorInvalidValue;
+  float* lse2 = workspace;
+  float* delta = workspace + (size_t)B * Hq * prm.S_pad;
+  prm.lse2 = lse2;
+  prm.delta = delta;
+  prm.dq = static_cast<__nv_bfloat16*>(dq);
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.error_word = dev.error_word;
+  return Dh == 128 ? launch_bwd_dh<128>(mq, mk, mv, mdo, prm, o, dout, lse, lse2, delta, dev, stream)
+                   : launch_bwd_dh<64>(mq, mk, mv, mdo, prm, o, dout, lse, lse2, delta, dev, stream);
+}
+
+}  // namespace chs

@@ -1,0 +1,843 @@
+// backward_sm103a.cuh -- backward pass of causal self-attention on the
+// 5th-generation tensor cores (sm_103a), Dh = 64 or 128.
+//
+// Given q, k, v, the forward output o, its row log-sum-exps and the upstream
+// gradient dO, the gradients follow from the chain rule through
+// o_i = sum_j p_ij v_j, p_i = softmax(s_i) and s_ij = scale q_i . k_j, with
+// the softmax derivative dp_i/dz_j = p_i (delta_ij - p_j) of "Механизм
+// внимания", section "Почему делить на корень из d_h":
+//     dV = P^T dO,   dP = dO V^T,   dS = P o (dP - D),  D_i = dO_i . o_i,
+//     dK = scale dS^T Q,   dQ = scale dS K.
+// (D_i = sum_j p_ij dp_ij, the contraction of that Jacobian, because
+// o_i = sum_j p_ij v_j.)  As section "Эффективные реализации" of the same
+// page describes for FlashAttention, the weights P are recomputed block by
+// block from the saved log-sum-exp, never stored.
+//
+// Three kernels, all deterministic (no atomics anywhere):
+//   attn_bwd_prep      D_i and the log-sum-exp in units of log2, per row;
+//   attn_bwd_dkdv      one CTA per 128-key block of one K/V head: K and V
+//                      stay in shared memory while the query blocks of every
+//                      query head of the group stream past; S^T = K Q^T and
+//                      dP^T = V dO^T land in tensor memory, the softmax
+//                      warps turn them into P^T and dS^T (bf16, written over
+//                      them), and dV += P^T dO, dK += dS^T Q accumulate in
+//                      tensor memory (M = 128 keys);
+//   attn_bwd_dq        one CTA per 128-row query block: Q and dO stay, the
+//                      key blocks stream past; S = Q K^T and dP = dO V^T,
+//                      dS as above, dQ += dS K (M = 128 queries).
+// dQ is computed by its own pass (recomputing S and dP) instead of being
+// reduced across key blocks with atomics: 7 MMAs per block pair instead of 5,
+// in exchange for a deterministic result.
+//
+// Roles as in the forward kernels: warps 0-3 (thread t owns tensor-memory
+// lane t) run the element-wise work and the epilogue, warp 4 lane 0 issues
+// every TMA copy, warp 5 issues every MMA (one elected lane).  Every wait is
+// bounded.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "sm103a_ptx.cuh"
+
+namespace chs {
+
+struct BwdParams {
+  int B, Hq, Hkv, S;
+  int causal, window;     // as in the forward (window > 0 only with causal)
+  float scale_log2;       // scale * log2(e)
+  float scale;            // applied to dK and dQ
+  int S_pad;              // S rounded up to 128: row stride of lse2 and delta
+  int nblk;               // ceil(S / 128)
+  int group;              // Hq / Hkv
+  int num_items;
+  const float* lse2;      // [B * Hq, S_pad] log2 of sum_j 2^(s_ij log2 e); +inf past S
+  const float* delta;     // [B * Hq, S_pad] D_i = dO_i . o_i; 0 past S
+  __nv_bfloat16* dq;      // [B, Hq, S, DH]
+  __nv_bfloat16* dk;      // [B, Hkv, S, DH]
+  __nv_bfloat16* dv;      // [B, Hkv, S, DH]
+  int* error_word;
+};
+
+template <int DH>
+struct BwdCfg {
+  static constexpr int kBox = 128 * 64 * 2;         // one 128-row x 64-column box
+  static constexpr int kTile = (DH / 64) * kBox;    // a 128 x DH tile
+  static constexpr int kThreads = 192;
+  static constexpr int kWarpProducer = 4, kWarpIssuer = 5;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColA0 = 256, kColA1 = 384;
+};
+
+// D_i = sum_d dO[i, d] o[i, d] (fp32 products of the bf16 values) and
+// lse2_i = lse_i * log2(e), one warp per row of [B * Hq, S_pad]; rows past S
+// get D = 0 and lse2 = +inf (their weights exp2(x - lse2) are then 0).
+template <int DH>
+__global__ void __launch_bounds__(256)
+    attn_bwd_prep(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                  const float* __restrict__ lse, float* __restrict__ lse2,
+                  float* __restrict__ delta, long long rows, int S, int S_pad) {
+  const long long r = (long long)blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (r >= rows) return;
+  const long long bh = r / S_pad;
+  const int i = (int)(r - bh * S_pad);
+  if (i >= S) {
+    if (lane == 0) {
+      delta[r] = 0.f;
+      lse2[r] = __int_as_float(0x7f800000);
+    }
+    return;
+  }
+  const size_t base = ((size_t)bh * S + i) * DH;
+  float acc = 0.f;
+  constexpr int kPer = DH / 32;   // 4 or 2 bf16 per lane
+  if constexpr (kPer == 4) {
+    const uint2 a = *reinterpret_cast<const uint2*>(o + base + 4 * lane);
+    const uint2 b = *reinterpret_cast<const uint2*>(dout + base + 4 * lane);
+    const uint32_t wa[2] = {a.x, a.y}, wb[2] = {b.x, b.y};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      acc = fmaf(__uint_as_float(wa[e] << 16), __uint_as_float(wb[e] << 16), acc);
+      acc = fmaf(__uint_as_float(wa[e] & 0xffff0000u), __uint_as_float(wb[e] & 0xffff0000u), acc);
+    }
+  } else {
+    const uint32_t wa = *reinterpret_cast<const uint32_t*>(o + base + 2 * lane);
+    const uint32_t wb = *reinterpret_cast<const uint32_t*>(dout + base + 2 * lane);
+    acc = fmaf(__uint_as_float(wa << 16), __uint_as_float(wb << 16), acc);
+    acc = fmaf(__uint_as_float(wa & 0xffff0000u), __uint_as_float(wb & 0xffff0000u), acc);
+  }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (lane == 0) {
+    delta[r] = acc;
+    lse2[r] = lse[(size_t)bh * S + i] * 1.4426950408889634f;
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// x if off <= span (unsigned), else 0 (a predicated select; see keep_if_le)
+__device__ __forceinline__ float zero_unless_le(float x, uint32_t off, uint32_t span) {
+  float d;
+  asm("{\n .reg .pred p;\n setp.le.u32 p, %1, %2;\n selp.f32 %0, %3, 0f00000000, p;\n}"
+      : "=f"(d) : "r"(off), "r"(span), "f"(x));
+  return d;
+}
+
+__device__ __forceinline__ void bwd_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// Heaviest-first snake order over the CTAs (as in the forward kernels).
+__device__ __forceinline__ int bwd_item(int k, int c, int G) {
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+// Query blocks [lo, hi] that see some key of key block kb (128-row blocks).
+__device__ __forceinline__ void bwd_qblocks_of(const BwdParams& p, int kb, int& lo, int& hi) {
+  if (!p.causal) {
+    lo = 0;
+    hi = p.nblk - 1;
+    return;
+  }
+  lo = kb;   // query i sees key j only if j <= i
+  hi = p.nblk - 1;
+  if (p.window > 0) hi = min(hi, (128 * kb + 127 + p.window - 1) / 128);   // i - j < W
+}
+
+// Key blocks [lo, hi] that query block qb sees.
+__device__ __forceinline__ void bwd_kblocks_of(const BwdParams& p, int qb, int& lo, int& hi) {
+  if (!p.causal) {
+    lo = 0;
+    hi = p.nblk - 1;
+    return;
+  }
+  hi = qb;
+  lo = p.window > 0 ? max(0, 128 * qb - p.window + 1) / 128 : 0;
+}
+
+// Does some (query, key) pair of query block qb x key block kb fall outside
+// the mask (or past S)?
+__device__ __forceinline__ bool bwd_needs_mask(const BwdParams& p, int qb, int kb) {
+  if (128 * kb + 127 >= p.S || 128 * qb + 127 >= p.S) return true;
+  if (!p.causal) return false;
+  if (128 * kb + 127 > 128 * qb) return true;                                  // j > i somewhere
+  if (p.window > 0 && 128 * qb + 127 - 128 * kb >= p.window) return true;      // i - j >= W somewhere
+  return false;
+}
+
+// ============================================================ dK, dV pass
+
+template <int DH>
+struct __align__(1024) BwdKvSmem {
+  using Cfg = BwdCfg<DH>;
+  uint8_t k[Cfg::kTile];           // this item's key block (stays)
+  uint8_t v[Cfg::kTile];           // this item's value block (stays)
+  uint8_t q[2][Cfg::kTile];        // query blocks, two stages
+  uint8_t dO[2][Cfg::kTile];       // their output gradients
+  float lse2[2][128];              // their log-sum-exps (log2 units)
+  float dlt[2][128];               // their D_i
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full, acc_final, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Item w of the dK/dV pass: key block kb (heaviest, i.e. earliest, first
+// under a causal mask) of K/V head bkv = b * Hkv + g.
+struct BwdKvItem {
+  int kb, bkv, b, g, lo, hi;
+};
+
+__device__ __forceinline__ BwdKvItem bwd_kv_item_of(const BwdParams& p, int w) {
+  BwdKvItem r;
+  const int per = p.B * p.Hkv;
+  r.kb = w / per;
+  r.bkv = w - r.kb * per;
+  r.b = r.bkv / p.Hkv;
+  r.g = r.bkv - r.b * p.Hkv;
+  bwd_qblocks_of(p, r.kb, r.lo, r.hi);
+  return r;
+}
+
+template <int DH>
+__device__ __forceinline__ void bwd_dkdv_producer(BwdKvSmem<DH>& sm, const BwdParams& p,
+                                                  const CUtensorMap* map_q,
+                                                  const CUtensorMap* map_k,
+                                                  const CUtensorMap* map_v,
+                                                  const CUtensorMap* map_do, volatile int* abort) {
+  using Cfg = BwdCfg<DH>;
+  constexpr int kBoxes = DH / 64;
+  const uint64_t keep = policy_evict_last();   // query blocks are re-read by other key blocks
+  uint32_t u = 0, loaded = 0, par = 0;
+  int items = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int w = bwd_item(it, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    const BwdKvItem I = bwd_kv_item_of(p, w);
+    if (items > 0 && !(ok = mbar_wait(&sm.kv_empty, (uint32_t)(items - 1) & 1u, abort))) break;
+    mbar_arrive_expect_tx(&sm.kv_full, 2 * Cfg::kTile);
+    for (int hf = 0; hf < kBoxes; ++hf) {
+      tma_load_3d(sm.k + hf * Cfg::kBox, map_k, &sm.kv_full, 64 * hf, 128 * I.kb, I.bkv);
+      tma_load_3d(sm.v + hf * Cfg::kBox, map_v, &sm.kv_full, 64 * hf, 128 * I.kb, I.bkv);
+    }
+    ++items;
+    for (int hh = 0; ok && hh < p.group; ++hh) {
+      const int bh = I.b * p.Hq + I.g * p.group + hh;
+      for (int qb = I.lo; qb <= I.hi; ++qb, ++u) {
+        const int st = (int)(u & 1u);
+        const uint32_t ph = (u >> 1) & 1u;
+        if (!(ok = mbar_wait(&sm.q_empty[st], ph ^ 1u, abort))) break;
+        mbar_arrive_expect_tx(&sm.q_full[st], 2 * Cfg::kTile + 2 * 512);
+        for (int hf = 0; hf < kBoxes; ++hf) {
+          tma_load_3d_hint(sm.q[st] + hf * Cfg::kBox, map_q, &sm.q_full[st], 64 * hf, 128 * qb, bh,
+                           keep);
+          tma_load_3d_hint(sm.dO[st] + hf * Cfg::kBox, map_do, &sm.q_full[st], 64 * hf, 128 * qb,
+                           bh, keep);
+        }
+        const size_t row0 = (size_t)bh * p.S_pad + 128 * qb;
+        bulk_load(sm.lse2[st], p.lse2 + row0, 512, &sm.q_full[st], keep);
+        bulk_load(sm.dlt[st], p.delta + row0, 512, &sm.q_full[st], keep);
+        loaded |= 1u << st;
+        par = (par & ~(1u << st)) | (ph << st);
+      }
+    }
+  }
+  // every copy this thread started has landed before the CTA may exit
+  if (items > 0) bwd_wait_drain(&sm.kv_full, (uint32_t)(items - 1) & 1u);
+  for (int i = 0; i < 2; ++i)
+    if (loaded & (1u << i)) bwd_wait_drain(&sm.q_full[i], (par >> i) & 1u);
+}
+
+// MMA issue order per item of N steps (one step = one query block of one
+// query head): S(0), dP(0), then per step n: dV(n) once P(n) is written,
+// S(n+1) (its columns held P(n), which dV(n), issued before it, reads),
+// dK(n) once dS(n) is written, dP(n+1) (its columns held dS(n)).  The
+// element-wise work of step n+1 therefore overlaps dK(n) and dP(n+1).
+template <int DH>
+__device__ __forceinline__ void bwd_dkdv_issuer(BwdKvSmem<DH>& sm, const BwdParams& p,
+                                                volatile int* abort) {
+  using Cfg = BwdCfg<DH>;
+  constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t idesc_acc = idesc_bf16_f32(128, DH, false, true);
+  constexpr uint64_t kKmajor = smem_desc_sw128(0, 16, 1024);
+  constexpr uint64_t kMnMajor = smem_desc_sw128(0, Cfg::kBox, 1024);
+  const uint64_t dk_ = kKmajor | (smem_u32(sm.k) >> 4);
+  const uint64_t dv_ = kKmajor | (smem_u32(sm.v) >> 4);
+  const uint64_t dq_k = kKmajor | (smem_u32(sm.q[0]) >> 4);
+  const uint64_t ddo_k = kKmajor | (smem_u32(sm.dO[0]) >> 4);
+  const uint64_t dq_mn = kMnMajor | (smem_u32(sm.q[0]) >> 4);
+  const uint64_t ddo_mn = kMnMajor | (smem_u32(sm.dO[0]) >> 4);
+  constexpr uint64_t kStage = Cfg::kTile >> 4;   // q[1] - q[0] (and dO) in descriptor units
+  // D (128 x 128) = A (128 x DH) B^T, both K-major (DH contiguous)
+  auto mma_nt = [&](uint32_t d, uint64_t a, uint64_t b) {
+#pragma unroll
+    for (int kk = 0; kk < DH / 16; ++kk) {
+      const uint32_t off = ((kk / 4) * Cfg::kBox + (kk % 4) * 32) >> 4;
+      mma_bf16_ss_warp(d, a + off, b + off, idesc_ss, kk > 0 ? 1u : 0u);
+    }
+  };
+  // D (128 x DH) (+)= A (tensor memory, 128 x 128 bf16) B, B MN-major (DH contiguous)
+  auto mma_acc = [&](uint32_t d, uint32_t a, uint64_t b, bool first) {
+#pragma unroll
+    for (int kk = 0; kk < 128 / 16; ++kk)
+      mma_bf16_ts_warp(d, a + kk * 8, b + kk * (2048 >> 4), idesc_acc,
+                       (!first || kk > 0) ? 1u : 0u);
+  };
+  auto wait_all = [&](uint64_t* bar, uint32_t ph) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort));
+  };
+  uint32_t u = 0;
+  int items = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int w = bwd_item(it, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    const BwdKvItem I = bwd_kv_item_of(p, w);
+    const int N = p.group * (I.hi - I.lo + 1);
+    if (!(ok = wait_all(&sm.kv_full, (uint32_t)items & 1u))) break;
+    ++items;
+    if (!(ok = wait_all(&sm.q_full[u & 1u], (u >> 1) & 1u))) break;
+    tc_fence_after_sync();
+    mma_nt(Cfg::kColS, dk_, dq_k + (u & 1u) * kStage);
+    mma_commit_warp(&sm.s_full);
+    mma_nt(Cfg::kColDP, dv_, ddo_k + (u & 1u) * kStage);
+    mma_commit_warp(&sm.dp_full);
+    if (N == 1) mma_commit_warp(&sm.kv_empty);
+    for (int n = 0; n < N; ++n, ++u) {
+      const uint64_t st = u & 1u, st1 = (u + 1) & 1u;
+      if (!(ok = wait_all(&sm.p_full, u & 1u))) break;
+      tc_fence_after_sync();
+      mma_acc(Cfg::kColA0, Cfg::kColS, ddo_mn + st * kStage, n == 0);   // dV += P^T dO
+      if (n + 1 < N) {
+        if (!(ok = wait_all(&sm.q_full[st1], ((u + 1) >> 1) & 1u))) break;
+        tc_fence_after_sync();
+        mma_nt(Cfg::kColS, dk_, dq_k + st1 * kStage);                  // S^T(n+1) = K Q^T
+        mma_commit_warp(&sm.s_full);
+      }
+      if (!(ok = wait_all(&sm.ds_full, u & 1u))) break;
+      tc_fence_after_sync();
+      mma_acc(Cfg::kColA1, Cfg::kColDP, dq_mn + st * kStage, n == 0);   // dK += dS^T Q
+      mma_commit_warp(&sm.q_empty[st]);
+      if (n + 1 < N) {
+        mma_nt(Cfg::kColDP, dv_, ddo_k + st1 * kStage);                 // dP^T(n+1) = V dO^T
+        mma_commit_warp(&sm.dp_full);
+        if (n + 2 == N) mma_commit_warp(&sm.kv_empty);
+      }
+    }
+    if (ok) mma_commit_warp(&sm.acc_final);
+  }
+  mma_commit_warp(&sm.mma_done);
+  bwd_wait_drain(&sm.mma_done, 0);
+}
+
+// Store 32 fp32 accumulator columns (times `mul`) as bf16 to dst (16-byte aligned).
+__device__ __forceinline__ void bwd_store32(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = pack_bf16x2(__uint_as_float(r[8 * q + 2 * e]) * mul,
+                         __uint_as_float(r[8 * q + 2 * e + 1]) * mul);
+    d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Element-wise work of the dK/dV pass (warps 0-3; thread t owns key row
+// k0 + t, tensor-memory lane t).  Per step: P^T = exp2(S^T * scale*log2e -
+// lse2[query]) (0 where masked), written as bf16 over the first 64 columns of
+// S^T and kept packed in registers; then dS^T = P^T o (dP^T - D[query]), as
+// bf16 over the first 64 columns of dP^T.  Per item: dV and scale * dK out.
+template <int DH>
+__device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdParams& p,
+                                                 uint32_t tbase, volatile int* abort, int warp,
+                                                 int lane) {
+  using Cfg = BwdCfg<DH>;
+  const int t = warp * 32 + lane;
+  const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+  const float sl2 = p.scale_log2;
+  uint32_t u = 0;
+  int items = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int w = bwd_item(it, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    const BwdKvItem I = bwd_kv_item_of(p, w);
+    const int j = 128 * I.kb + t;   // this thread's key
+    for (int hh = 0; ok && hh < p.group; ++hh) {
+      for (int qb = I.lo; qb <= I.hi; ++qb, ++u) {
+        const int st = (int)(u & 1u);
+        // the stage's lse2 / D (bulk copies counted on q_full)
+        if (!(ok = mbar_wait(&sm.q_full[st], (u >> 1) & 1u, abort))) break;
+        if (!(ok = mbar_wait(&sm.s_full, u & 1u, abort))) break;
+        tc_fence_after_sync();
+        const float* L = sm.lse2[st];
+        const float* D = sm.dlt[st];
+        // visible query columns of key j: c in [clo, chi] (query i = 128 qb + c)
+        const bool msk = bwd_needs_mask(p, qb, I.kb);
+        int clo = 0, chi = 127;
+        if (p.causal) clo = j - 128 * qb;                          // i >= j
+        if (p.window > 0) chi = min(chi, j - 128 * qb + p.window - 1);   // i - j < W
+        chi = min(chi, p.S - 1 - 128 * qb);                        // i < S
+        const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
+        if (chi < clo) clo = 1 << 30;
+
+        uint32_t pk[64];   // P^T of this row, bf16 pairs
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t x[32];
+          tmem_ld_32x32b_x32(lane_addr + Cfg::kColS + 32 * c, x);
+          tmem_ld_wait(x);
+          uint32_t w16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = 32 * c + 2 * e;
+            float a = ex2_approx(fmaf(__uint_as_float(x[2 * e]), sl2, -L[col]));
+            float b = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), sl2, -L[col + 1]));
+            if (msk) {
+              a = zero_unless_le(a, (uint32_t)(col - clo), span);
+              b = zero_unless_le(b, (uint32_t)(col + 1 - clo), span);
+            }
+            w16[e] = pack_bf16x2(a, b);
+            pk[16 * c + e] = w16[e];
+          }
+          tmem_st_32x32b_x16(lane_addr + Cfg::kColS + 16 * c, w16);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&sm.p_full);
+
+        if (!(ok = mbar_wait(&sm.dp_full, u & 1u, abort))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t y[32];
+          tmem_ld_32x32b_x32(lane_addr + Cfg::kColDP + 32 * c, y);
+          tmem_ld_wait(y);
+          uint32_t w16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = 32 * c + 2 * e;
+            const float a = bf16_lo(pk[16 * c + e]) * (__uint_as_float(y[2 * e]) - D[col]);
+            const float b = bf16_hi(pk[16 * c + e]) * (__uint_as_float(y[2 * e + 1]) - D[col + 1]);
+            w16[e] = pack_bf16x2(a, b);
+          }
+          // (columns written here were all loaded by this or an earlier chunk)
+          tmem_st_32x32b_x16(lane_addr + Cfg::kColDP + 16 * c, w16);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&sm.ds_full);
+      }
+    }
+    if (!ok) break;
+
+    // ---- epilogue: dV and scale * dK of key j
+    if (!(ok = mbar_wait(&sm.acc_final, (uint32_t)items & 1u, abort))) break;
+    ++items;
+    tc_fence_after_sync();
+    const bool store = j < p.S;
+    const size_t row = ((size_t)I.bkv * p.S + j) * DH;
+#pragma unroll 1
+    for (int c = 0; c < DH / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(lane_addr + Cfg::kColA0 + 32 * c, r);
+      tmem_ld_wait(r);
+      if (store) bwd_store32(p.dv + row + 32 * c, r, 1.0f);
+      tmem_ld_32x32b_x32(lane_addr + Cfg::kColA1 + 32 * c, r);
+      tmem_ld_wait(r);
+      if (store) bwd_store32(p.dk + row + 32 * c, r, p.scale);
+    }
+    // the next item's first dV / dK overwrite the accumulators only after
+    // this thread's next arrive on p_full / ds_full, which follows these loads
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
+    attn_bwd_dkdv(const __grid_constant__ CUtensorMap map_q,
+                  const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v,
+                  const __grid_constant__ CUtensorMap map_do, const BwdParams p) {
+  using Cfg = BwdCfg<DH>;
+  using Smem = BwdKvSmem<DH>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  volatile int* abort = &sm.abort_flag;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (warp == Cfg::kWarpProducer && lane == 0) {
+    prefetch_tensormap(&map_q);
+    prefetch_tensormap(&map_k);
+    prefetch_tensormap(&map_v);
+    prefetch_tensormap(&map_do);
+  }
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    mbar_init(&sm.kv_full, 1);
+    mbar_init(&sm.kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.q_full[i], 1);
+      mbar_init(&sm.q_empty[i], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.ds_full, 128);
+    mbar_init(&sm.acc_final, 1);
+    mbar_init(&sm.mma_done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == Cfg::kWarpProducer) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = sm.tmem_base;
+  // compile-time tensor-memory columns: the allocation must start at column 0
+  if (tbase != 0 && threadIdx.x == 0) sm.abort_flag = 1;
+  if (tbase == 0) {
+    if (warp == Cfg::kWarpProducer) {
+      if (lane == 0) bwd_dkdv_producer<DH>(sm, p, &map_q, &map_k, &map_v, &map_do, abort);
+    } else if (warp == Cfg::kWarpIssuer) {
+      bwd_dkdv_issuer<DH>(sm, p, abort);
+    } else {
+      bwd_dkdv_softmax<DH>(sm, p, tbase, abort, warp, lane);
+    }
+  }
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == Cfg::kWarpProducer) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, 512);
+  }
+  if (threadIdx.x == 0 && sm.abort_flag) atomicExch(p.error_word, 4);   // ATTN_ERR_TIMEOUT
+}
+
+// ============================================================ dQ pass
+
+template <int DH>
+struct __align__(1024) BwdQSmem {
+  using Cfg = BwdCfg<DH>;
+  uint8_t q[Cfg::kTile];           // this item's query block (stays)
+  uint8_t dO[Cfg::kTile];          // and its output gradient
+  uint8_t k[2][Cfg::kTile];        // key blocks, two stages
+  uint8_t v[2][Cfg::kTile];        // value blocks
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full, s_free, dp_full, ds_full, acc_final, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Item w of the dQ pass: query block qb (heaviest, i.e. last, first under a
+// causal mask) of query head bh = b * Hq + h.
+struct BwdQItem {
+  int qb, bh, bkv, lo, hi;
+};
+
+__device__ __forceinline__ BwdQItem bwd_q_item_of(const BwdParams& p, int w) {
+  BwdQItem r;
+  const int per = p.B * p.Hq;
+  const int blk = w / per;
+  r.qb = p.nblk - 1 - blk;
+  r.bh = w - blk * per;
+  const int b = r.bh / p.Hq;
+  r.bkv = b * p.Hkv + (r.bh - b * p.Hq) / p.group;   // g(h) = floor(h / (H/G))
+  bwd_kblocks_of(p, r.qb, r.lo, r.hi);
+  return r;
+}
+
+template <int DH>
+__device__ __forceinline__ void bwd_dq_producer(BwdQSmem<DH>& sm, const BwdParams& p,
+                                                const CUtensorMap* map_q, const CUtensorMap* map_k,
+                                                const CUtensorMap* map_v,
+                                                const CUtensorMap* map_do, volatile int* abort) {
+  using Cfg = BwdCfg<DH>;
+  constexpr int kBoxes = DH / 64;
+  const uint64_t keep = policy_evict_last();   // key blocks are re-read by other query blocks
+  uint32_t u = 0, loaded = 0, par = 0;
+  int items = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int w = bwd_item(it, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    const BwdQItem I = bwd_q_item_of(p, w);
+    if (items > 0 && !(ok = mbar_wait(&sm.q_empty, (uint32_t)(items - 1) & 1u, abort))) break;
+    mbar_arrive_expect_tx(&sm.q_full, 2 * Cfg::kTile);
+    for (int hf = 0; hf < kBoxes; ++hf) {
+      tma_load_3d(sm.q + hf * Cfg::kBox, map_q, &sm.q_full, 64 * hf, 128 * I.qb, I.bh);
+      tma_load_3d(sm.dO + hf * Cfg::kBox, map_do, &sm.q_full, 64 * hf, 128 * I.qb, I.bh);
+    }
+    ++items;
+    for (int kb = I.lo; kb <= I.hi; ++kb, ++u) {
+      const int st = (int)(u & 1u);
+      const uint32_t ph = (u >> 1) & 1u;
+      if (!(ok = mbar_wait(&sm.kv_empty[st], ph ^ 1u, abort))) break;
+      mbar_arrive_expect_tx(&sm.kv_full[st], 2 * Cfg::kTile);
+      for (int hf = 0; hf < kBoxes; ++hf) {
+        tma_load_3d_hint(sm.k[st] + hf * Cfg::kBox, map_k, &sm.kv_full[st], 64 * hf, 128 * kb,
+                         I.bkv, keep);
+        tma_load_3d_hint(sm.v[st] + hf * Cfg::kBox, map_v, &sm.kv_full[st], 64 * hf, 128 * kb,
+                         I.bkv, keep);
+      }
+      loaded |= 1u << st;
+      par = (par & ~(1u << st)) | (ph << st);
+    }
+  }
+  if (items > 0) bwd_wait_drain(&sm.q_full, (uint32_t)(items - 1) & 1u);
+  for (int i = 0; i < 2; ++i)
+    if (loaded & (1u << i)) bwd_wait_drain(&sm.kv_full[i], (par >> i) & 1u);
+}
+
+// MMA issue order per item of N key blocks: S(0), dP(0), then per block n:
+// S(n+1) once the element-wise warps have read S(n), dQ(n) once dS(n) is
+// written, dP(n+1) (its columns held dS(n), which dQ(n), issued before it,
+// reads).
+template <int DH>
+__device__ __forceinline__ void bwd_dq_issuer(BwdQSmem<DH>& sm, const BwdParams& p,
+                                              volatile int* abort) {
+  using Cfg = BwdCfg<DH>;
+  constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t idesc_acc = idesc_bf16_f32(128, DH, false, true);
+  constexpr uint64_t kKmajor = smem_desc_sw128(0, 16, 1024);
+  constexpr uint64_t kMnMajor = smem_desc_sw128(0, Cfg::kBox, 1024);
+  const uint64_t dq_ = kKmajor | (smem_u32(sm.q) >> 4);
+  const uint64_t ddo_ = kKmajor | (smem_u32(sm.dO) >> 4);
+  const uint64_t dk_k = kKmajor | (smem_u32(sm.k[0]) >> 4);
+  const uint64_t dv_k = kKmajor | (smem_u32(sm.v[0]) >> 4);
+  const uint64_t dk_mn = kMnMajor | (smem_u32(sm.k[0]) >> 4);
+  constexpr uint64_t kStage = Cfg::kTile >> 4;
+  auto mma_nt = [&](uint32_t d, uint64_t a, uint64_t b) {
+#pragma unroll
+    for (int kk = 0; kk < DH / 16; ++kk) {
+      const uint32_t off = ((kk / 4) * Cfg::kBox + (kk % 4) * 32) >> 4;
+      mma_bf16_ss_warp(d, a + off, b + off, idesc_ss, kk > 0 ? 1u : 0u);
+    }
+  };
+  auto wait_all = [&](uint64_t* bar, uint32_t ph) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort));
+  };
+  uint32_t u = 0;
+  int items = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int w = bwd_item(it, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    const BwdQItem I = bwd_q_item_of(p, w);
+    const int N = I.hi - I.lo + 1;
+    if (!(ok = wait_all(&sm.q_full, (uint32_t)items & 1u))) break;
+    ++items;
+    if (!(ok = wait_all(&sm.kv_full[u & 1u], (u >> 1) & 1u))) break;
+    tc_fence_after_sync();
+    mma_nt(Cfg::kColS, dq_, dk_k + (u & 1u) * kStage);
+    mma_commit_warp(&sm.s_full);
+    mma_nt(Cfg::kColDP, ddo_, dv_k + (u & 1u) * kStage);
+    mma_commit_warp(&sm.dp_full);
+    if (N == 1) mma_commit_warp(&sm.q_empty);
+    for (int n = 0; n < N; ++n, ++u) {
+      const uint64_t st = u & 1u, st1 = (u + 1) & 1u;
+      if (n + 1 < N) {
+        if (!(ok = wait_all(&sm.s_free, u & 1u))) break;
+        if (!(ok = wait_all(&sm.kv_full[st1], ((u + 1) >> 1) & 1u))) break;
+        tc_fence_after_sync();
+        mma_nt(Cfg::kColS, dq_, dk_k + st1 * kStage);                    // S(n+1) = Q K^T
+        mma_commit_warp(&sm.s_full);
+      }
+      if (!(ok = wait_all(&sm.ds_full, u & 1u))) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < 128 / 16; ++kk)                              // dQ += dS K
+        mma_bf16_ts_warp(Cfg::kColA0, Cfg::kColDP + kk * 8, dk_mn + st * kStage + kk * (2048 >> 4),
+                         idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_warp(&sm.kv_empty[st]);
+      if (n + 1 < N) {
+        mma_nt(Cfg::kColDP, ddo_, dv_k + st1 * kStage);                  // dP(n+1) = dO V^T
+        mma_commit_warp(&sm.dp_full);
+        if (n + 2 == N) mma_commit_warp(&sm.q_empty);
+      }
+    }
+    if (ok) mma_commit_warp(&sm.acc_final);
+  }
+  mma_commit_warp(&sm.mma_done);
+  bwd_wait_drain(&sm.mma_done, 0);
+}
+
+// Element-wise work of the dQ pass (thread t owns query row 128 qb + t):
+// P = exp2(S * scale*log2e - lse2_i) (0 where masked), kept packed in
+// registers; dS = P o (dP - D_i) as bf16 over the first 64 columns of dP.
+// Per item: scale * dQ out.
+template <int DH>
+__device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams& p,
+                                               uint32_t tbase, volatile int* abort, int warp,
+                                               int lane) {
+  using Cfg = BwdCfg<DH>;
+  const int t = warp * 32 + lane;
+  const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+  const float sl2 = p.scale_log2;
+  uint32_t u = 0;
+  int items = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int w = bwd_item(it, blockIdx.x, gridDim.x);
+    if (w >= p.num_items) break;
+    const BwdQItem I = bwd_q_item_of(p, w);
+    const int i = 128 * I.qb + t;   // this thread's query
+    const float L = p.lse2[(size_t)I.bh * p.S_pad + i];
+    const float Di = p.delta[(size_t)I.bh * p.S_pad + i];
+    for (int kb = I.lo; kb <= I.hi; ++kb, ++u) {
+      if (!(ok = mbar_wait(&sm.s_full, u & 1u, abort))) break;
+      tc_fence_after_sync();
+      // visible keys of query i: [klo, khi], as columns [clo, chi] of block kb
+      const bool msk = bwd_needs_mask(p, I.qb, kb);
+      int khi = p.S - 1;
+      if (p.causal) khi = min(khi, i);
+      const int klo = p.window > 0 ? i - p.window + 1 : 0;
+      int clo = klo - 128 * kb;
+      const int chi = khi - 128 * kb;
+      const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
+      if (chi < clo) clo = 1 << 30;
+
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t x[32];
+        tmem_ld_32x32b_x32(lane_addr + Cfg::kColS + 32 * c, x);
+        tmem_ld_wait(x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = 32 * c + 2 * e;
+          float a = ex2_approx(fmaf(__uint_as_float(x[2 * e]), sl2, -L));
+          float b = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), sl2, -L));
+          if (msk) {
+            a = zero_unless_le(a, (uint32_t)(col - clo), span);
+            b = zero_unless_le(b, (uint32_t)(col + 1 - clo), span);
+          }
+          pk[16 * c + e] = pack_bf16x2(a, b);
+        }
+      }
+      // S is in registers: the next S may overwrite it
+      tc_fence_before_sync();
+      mbar_arrive(&sm.s_free);
+
+      if (!(ok = mbar_wait(&sm.dp_full, u & 1u, abort))) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t y[32];
+        tmem_ld_32x32b_x32(lane_addr + Cfg::kColDP + 32 * c, y);
+        tmem_ld_wait(y);
+        uint32_t w16[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float a = bf16_lo(pk[16 * c + e]) * (__uint_as_float(y[2 * e]) - Di);
+          const float b = bf16_hi(pk[16 * c + e]) * (__uint_as_float(y[2 * e + 1]) - Di);
+          w16[e] = pack_bf16x2(a, b);
+        }
+        tmem_st_32x32b_x16(lane_addr + Cfg::kColDP + 16 * c, w16);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&sm.ds_full);
+    }
+    if (!ok) break;
+
+    // ---- epilogue: scale * dQ of query i
+    if (!(ok = mbar_wait(&sm.acc_final, (uint32_t)items & 1u, abort))) break;
+    ++items;
+    tc_fence_after_sync();
+    const bool store = i < p.S;
+    const size_t row = ((size_t)I.bh * p.S + i) * DH;
+#pragma unroll 1
+    for (int c = 0; c < DH / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(lane_addr + Cfg::kColA0 + 32 * c, r);
+      tmem_ld_wait(r);
+      if (store) bwd_store32(p.dq + row + 32 * c, r, p.scale);
+    }
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
+    attn_bwd_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                const __grid_constant__ CUtensorMap map_v,
+                const __grid_constant__ CUtensorMap map_do, const BwdParams p) {
+  using Cfg = BwdCfg<DH>;
+  using Smem = BwdQSmem<DH>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  volatile int* abort = &sm.abort_flag;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (warp == Cfg::kWarpProducer && lane == 0) {
+    prefetch_tensormap(&map_q);
+    prefetch_tensormap(&map_k);
+    prefetch_tensormap(&map_v);
+    prefetch_tensormap(&map_do);
+  }
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.kv_full[i], 1);
+      mbar_init(&sm.kv_empty[i], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_free, 128);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.ds_full, 128);
+    mbar_init(&sm.acc_final, 1);
+    mbar_init(&sm.mma_done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == Cfg::kWarpProducer) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = sm.tmem_base;
+  if (tbase != 0 && threadIdx.x == 0) sm.abort_flag = 1;
+  if (tbase == 0) {
+    if (warp == Cfg::kWarpProducer) {
+      if (lane == 0) bwd_dq_producer<DH>(sm, p, &map_q, &map_k, &map_v, &map_do, abort);
+    } else if (warp == Cfg::kWarpIssuer) {
+      bwd_dq_issuer<DH>(sm, p, abort);
+    } else {
+      bwd_dq_softmax<DH>(sm, p, tbase, abort, warp, lane);
+    }
+  }
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == Cfg::kWarpProducer) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, 512);
+  }
+  if (threadIdx.x == 0 && sm.abort_flag) atomicExch(p.error_word, 4);   // ATTN_ERR_TIMEOUT
+}
+
+template <int DH>
+constexpr size_t bwd_dkdv_smem_bytes() { return sizeof(BwdKvSmem<DH>) + 1024; }
+template <int DH>
+constexpr size_t bwd_dq_smem_bytes() { return sizeof(BwdQSmem<DH>) + 1024; }
+
+}  // namespace chs

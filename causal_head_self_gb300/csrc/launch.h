@@ -40,9 +40,10 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int Dh, int rows, long 
 // Queries: Sq rows per (b, h), at positions start_pos .. start_pos + Sq - 1.
 // K, V: Tkv rows per (b, K/V head) in memory, of which the first
 // start_pos + Sq are visible (a plain prefill: Tkv = Sq, start_pos = 0).
-cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
-                           int Hkv, int Sq, int Tkv, int start_pos, int Dh, int causal,
-                           int window, float scale_log2, const DeviceInfo& dev,
+// lse (optional, [B, Hq, Sq] fp32) receives each row's log-sum-exp.
+cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int Hq, int Hkv, int Sq, int Tkv, int start_pos, int Dh,
+                           int causal, int window, float scale_log2, const DeviceInfo& dev,
                            cudaStream_t stream);
 
 struct DecodePlan {
@@ -77,5 +78,14 @@ cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, cons
                              void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,
                              float scale_log2, const DecodePlan& plan, void* partials,
                              const DeviceInfo& dev, cudaStream_t stream);
+
+// Backward pass (Dh 64 or 128): dq [B, Hq, S, Dh], dk and dv [B, Hkv, S, Dh]
+// from q, k, v, the forward output o, its log-sum-exps lse [B, Hq, S] and
+// dout; workspace holds bwd_workspace_bytes(B, Hq, S) bytes (16-byte aligned).
+size_t bwd_workspace_bytes(int B, int Hq, int S);
+cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       float* workspace, int B, int Hq, int Hkv, int S, int Dh, int causal,
+                       int window, float scale, const DeviceInfo& dev, cudaStream_t stream);
 
 }  // namespace chs

@@ -37,6 +37,7 @@ struct Prefill256Params {
   int group;            // Hq / Hkv
   __nv_bfloat16* o;     // [B, Hq, Sq, 256]
   int o_wide;           // o is 32-byte aligned: 32-byte stores
+  float* lse;           // optional [B, Hq, Sq]: log sum_j exp(s_ij) per row (natural log)
   int* error_word;
   int fault;            // test hook: 1 = the first K tile is never loaded
 };
@@ -365,6 +366,9 @@ __device__ __forceinline__ void prefill256_softmax(Prefill256Smem& sm, const Pre
     const int orow = tile.q0 + t;   // output row within the chunk
     uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)tile.bh * p.Sq + orow) * Cfg::DH);
     const bool store = orow < p.Sq;
+    // sum_j exp(s_ij) = 2^m_run * l_run (m_run in units of log2)
+    if (p.lse != nullptr && store)
+      p.lse[(size_t)tile.bh * p.Sq + orow] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
 #pragma unroll 1
     for (int c = 0; c < Cfg::DH / 32; c += 2) {
       uint32_t o0[32], o1[32];

@@ -45,10 +45,10 @@ static FastDiv make_fast_div(uint32_t d) {
 }
 
 // Head size 256: one 128-row sub-tile per work item, 64-key tiles.
-static cudaError_t launch_prefill256(const void* q, const void* k, const void* v, void* o, int B,
-                                     int Hq, int Hkv, int Sq, int Tkv, int start_pos, int causal,
-                                     int window, float scale_log2, const DeviceInfo& dev,
-                                     cudaStream_t stream) {
+static cudaError_t launch_prefill256(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, int B, int Hq, int Hkv, int Sq, int Tkv,
+                                     int start_pos, int causal, int window, float scale_log2,
+                                     const DeviceInfo& dev, cudaStream_t stream) {
   using Cfg = Prefill256Cfg;
   const int Skv = start_pos + Sq;
   CUtensorMap mq, mk, mv;
@@ -74,6 +74,7 @@ static cudaError_t launch_prefill256(const void* q, const void* k, const void* v
   prm.num_items = (int)items;
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.o_wide = (reinterpret_cast<uintptr_t>(o) & 31) == 0;
+  prm.lse = lse;
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
   constexpr size_t smem = prefill256_smem_bytes();
@@ -89,12 +90,12 @@ static cudaError_t launch_prefill256(const void* q, const void* k, const void* v
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
-                           int Hkv, int Sq, int Tkv, int start_pos, int Dh, int causal,
-                           int window, float scale_log2, const DeviceInfo& dev,
+cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int Hq, int Hkv, int Sq, int Tkv, int start_pos, int Dh,
+                           int causal, int window, float scale_log2, const DeviceInfo& dev,
                            cudaStream_t stream) {
   if (Dh == 256)
-    return launch_prefill256(q, k, v, o, B, Hq, Hkv, Sq, Tkv, start_pos, causal, window,
+    return launch_prefill256(q, k, v, o, lse, B, Hq, Hkv, Sq, Tkv, start_pos, causal, window,
                              scale_log2, dev, stream);
   // K and V hold Tkv rows per head in memory; the chunk sees the first
   // start_pos + Sq of them, and the maps cover only those (the last key
@@ -121,6 +122,7 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o,
   prm.num_items = (int)items;
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.o_wide = (reinterpret_cast<uintptr_t>(o) & 31) == 0;
+  prm.lse = lse;
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
   prm.div_bh = make_fast_div((uint32_t)(B * Hq));

@@ -65,6 +65,7 @@ struct PrefillParams {
   int num_items;      // work items: num_qblocks * B * Hq
   __nv_bfloat16* o;   // output [B, Hq, Sq, DH]
   int o_wide;         // o is 32-byte aligned: 32-byte stores
+  float* lse;         // optional [B, Hq, Sq]: log sum_j exp(s_ij) per row (natural log)
   int* error_word;    // set to a nonzero status when a wait gives up
   int fault;          // test hook: 1 = the first K tile is never loaded
   FastDiv div_bh;     // by B * Hq (work items per query block)
@@ -569,6 +570,9 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
     const int orow = tile.row_first(s) + t;  // output row within the chunk
     uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.Sq + orow) * DH);
     const bool store = orow < p.Sq;
+    // sum_j exp(s_ij) = 2^m_run * l_run (m_run in units of log2)
+    if (p.lse != nullptr && store)
+      p.lse[(size_t)bh * p.Sq + orow] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
 #pragma unroll
     for (int c = 0; c < DH / 32; c += 2) {
       uint32_t o0[32], o1[32];

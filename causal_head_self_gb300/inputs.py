@@ -33,6 +33,11 @@ WORKLOADS = {
                                              causal=True, window=0, seed=6),
     "prefill_gqa_b1_h16kv8_s8192_d256_w4096": dict(kind="prefill", B=1, Hq=16, Hkv=8, S=8192,
                                                    Dh=256, causal=True, window=4096, seed=6),
+    # the backward pass of causal MHA at 4096 tokens (and of the GQA prefill)
+    "backward_mha_b1_h32_s4096_d128": dict(kind="backward", B=1, Hq=32, Hkv=32, S=4096, Dh=128,
+                                           causal=True, window=0, seed=2),
+    "backward_gqa_b2_h32kv8_s2048_d128": dict(kind="backward", B=2, Hq=32, Hkv=8, S=2048,
+                                              Dh=128, causal=True, window=0, seed=7),
     # one decode step for 16 sequences against caches of 16384..32768 keys
     "decode_gqa_b16_h32kv8_t32768_d128": dict(kind="decode", B=16, Hq=32, Hkv=8, Tmax=32768,
                                               Dh=128, lmin=16384, lmax=32768, window=0, seed=4),
@@ -55,6 +60,13 @@ def prefill_inputs(B, Hq, Hkv, S, Dh, seed):
     return q, k, v
 
 
+def grad_inputs(shape, seed):
+    """An upstream gradient dL/do of the given shape: i.i.d. N(0, 1), bf16 on
+    the host (its own generator, so adding it changes no other draw)."""
+    gen = torch.Generator(device="cpu").manual_seed(int(seed) + 7919)
+    return _randn_bf16(tuple(shape), gen)
+
+
 def decode_inputs(B, Hq, Hkv, Tmax, Dh, lmin, lmax, seed):
     """q [B,Hq,1,Dh], kcache and vcache [B,Hkv,Tmax,Dh] (bf16), and the
     per-sequence key counts seqlens [B] (int32, uniform in [lmin, lmax])."""
@@ -71,5 +83,8 @@ def workload_inputs(name):
     w = WORKLOADS[name]
     if w["kind"] == "prefill":
         return prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["S"], w["Dh"], w["seed"])
+    if w["kind"] == "backward":
+        q, k, v = prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["S"], w["Dh"], w["seed"])
+        return q, k, v, grad_inputs(q.shape, w["seed"])
     return decode_inputs(w["B"], w["Hq"], w["Hkv"], w["Tmax"], w["Dh"], w["lmin"], w["lmax"],
                          w["seed"])

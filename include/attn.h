@@ -20,7 +20,7 @@
  *     heads moved ahead of the sequence axis).  All tensor pointers are
  *     DEVICE pointers, 16-byte aligned.  The caller owns every tensor.
  *   - Dh must be 64, 128 or 256 (the Gemma head size) for every entry
- *     point (ATTN_ERR_UNSUPPORTED otherwise).
+ *     point but attn_bwd (64 or 128) (ATTN_ERR_UNSUPPORTED otherwise).
  *   - Hq % Hkv == 0 is required (ATTN_ERR_INVALID_ARG otherwise).
  *   - scale == 0 selects 1/sqrt(Dh), the textbook's choice (divide by the
  *     square root of the HEAD size, not the model width); a positive scale is
@@ -53,7 +53,7 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2,  /* a head size the entry point does not take */
   ATTN_ERR_CUDA = 3,         /* a CUDA runtime or launch error */
   ATTN_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (reported by attn_status) */
-  ATTN_ERR_NO_MEMORY = 5,    /* the decode workspace could not be allocated */
+  ATTN_ERR_NO_MEMORY = 5,    /* a library workspace could not be allocated */
   ATTN_ERR_SCRATCH_LIMIT = 6 /* attn_decode_noalloc: the call needs more than its fixed scratch */
 } attn_status_t;
 
@@ -72,6 +72,52 @@ typedef enum {
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
              int S, int Dh, int causal, int window, float scale, cudaStream_t stream);
+
+/*
+ * attn_fwd_lse -- attn_fwd that also writes each query row's log-sum-exp,
+ *   lse  [B, Hq, S]  (device, fp32, written; 4-byte aligned, must not
+ *                     overlap the other tensors)
+ *   lse[b, h, i] = log sum_j exp(s_ij) over the visible keys j, natural log,
+ *   with s_ij = scale * q_i . k_j the scaled score (the softmax
+ *   normaliser of "Механизм внимания", section "Scaled dot-product
+ *   attention", in log form).  attn_bwd recomputes the weights from it.
+ * o is bit-identical to attn_fwd's.  lse == NULL is ATTN_ERR_INVALID_ARG
+ * (unless B == 0 or S == 0, a no-op).
+ */
+int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int S, int Dh, int causal, int window, float scale,
+                 cudaStream_t stream);
+
+/*
+ * attn_bwd -- backward pass of attn_fwd: the gradients of a loss L with
+ * respect to q, k and v, given dout = dL/do.  The chain rule through the
+ * definition, with the softmax derivative dp_i/dz_j = p_i (delta_ij - p_j)
+ * of "Механизм внимания", section "Почему делить на корень из d_h"; the
+ * weights are recomputed block by block from lse (section "Эффективные
+ * реализации": FlashAttention recomputes them in the backward pass):
+ *     dV = P^T dO,  dS = P o (dO V^T - D),  D_i = dO_i . o_i,
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ *   q, k, v, causal, window, scale  exactly as passed to attn_fwd_lse
+ *   o     [B, Hq,  S, Dh]  attn_fwd_lse's output       (device, bf16, read)
+ *   dout  [B, Hq,  S, Dh]  dL/do                       (device, bf16, read)
+ *   lse   [B, Hq,  S]      attn_fwd_lse's lse          (device, fp32, read)
+ *   dq    [B, Hq,  S, Dh]  dL/dq                       (device, bf16, written)
+ *   dk    [B, Hkv, S, Dh]  dL/dk, summed over the query heads of each group
+ *   dv    [B, Hkv, S, Dh]  dL/dv, likewise             (device, bf16, written)
+ * dq, dk and dv must not overlap each other or any input.  Dh must be 64 or
+ * 128 (ATTN_ERR_UNSUPPORTED otherwise).  The result is deterministic (no
+ * atomics): one pass computes dK and dV per key block, a second dQ per query
+ * block.  Per-row intermediates live in a library-owned device workspace
+ * (8 bytes per query row, allocated on first use and grown on demand,
+ * ATTN_ERR_NO_MEMORY if that fails); backward calls that overlap on the GPU
+ * race on it.  B == 0 or S == 0 is a no-op.
+ * Work: 10*Dh FLOPs per visible (query, key) pair per query head (S
+ * recomputed, dP, dV, dQ, dK: 2*Dh each), 2.5 x attn_fwd's; the kernels
+ * execute 14*Dh (S and dP are computed in both passes).
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dh,
+             int causal, int window, float scale, cudaStream_t stream);
 
 /*
  * attn_fwd_chunk -- prefill of one chunk against a KV cache ("Механизм
