@@ -22,7 +22,8 @@ static cudaError_t launch_bwd_dh(const CUtensorMap& mq, const CUtensorMap& mk,
   });
   if (e != cudaSuccess) return e;
   const long long rows = (long long)prm.B * prm.Hq * prm.S_pad;
-  attn_bwd_prep<DH><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+  constexpr int rpb = bwd_prep_rows_per_block<DH>();
+  attn_bwd_prep<DH><<<(unsigned)((rows + rpb - 1) / rpb), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2,
       delta, rows, prm.S, prm.S_pad);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -67,7 +68,7 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   prm.S_pad = prm.nblk * 128;
   prm.group = Hq / Hkv;
   if ((long long)prm.nblk * B * Hq > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (((long long)B * Hq * prm.S_pad + 7) / 8 > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (((long long)B * Hq * prm.S_pad + 15) / 16 > 0x7fffffffLL) return cudaErrorInvalidValue;
   float* lse2 = workspace;
   float* delta = workspace + (size_t)B * Hq * prm.S_pad;
   prm.lse2 = lse2;

@@ -29,10 +29,11 @@
 // reduced across key blocks with atomics: 7 MMAs per block pair instead of 5,
 // in exchange for a deterministic result.
 //
-// Roles as in the forward kernels: warps 0-3 (thread t owns tensor-memory
-// lane t) run the element-wise work and the epilogue, warp 4 lane 0 issues
-// every TMA copy, warp 5 issues every MMA (one elected lane).  Every wait is
-// bounded.
+// Roles: warps 0-7 run the element-wise work and the epilogues, two
+// warpgroups on the two column halves of the same 128 rows (thread t of
+// either owns tensor-memory lane t), so each does half of every step's
+// exponentials and the two halves run side by side; warp 8 lane 0 issues
+// every TMA copy, warp 9 every MMA (one elected lane).  Every wait is bounded.
 #pragma once
 
 #include <cstdint>
@@ -64,54 +65,56 @@ template <int DH>
 struct BwdCfg {
   static constexpr int kBox = 128 * 64 * 2;         // one 128-row x 64-column box
   static constexpr int kTile = (DH / 64) * kBox;    // a 128 x DH tile
-  static constexpr int kThreads = 192;
-  static constexpr int kWarpProducer = 4, kWarpIssuer = 5;
+  // warps 0-7: element-wise work (warp w: tensor-memory lanes 32 (w % 4) ..,
+  // columns 64 (w / 4) .. + 63 of S and dP); warp 8: TMA; warp 9: MMA
+  static constexpr int kThreads = 320;
+  static constexpr int kWarpProducer = 8, kWarpIssuer = 9;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColA0 = 256, kColA1 = 384;
 };
 
+// Where the bf16 pairs of columns 16 kk .. 16 kk + 15 of a 128-column S or dP
+// buffer are written (P over S, dS over dP): each column half's pairs go to
+// the first 32 columns of that half, so that one warpgroup's stores never
+// land on columns the other warpgroup has still to load.
+__host__ __device__ constexpr uint32_t bwd_packed_col(int kk) {
+  return 8u * (uint32_t)kk + (kk >= 4 ? 32u : 0u);
+}
+
 // D_i = sum_d dO[i, d] o[i, d] (fp32 products of the bf16 values) and
-// lse2_i = lse_i * log2(e), one warp per row of [B * Hq, S_pad]; rows past S
-// get D = 0 and lse2 = +inf (their weights exp2(x - lse2) are then 0).
+// lse2_i = lse_i * log2(e) for every row of [B * Hq, S_pad]; rows past S get
+// D = 0 and lse2 = +inf (their weights exp2(x - lse2) are then 0).  DH / 8
+// lanes per row, 16 bytes of o and of dO each.
+template <int DH>
+constexpr int bwd_prep_rows_per_block() { return 256 / (DH / 8); }
+
 template <int DH>
 __global__ void __launch_bounds__(256)
     attn_bwd_prep(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                   const float* __restrict__ lse, float* __restrict__ lse2,
                   float* __restrict__ delta, long long rows, int S, int S_pad) {
-  const long long r = (long long)blockIdx.x * 8 + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  if (r >= rows) return;
+  constexpr int kLanes = DH / 8;   // 16 or 8 lanes per row
+  const long long r = (long long)blockIdx.x * bwd_prep_rows_per_block<DH>() + threadIdx.x / kLanes;
+  const int sub = threadIdx.x % kLanes;
   const long long bh = r / S_pad;
   const int i = (int)(r - bh * S_pad);
-  if (i >= S) {
-    if (lane == 0) {
-      delta[r] = 0.f;
-      lse2[r] = __int_as_float(0x7f800000);
-    }
-    return;
-  }
-  const size_t base = ((size_t)bh * S + i) * DH;
+  const bool valid = r < rows && i < S;
   float acc = 0.f;
-  constexpr int kPer = DH / 32;   // 4 or 2 bf16 per lane
-  if constexpr (kPer == 4) {
-    const uint2 a = *reinterpret_cast<const uint2*>(o + base + 4 * lane);
-    const uint2 b = *reinterpret_cast<const uint2*>(dout + base + 4 * lane);
-    const uint32_t wa[2] = {a.x, a.y}, wb[2] = {b.x, b.y};
+  if (valid) {
+    const size_t base = ((size_t)bh * S + i) * DH + 8 * sub;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + base);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + base);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
+    for (int e = 0; e < 4; ++e) {
       acc = fmaf(__uint_as_float(wa[e] << 16), __uint_as_float(wb[e] << 16), acc);
       acc = fmaf(__uint_as_float(wa[e] & 0xffff0000u), __uint_as_float(wb[e] & 0xffff0000u), acc);
     }
-  } else {
-    const uint32_t wa = *reinterpret_cast<const uint32_t*>(o + base + 2 * lane);
-    const uint32_t wb = *reinterpret_cast<const uint32_t*>(dout + base + 2 * lane);
-    acc = fmaf(__uint_as_float(wa << 16), __uint_as_float(wb << 16), acc);
-    acc = fmaf(__uint_as_float(wa & 0xffff0000u), __uint_as_float(wb & 0xffff0000u), acc);
   }
 #pragma unroll
-  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (lane == 0) {
-    delta[r] = acc;
-    lse2[r] = lse[(size_t)bh * S + i] * 1.4426950408889634f;
+  for (int m = kLanes / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (sub == 0 && r < rows) {
+    delta[r] = valid ? acc : 0.f;
+    lse2[r] = valid ? lse[(size_t)bh * S + i] * 1.4426950408889634f : __int_as_float(0x7f800000);
   }
 }
 
@@ -285,11 +288,12 @@ __device__ __forceinline__ void bwd_dkdv_issuer(BwdKvSmem<DH>& sm, const BwdPara
       mma_bf16_ss_warp(d, a + off, b + off, idesc_ss, kk > 0 ? 1u : 0u);
     }
   };
-  // D (128 x DH) (+)= A (tensor memory, 128 x 128 bf16) B, B MN-major (DH contiguous)
+  // D (128 x DH) (+)= A (tensor memory, 128 x 128 bf16 pairs at bwd_packed_col) B,
+  // B MN-major (DH contiguous)
   auto mma_acc = [&](uint32_t d, uint32_t a, uint64_t b, bool first) {
 #pragma unroll
     for (int kk = 0; kk < 128 / 16; ++kk)
-      mma_bf16_ts_warp(d, a + kk * 8, b + kk * (2048 >> 4), idesc_acc,
+      mma_bf16_ts_warp(d, a + bwd_packed_col(kk), b + kk * (2048 >> 4), idesc_acc,
                        (!first || kk > 0) ? 1u : 0u);
   };
   auto wait_all = [&](uint64_t* bar, uint32_t ph) -> bool {
@@ -353,18 +357,22 @@ __device__ __forceinline__ void bwd_store32(__nv_bfloat16* dst, const uint32_t (
   }
 }
 
-// Element-wise work of the dK/dV pass (warps 0-3; thread t owns key row
-// k0 + t, tensor-memory lane t).  Per step: P^T = exp2(S^T * scale*log2e -
-// lse2[query]) (0 where masked), written as bf16 over the first 64 columns of
-// S^T and kept packed in registers; then dS^T = P^T o (dP^T - D[query]), as
-// bf16 over the first 64 columns of dP^T.  Per item: dV and scale * dK out.
+// Element-wise work of the dK/dV pass (warps 0-7; thread t of warpgroup wg
+// owns key row k0 + t, tensor-memory lane t, and query columns
+// 64 wg .. 64 wg + 63).  Per step: P^T = exp2(S^T * scale*log2e - lse2[query])
+// (0 where masked), written as bf16 pairs (see bwd_packed_col) and kept in
+// registers; then dS^T = P^T o (dP^T - D[query]), as bf16 pairs over dP^T.
+// Per item: warpgroup 0 writes dV, warpgroup 1 scale * dK.
 template <int DH>
 __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdParams& p,
                                                  uint32_t tbase, volatile int* abort, int warp,
                                                  int lane) {
   using Cfg = BwdCfg<DH>;
-  const int t = warp * 32 + lane;
-  const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+  const int wg = warp / 4;
+  const int t = (warp % 4) * 32 + lane;
+  const uint32_t lane_addr = tbase + ((uint32_t)((warp % 4) * 32) << 16);
+  const uint32_t colS = lane_addr + Cfg::kColS + 64 * wg;      // this half's scores
+  const uint32_t colDP = lane_addr + Cfg::kColDP + 64 * wg;
   const float sl2 = p.scale_log2;
   uint32_t u = 0;
   int items = 0;
@@ -381,37 +389,44 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
         if (!(ok = mbar_wait(&sm.q_full[st], (u >> 1) & 1u, abort))) break;
         if (!(ok = mbar_wait(&sm.s_full, u & 1u, abort))) break;
         tc_fence_after_sync();
-        const float* L = sm.lse2[st];
-        const float* D = sm.dlt[st];
-        // visible query columns of key j: c in [clo, chi] (query i = 128 qb + c)
+        const float4* L4 = reinterpret_cast<const float4*>(sm.lse2[st] + 64 * wg);
+        const float4* D4 = reinterpret_cast<const float4*>(sm.dlt[st] + 64 * wg);
+        // visible query columns of key j: c in [clo, chi] of this half (query
+        // i = 128 qb + 64 wg + c)
         const bool msk = bwd_needs_mask(p, qb, I.kb);
-        int clo = 0, chi = 127;
-        if (p.causal) clo = j - 128 * qb;                          // i >= j
-        if (p.window > 0) chi = min(chi, j - 128 * qb + p.window - 1);   // i - j < W
-        chi = min(chi, p.S - 1 - 128 * qb);                        // i < S
+        const int i0 = 128 * qb + 64 * wg;
+        int clo = 0, chi = 63;
+        if (p.causal) clo = j - i0;                                     // i >= j
+        if (p.window > 0) chi = min(chi, j - i0 + p.window - 1);        // i - j < W
+        chi = min(chi, p.S - 1 - i0);                                   // i < S
         const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
         if (chi < clo) clo = 1 << 30;
 
-        uint32_t pk[64];   // P^T of this row, bf16 pairs
+        uint32_t pk[32];   // P^T of this row's half, bf16 pairs
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t x[32];
-          tmem_ld_32x32b_x32(lane_addr + Cfg::kColS + 32 * c, x);
+          tmem_ld_32x32b_x32(colS + 32 * c, x);
           tmem_ld_wait(x);
           uint32_t w16[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int col = 32 * c + 2 * e;
-            float a = ex2_approx(fmaf(__uint_as_float(x[2 * e]), sl2, -L[col]));
-            float b = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), sl2, -L[col + 1]));
-            if (msk) {
-              a = zero_unless_le(a, (uint32_t)(col - clo), span);
-              b = zero_unless_le(b, (uint32_t)(col + 1 - clo), span);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 l = L4[8 * c + e4];
+            const float ls[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 2 * e4 + h, col = 32 * c + 2 * e;
+              float a = ex2_approx(fmaf(__uint_as_float(x[2 * e]), sl2, -ls[2 * h]));
+              float b = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), sl2, -ls[2 * h + 1]));
+              if (msk) {
+                a = zero_unless_le(a, (uint32_t)(col - clo), span);
+                b = zero_unless_le(b, (uint32_t)(col + 1 - clo), span);
+              }
+              w16[e] = pack_bf16x2(a, b);
+              pk[16 * c + e] = w16[e];
             }
-            w16[e] = pack_bf16x2(a, b);
-            pk[16 * c + e] = w16[e];
           }
-          tmem_st_32x32b_x16(lane_addr + Cfg::kColS + 16 * c, w16);
+          tmem_st_32x32b_x16(colS + 16 * c, w16);
         }
         tmem_st_wait();
         tc_fence_before_sync();
@@ -420,20 +435,26 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
         if (!(ok = mbar_wait(&sm.dp_full, u & 1u, abort))) break;
         tc_fence_after_sync();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t y[32];
-          tmem_ld_32x32b_x32(lane_addr + Cfg::kColDP + 32 * c, y);
+          tmem_ld_32x32b_x32(colDP + 32 * c, y);
           tmem_ld_wait(y);
           uint32_t w16[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int col = 32 * c + 2 * e;
-            const float a = bf16_lo(pk[16 * c + e]) * (__uint_as_float(y[2 * e]) - D[col]);
-            const float b = bf16_hi(pk[16 * c + e]) * (__uint_as_float(y[2 * e + 1]) - D[col + 1]);
-            w16[e] = pack_bf16x2(a, b);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 dd = D4[8 * c + e4];
+            const float ds[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 2 * e4 + h;
+              const float a = bf16_lo(pk[16 * c + e]) * (__uint_as_float(y[2 * e]) - ds[2 * h]);
+              const float b =
+                  bf16_hi(pk[16 * c + e]) * (__uint_as_float(y[2 * e + 1]) - ds[2 * h + 1]);
+              w16[e] = pack_bf16x2(a, b);
+            }
           }
-          // (columns written here were all loaded by this or an earlier chunk)
-          tmem_st_32x32b_x16(lane_addr + Cfg::kColDP + 16 * c, w16);
+          // (the pairs land on columns this thread loaded in chunk 0)
+          tmem_st_32x32b_x16(colDP + 16 * c, w16);
         }
         tmem_st_wait();
         tc_fence_before_sync();
@@ -442,21 +463,21 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
     }
     if (!ok) break;
 
-    // ---- epilogue: dV and scale * dK of key j
+    // ---- epilogue: warpgroup 0 dV, warpgroup 1 scale * dK, of key j
     if (!(ok = mbar_wait(&sm.acc_final, (uint32_t)items & 1u, abort))) break;
     ++items;
     tc_fence_after_sync();
     const bool store = j < p.S;
     const size_t row = ((size_t)I.bkv * p.S + j) * DH;
+    __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + row;
+    const uint32_t colA = lane_addr + (wg == 0 ? Cfg::kColA0 : Cfg::kColA1);
+    const float mul = wg == 0 ? 1.0f : p.scale;
 #pragma unroll 1
     for (int c = 0; c < DH / 32; ++c) {
       uint32_t r[32];
-      tmem_ld_32x32b_x32(lane_addr + Cfg::kColA0 + 32 * c, r);
+      tmem_ld_32x32b_x32(colA + 32 * c, r);
       tmem_ld_wait(r);
-      if (store) bwd_store32(p.dv + row + 32 * c, r, 1.0f);
-      tmem_ld_32x32b_x32(lane_addr + Cfg::kColA1 + 32 * c, r);
-      tmem_ld_wait(r);
-      if (store) bwd_store32(p.dk + row + 32 * c, r, p.scale);
+      if (store) bwd_store32(dst + 32 * c, r, mul);
     }
     // the next item's first dV / dK overwrite the accumulators only after
     // this thread's next arrive on p_full / ds_full, which follows these loads
@@ -493,8 +514,8 @@ __global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.p_full, 128);
-    mbar_init(&sm.ds_full, 128);
+    mbar_init(&sm.p_full, 256);
+    mbar_init(&sm.ds_full, 256);
     mbar_init(&sm.acc_final, 1);
     mbar_init(&sm.mma_done, 1);
     fence_mbarrier_init();
@@ -662,7 +683,8 @@ __device__ __forceinline__ void bwd_dq_issuer(BwdQSmem<DH>& sm, const BwdParams&
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < 128 / 16; ++kk)                              // dQ += dS K
-        mma_bf16_ts_warp(Cfg::kColA0, Cfg::kColDP + kk * 8, dk_mn + st * kStage + kk * (2048 >> 4),
+        mma_bf16_ts_warp(Cfg::kColA0, Cfg::kColDP + bwd_packed_col(kk),
+                         dk_mn + st * kStage + kk * (2048 >> 4),
                          idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
       mma_commit_warp(&sm.kv_empty[st]);
       if (n + 1 < N) {
@@ -677,17 +699,21 @@ __device__ __forceinline__ void bwd_dq_issuer(BwdQSmem<DH>& sm, const BwdParams&
   bwd_wait_drain(&sm.mma_done, 0);
 }
 
-// Element-wise work of the dQ pass (thread t owns query row 128 qb + t):
+// Element-wise work of the dQ pass (warps 0-7; thread t of warpgroup wg owns
+// query row 128 qb + t and key columns 64 wg .. 64 wg + 63):
 // P = exp2(S * scale*log2e - lse2_i) (0 where masked), kept packed in
-// registers; dS = P o (dP - D_i) as bf16 over the first 64 columns of dP.
-// Per item: scale * dQ out.
+// registers; dS = P o (dP - D_i) as bf16 pairs over dP (see bwd_packed_col).
+// Per item: scale * dQ out, each warpgroup half of its columns.
 template <int DH>
 __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams& p,
                                                uint32_t tbase, volatile int* abort, int warp,
                                                int lane) {
   using Cfg = BwdCfg<DH>;
-  const int t = warp * 32 + lane;
-  const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+  const int wg = warp / 4;
+  const int t = (warp % 4) * 32 + lane;
+  const uint32_t lane_addr = tbase + ((uint32_t)((warp % 4) * 32) << 16);
+  const uint32_t colS = lane_addr + Cfg::kColS + 64 * wg;
+  const uint32_t colDP = lane_addr + Cfg::kColDP + 64 * wg;
   const float sl2 = p.scale_log2;
   uint32_t u = 0;
   int items = 0;
@@ -702,21 +728,22 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
     for (int kb = I.lo; kb <= I.hi; ++kb, ++u) {
       if (!(ok = mbar_wait(&sm.s_full, u & 1u, abort))) break;
       tc_fence_after_sync();
-      // visible keys of query i: [klo, khi], as columns [clo, chi] of block kb
+      // visible keys of query i: [klo, khi], as columns [clo, chi] of this half
       const bool msk = bwd_needs_mask(p, I.qb, kb);
+      const int j0 = 128 * kb + 64 * wg;
       int khi = p.S - 1;
       if (p.causal) khi = min(khi, i);
       const int klo = p.window > 0 ? i - p.window + 1 : 0;
-      int clo = klo - 128 * kb;
-      const int chi = khi - 128 * kb;
+      int clo = klo - j0;
+      const int chi = khi - j0;
       const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
       if (chi < clo) clo = 1 << 30;
 
-      uint32_t pk[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t x[32];
-        tmem_ld_32x32b_x32(lane_addr + Cfg::kColS + 32 * c, x);
+        tmem_ld_32x32b_x32(colS + 32 * c, x);
         tmem_ld_wait(x);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -737,9 +764,9 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
       if (!(ok = mbar_wait(&sm.dp_full, u & 1u, abort))) break;
       tc_fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t y[32];
-        tmem_ld_32x32b_x32(lane_addr + Cfg::kColDP + 32 * c, y);
+        tmem_ld_32x32b_x32(colDP + 32 * c, y);
         tmem_ld_wait(y);
         uint32_t w16[16];
 #pragma unroll
@@ -748,7 +775,7 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
           const float b = bf16_hi(pk[16 * c + e]) * (__uint_as_float(y[2 * e + 1]) - Di);
           w16[e] = pack_bf16x2(a, b);
         }
-        tmem_st_32x32b_x16(lane_addr + Cfg::kColDP + 16 * c, w16);
+        tmem_st_32x32b_x16(colDP + 16 * c, w16);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -756,14 +783,14 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
     }
     if (!ok) break;
 
-    // ---- epilogue: scale * dQ of query i
+    // ---- epilogue: scale * dQ of query i, this warpgroup's half of the columns
     if (!(ok = mbar_wait(&sm.acc_final, (uint32_t)items & 1u, abort))) break;
     ++items;
     tc_fence_after_sync();
     const bool store = i < p.S;
     const size_t row = ((size_t)I.bh * p.S + i) * DH;
 #pragma unroll 1
-    for (int c = 0; c < DH / 32; ++c) {
+    for (int c = wg * (DH / 64); c < (wg + 1) * (DH / 64); ++c) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(lane_addr + Cfg::kColA0 + 32 * c, r);
       tmem_ld_wait(r);
@@ -800,9 +827,9 @@ __global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
       mbar_init(&sm.kv_empty[i], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 128);
+    mbar_init(&sm.s_free, 256);
     mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.ds_full, 128);
+    mbar_init(&sm.ds_full, 256);
     mbar_init(&sm.acc_final, 1);
     mbar_init(&sm.mma_done, 1);
     fence_mbarrier_init();
