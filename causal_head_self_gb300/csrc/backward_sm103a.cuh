@@ -361,7 +361,7 @@ __device__ __forceinline__ void bwd_store32(__nv_bfloat16* dst, const uint32_t (
 // owns key row k0 + t, tensor-memory lane t, and query columns
 // 64 wg .. 64 wg + 63).  Per step: P^T = exp2(S^T * scale*log2e - lse2[query])
 // (0 where masked), written as bf16 pairs (see bwd_packed_col) and kept in
-// registers; then dS^T = P^T o (dP^T - D[query]), as bf16 pairs over dP^T.
+// fp32 registers; then dS^T = P^T o (dP^T - D[query]), as bf16 pairs over dP^T.
 // Per item: warpgroup 0 writes dV, warpgroup 1 scale * dK.
 template <int DH>
 __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdParams& p,
@@ -373,7 +373,7 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
   const uint32_t lane_addr = tbase + ((uint32_t)((warp % 4) * 32) << 16);
   const uint32_t colS = lane_addr + Cfg::kColS + 64 * wg;      // this half's scores
   const uint32_t colDP = lane_addr + Cfg::kColDP + 64 * wg;
-  const float sl2 = p.scale_log2;
+  const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
   uint32_t u = 0;
   int items = 0;
   bool ok = true;
@@ -402,28 +402,33 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
         const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
         if (chi < clo) clo = 1 << 30;
 
-        uint32_t pk[32];   // P^T of this row's half, bf16 pairs
+        uint32_t x0[32], x1[32];
+        tmem_ld_32x32b_x32(colS, x0);
+        tmem_ld_32x32b_x32(colS + 32, x1);
+        tmem_ld_wait(x0);
+        tmem_ld_wait(x1);
+        float pf[64];   // P^T of this row's half (fp32)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t x[32];
-          tmem_ld_32x32b_x32(colS + 32 * c, x);
-          tmem_ld_wait(x);
+          const uint32_t* x = c ? x1 : x0;
           uint32_t w16[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 l = L4[8 * c + e4];
-            const float ls[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int e = 2 * e4 + h, col = 32 * c + 2 * e;
-              float a = ex2_approx(fmaf(__uint_as_float(x[2 * e]), sl2, -ls[2 * h]));
-              float b = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), sl2, -ls[2 * h + 1]));
+              const float2 xs = __ffma2_rn(
+                  make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])), sl2,
+                  h ? make_float2(-l.z, -l.w) : make_float2(-l.x, -l.y));
+              float a = ex2_approx(xs.x), b = ex2_approx(xs.y);
               if (msk) {
                 a = zero_unless_le(a, (uint32_t)(col - clo), span);
                 b = zero_unless_le(b, (uint32_t)(col + 1 - clo), span);
               }
+              pf[col] = a;
+              pf[col + 1] = b;
               w16[e] = pack_bf16x2(a, b);
-              pk[16 * c + e] = w16[e];
             }
           }
           tmem_st_32x32b_x16(colS + 16 * c, w16);
@@ -442,15 +447,15 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
           uint32_t w16[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 dd = D4[8 * c + e4];
-            const float ds[4] = {dd.x, dd.y, dd.z, dd.w};
+            const float4 d = D4[8 * c + e4];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const int e = 2 * e4 + h;
-              const float a = bf16_lo(pk[16 * c + e]) * (__uint_as_float(y[2 * e]) - ds[2 * h]);
-              const float b =
-                  bf16_hi(pk[16 * c + e]) * (__uint_as_float(y[2 * e + 1]) - ds[2 * h + 1]);
-              w16[e] = pack_bf16x2(a, b);
+              const int e = 2 * e4 + h, col = 32 * c + 2 * e;
+              const float2 dd = __fadd2_rn(
+                  make_float2(__uint_as_float(y[2 * e]), __uint_as_float(y[2 * e + 1])),
+                  h ? make_float2(-d.z, -d.w) : make_float2(-d.x, -d.y));
+              const float2 ds = __fmul2_rn(make_float2(pf[col], pf[col + 1]), dd);
+              w16[e] = pack_bf16x2(ds.x, ds.y);
             }
           }
           // (the pairs land on columns this thread loaded in chunk 0)
@@ -701,7 +706,7 @@ __device__ __forceinline__ void bwd_dq_issuer(BwdQSmem<DH>& sm, const BwdParams&
 
 // Element-wise work of the dQ pass (warps 0-7; thread t of warpgroup wg owns
 // query row 128 qb + t and key columns 64 wg .. 64 wg + 63):
-// P = exp2(S * scale*log2e - lse2_i) (0 where masked), kept packed in
+// P = exp2(S * scale*log2e - lse2_i) (0 where masked), kept in fp32
 // registers; dS = P o (dP - D_i) as bf16 pairs over dP (see bwd_packed_col).
 // Per item: scale * dQ out, each warpgroup half of its columns.
 template <int DH>
@@ -714,7 +719,7 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
   const uint32_t lane_addr = tbase + ((uint32_t)((warp % 4) * 32) << 16);
   const uint32_t colS = lane_addr + Cfg::kColS + 64 * wg;
   const uint32_t colDP = lane_addr + Cfg::kColDP + 64 * wg;
-  const float sl2 = p.scale_log2;
+  const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
   uint32_t u = 0;
   int items = 0;
   bool ok = true;
@@ -725,6 +730,7 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
     const int i = 128 * I.qb + t;   // this thread's query
     const float L = p.lse2[(size_t)I.bh * p.S_pad + i];
     const float Di = p.delta[(size_t)I.bh * p.S_pad + i];
+    const float2 negL = make_float2(-L, -L), negD = make_float2(-Di, -Di);
     for (int kb = I.lo; kb <= I.hi; ++kb, ++u) {
       if (!(ok = mbar_wait(&sm.s_full, u & 1u, abort))) break;
       tc_fence_after_sync();
@@ -739,27 +745,29 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
       const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
       if (chi < clo) clo = 1 << 30;
 
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t x[32];
-        tmem_ld_32x32b_x32(colS + 32 * c, x);
-        tmem_ld_wait(x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = 32 * c + 2 * e;
-          float a = ex2_approx(fmaf(__uint_as_float(x[2 * e]), sl2, -L));
-          float b = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), sl2, -L));
-          if (msk) {
-            a = zero_unless_le(a, (uint32_t)(col - clo), span);
-            b = zero_unless_le(b, (uint32_t)(col + 1 - clo), span);
-          }
-          pk[16 * c + e] = pack_bf16x2(a, b);
-        }
-      }
+      uint32_t x0[32], x1[32];
+      tmem_ld_32x32b_x32(colS, x0);
+      tmem_ld_32x32b_x32(colS + 32, x1);
+      tmem_ld_wait(x0);
+      tmem_ld_wait(x1);
       // S is in registers: the next S may overwrite it
       tc_fence_before_sync();
       mbar_arrive(&sm.s_free);
+      float pf[64];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const uint32_t* x = e < 16 ? x0 : x1;
+        const int col = 2 * e, k = 2 * (e % 16);
+        const float2 xs = __ffma2_rn(make_float2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])),
+                                     sl2, negL);
+        float a = ex2_approx(xs.x), b = ex2_approx(xs.y);
+        if (msk) {
+          a = zero_unless_le(a, (uint32_t)(col - clo), span);
+          b = zero_unless_le(b, (uint32_t)(col + 1 - clo), span);
+        }
+        pf[col] = a;
+        pf[col + 1] = b;
+      }
 
       if (!(ok = mbar_wait(&sm.dp_full, u & 1u, abort))) break;
       tc_fence_after_sync();
@@ -771,9 +779,11 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
         uint32_t w16[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float a = bf16_lo(pk[16 * c + e]) * (__uint_as_float(y[2 * e]) - Di);
-          const float b = bf16_hi(pk[16 * c + e]) * (__uint_as_float(y[2 * e + 1]) - Di);
-          w16[e] = pack_bf16x2(a, b);
+          const int col = 32 * c + 2 * e;
+          const float2 dd = __fadd2_rn(
+              make_float2(__uint_as_float(y[2 * e]), __uint_as_float(y[2 * e + 1])), negD);
+          const float2 ds = __fmul2_rn(make_float2(pf[col], pf[col + 1]), dd);
+          w16[e] = pack_bf16x2(ds.x, ds.y);
         }
         tmem_st_32x32b_x16(colDP + 16 * c, w16);
       }
