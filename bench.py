@@ -286,6 +286,97 @@ def run_reference(args, rank, world):
     }
 
 
+def _time_launches(fn, flush, stream, iters=10, warmup=3):
+    """Median CUDA-event time (s) of fn() on `stream`, L2 flushed before each."""
+    for _ in range(warmup):
+        fn()
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    return statistics.median(ts)
+
+
+def chunk_flops(w):
+    """4*Dh per visible (query, key) pair of the chunk: row r sees start + r + 1 keys."""
+    pairs = sum(w["start"] + r + 1 for r in range(w["Sq"]))
+    return 4 * w["Dh"] * w["B"] * w["Hq"] * pairs
+
+
+def time_next_rows(chs, dev, flush, stream, peaks):
+    """The rows beyond the headline step, each on its own workload (median of
+    10 launches after 3 warm-ups, L2 flushed before each): chunked prefill,
+    rolling-buffer decode, head size 256 prefill, MQA decode (tensor cores),
+    and the backward pass (2.5x the forward's FLOPs)."""
+    out = {}
+    bf16, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+
+    name = "chunk_gqa_b2_h32kv8_c1024_at3072_d128"
+    w = inputs.WORKLOADS[name]
+    q, kc, vc = (x.to(dev) for x in inputs.workload_inputs(name))
+    t = _time_launches(lambda: chs.attn_fwd_chunk(q, kc, vc, w["start"]), flush, stream)
+    tf = chunk_flops(w) / t / 1e12
+    out["F1_chunked_prefill"] = {"workload": name, "value": tf, "unit": "TFLOP/s",
+                                 "frac_bf16": tf / bf16, "ms_per_launch": t * 1e3}
+    del q, kc, vc
+
+    name = "ring_decode_gqa_b16_h32kv8_c4096_d128"
+    w = inputs.WORKLOADS[name]
+    q, kc, vc, sl = inputs.decode_inputs(w["B"], w["Hq"], w["Hkv"], w["Tmax"], w["Dh"], w["lmin"],
+                                         w["lmax"], w["seed"])
+    q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
+    t = _time_launches(lambda: chs.attn_decode_ring(q, kc, vc, sld, window=w["window"]),
+                       flush, stream)
+    keys = np.minimum(sl.numpy().astype(np.int64), w["window"]).sum()
+    by = keys * w["Hkv"] * w["Dh"] * 2 * 2 + 2 * q.numel() * 2 + sl.numel() * 4
+    out["F2_ring_decode"] = {"workload": name, "value": by / t / 1e9, "unit": "GB/s",
+                             "frac_hbm": by / t / 1e9 / hbm, "tokens_per_s": w["B"] / t,
+                             "ms_per_launch": t * 1e3}
+    del q, kc, vc, sld
+
+    name = "prefill_gqa_b1_h16kv8_s8192_d256"
+    w = inputs.WORKLOADS[name]
+    q, k, v = (x.to(dev) for x in inputs.workload_inputs(name))
+    t = _time_launches(lambda: chs.attn_fwd(q, k, v), flush, stream)
+    tf = prefill_flops(w) / t / 1e12
+    out["F3_prefill_d256"] = {"workload": name, "value": tf, "unit": "TFLOP/s",
+                              "frac_bf16": tf / bf16, "ms_per_launch": t * 1e3}
+    del q, k, v
+
+    name = "decode_mqa_b16_h32kv1_t32768_d128"
+    w = inputs.WORKLOADS[name]
+    q, kc, vc, sl = inputs.workload_inputs(name)
+    by = decode_bytes(w, sl.numpy())
+    q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
+    t = _time_launches(lambda: chs.attn_decode(q, kc, vc, sld), flush, stream)
+    out["F3_mqa_decode"] = {"workload": name, "value": by / t / 1e9, "unit": "GB/s",
+                            "frac_hbm": by / t / 1e9 / hbm,
+                            "tflops": decode_flops(w, sl.numpy()) / t / 1e12,
+                            "tokens_per_s": w["B"] / t, "ms_per_launch": t * 1e3}
+    del q, kc, vc, sld
+
+    name = "backward_mha_b1_h32_s4096_d128"
+    w = inputs.WORKLOADS[name]
+    q, k, v, do = (x.to(dev) for x in inputs.workload_inputs(name))
+    o, lse = chs.attn_fwd_lse(q, k, v)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    t = _time_launches(lambda: chs.attn_bwd(q, k, v, o, do, lse, dq, dk, dv), flush, stream)
+    fl = 2.5 * 4 * w["Dh"] * w["B"] * w["Hq"] * visible_pairs(w["S"], w["causal"], w["window"])
+    out["F4_backward"] = {"workload": name, "value": fl / t / 1e12, "unit": "TFLOP/s",
+                          "frac_bf16": fl / t / 1e12 / bf16, "ms_per_launch": t * 1e3,
+                          "flops": "2.5 x the forward's (10*Dh per visible pair per head); "
+                                   "the kernels execute 14*Dh (S and dP in both passes)"}
+    del q, k, v, do, o, lse, dq, dk, dv
+    if chs.attn_status() != chs.ATTN_OK:
+        raise RuntimeError("device error while timing the next rows")
+    return out
+
+
 def run_gpu(args, rank, world, local_rank):
     import causal_head_self_gb300 as chs
     torch.cuda.set_device(local_rank)
@@ -377,6 +468,8 @@ def run_gpu(args, rank, world, local_rank):
     tp_e2e, td_e2e = max_over_ranks([tp_e2e, td_e2e], world, dev)
     if rank != 0:
         return None
+    del qp, kp, vp, op, qdp, kcp, vcp, slp, odp
+    extras = time_next_rows(chs, dev, flush, stream, read_peaks()[0])
 
     # ---------------------------------------------------------- report
     K = args.steps
@@ -438,6 +531,7 @@ def run_gpu(args, rank, world, local_rank):
                            "h2d_bytes_per_step": sum(x.numel() * x.element_size()
                                                      for x in (qdh, kch, vch, slh)),
                            "d2h_bytes_per_step": od.numel() * od.element_size()}},
+        "next_rows": extras,
         "gpu_launches": 2 * K,   # one prefill and one decode kernel per step
         "clocks": clocks.summary(),
         "wall_s_timed_region": t_wall,

@@ -38,6 +38,21 @@ WORKLOADS = {
                                            causal=True, window=0, seed=2),
     "backward_gqa_b2_h32kv8_s2048_d128": dict(kind="backward", B=2, Hq=32, Hkv=8, S=2048,
                                               Dh=128, causal=True, window=0, seed=7),
+    # the S=4096 backward on 8 heads (a profiler-sized case)
+    "backward_mha_b1_h8_s4096_d128": dict(kind="backward", B=1, Hq=8, Hkv=8, S=4096, Dh=128,
+                                          causal=True, window=0, seed=2),
+    # chunked prefill: a 1024-token chunk after 3072 cached tokens (cache of 4096 rows)
+    "chunk_gqa_b2_h32kv8_c1024_at3072_d128": dict(kind="chunk", B=2, Hq=32, Hkv=8, Sq=1024,
+                                                  Tmax=4096, start=3072, Dh=128, causal=True,
+                                                  window=0, seed=8),
+    # rolling-buffer decode: a 4096-row ring per (sequence, K/V head) holding the
+    # last 4096 of 16384..32768 positions, window 4096
+    "ring_decode_gqa_b16_h32kv8_c4096_d128": dict(kind="ring", B=16, Hq=32, Hkv=8, Tmax=4096,
+                                                  Dh=128, lmin=16384, lmax=32768, window=4096,
+                                                  seed=9),
+    # MQA decode: 32 query heads on one K/V head (the tensor-core decode path)
+    "decode_mqa_b16_h32kv1_t32768_d128": dict(kind="decode", B=16, Hq=32, Hkv=1, Tmax=32768,
+                                              Dh=128, lmin=16384, lmax=32768, window=0, seed=10),
     # one decode step for 16 sequences against caches of 16384..32768 keys
     "decode_gqa_b16_h32kv8_t32768_d128": dict(kind="decode", B=16, Hq=32, Hkv=8, Tmax=32768,
                                               Dh=128, lmin=16384, lmax=32768, window=0, seed=4),
@@ -86,5 +101,8 @@ def workload_inputs(name):
     if w["kind"] == "backward":
         q, k, v = prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["S"], w["Dh"], w["seed"])
         return q, k, v, grad_inputs(q.shape, w["seed"])
+    if w["kind"] == "chunk":
+        q, k, v = prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["Tmax"], w["Dh"], w["seed"])
+        return q[:, :, :w["Sq"]].contiguous(), k, v
     return decode_inputs(w["B"], w["Hq"], w["Hkv"], w["Tmax"], w["Dh"], w["lmin"], w["lmax"],
                          w["seed"])

@@ -30,6 +30,20 @@ def main(argv=None):
         o = torch.empty_like(q)
         for _ in range(args.iters):
             chs.attn_fwd(q, k, v, o, causal=bool(w["causal"]), window=w["window"])
+    elif w["kind"] == "backward":
+        q, k, v, do = (x.to(dev) for x in inputs.workload_inputs(args.workload))
+        o, lse = chs.attn_fwd_lse(q, k, v, causal=bool(w["causal"]), window=w["window"])
+        for _ in range(args.iters):
+            chs.attn_bwd(q, k, v, o, do, lse, causal=bool(w["causal"]), window=w["window"])
+    elif w["kind"] == "chunk":
+        q, kc, vc = (x.to(dev) for x in inputs.workload_inputs(args.workload))
+        for _ in range(args.iters):
+            chs.attn_fwd_chunk(q, kc, vc, w["start"], causal=bool(w["causal"]), window=w["window"])
+    elif w["kind"] == "ring":
+        q, kc, vc, sl = (x.to(dev) for x in inputs.decode_inputs(
+            w["B"], w["Hq"], w["Hkv"], w["Tmax"], w["Dh"], w["lmin"], w["lmax"], w["seed"]))
+        for _ in range(args.iters):
+            chs.attn_decode_ring(q, kc, vc, sl, window=w["window"])
     else:
         q, kc, vc, sl = (x.to(dev) for x in inputs.workload_inputs(args.workload))
         o = torch.empty_like(q)
