@@ -96,3 +96,43 @@ def test_python_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         _binding.attn_fwd(q, q, q)
+
+
+def test_fwd_lse_argument_checks(lib):
+    a = (1, 4, 4, 16, 128, 1, 0)
+    f = lib.attn_fwd_lse
+    assert f(*P, None, *a, 0.0, None) == _binding.ATTN_ERR_INVALID_ARG          # no lse
+    assert f(*P, 0x50002, *a, 0.0, None) == _binding.ATTN_ERR_INVALID_ARG       # misaligned lse
+    assert f(*P, 0x50000, 1, 4, 4, 16, 96, 1, 0, 0.0, None) == _binding.ATTN_ERR_UNSUPPORTED
+    assert f(*P, None, 0, 4, 4, 16, 128, 1, 0, 0.0, None) == _binding.ATTN_OK   # empty: no-op
+    assert f(*P, 0x10000, *a, 0.0, None) == _binding.ATTN_ERR_INVALID_ARG       # lse aliases q
+
+
+# q, k, v, o, dout, lse, dq, dk, dv (disjoint fake addresses)
+PB = [0x100000 * (i + 1) for i in range(9)]
+
+
+def bwd(lib, *args, ptrs=PB, scale=0.0):
+    B, Hq, Hkv, S, Dh, causal, window = args
+    return lib.attn_bwd(*ptrs, B, Hq, Hkv, S, Dh, causal, window, scale, None)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 6, 4, 16, 128, 1, 0), _binding.ATTN_ERR_INVALID_ARG),   # Hq % Hkv != 0
+    ((1, 4, 4, 16, 256, 1, 0), _binding.ATTN_ERR_UNSUPPORTED),   # backward takes Dh 64 / 128
+    ((1, 4, 4, 16, 128, 0, 8), _binding.ATTN_ERR_INVALID_ARG),   # window without causal
+    ((1, 4, 4, 16, 128, 2, 0), _binding.ATTN_ERR_INVALID_ARG),   # causal flag not 0/1
+    ((0, 4, 4, 16, 128, 1, 0), _binding.ATTN_OK),                # empty batch: no-op
+    ((2, 4, 4, 0, 128, 1, 0), _binding.ATTN_OK),                 # empty sequence: no-op
+])
+def test_bwd_argument_checks(lib, args, code):
+    assert bwd(lib, *args) == code
+
+
+def test_bwd_rejects_bad_pointers_aliasing_and_scale(lib):
+    a = (1, 4, 4, 16, 128, 1, 0)
+    assert bwd(lib, *a, scale=-1.0) == _binding.ATTN_ERR_INVALID_ARG
+    assert bwd(lib, *a, ptrs=PB[:5] + [0] + PB[6:]) == _binding.ATTN_ERR_INVALID_ARG        # no lse
+    assert bwd(lib, *a, ptrs=PB[:6] + [PB[6] + 8] + PB[7:]) == _binding.ATTN_ERR_INVALID_ARG  # dq misaligned
+    assert bwd(lib, *a, ptrs=PB[:6] + [PB[0]] + PB[7:]) == _binding.ATTN_ERR_INVALID_ARG     # dq = q
+    assert bwd(lib, *a, ptrs=PB[:7] + [PB[6]] + PB[8:]) == _binding.ATTN_ERR_INVALID_ARG     # dk = dq
