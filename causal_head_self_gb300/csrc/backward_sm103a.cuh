@@ -65,19 +65,25 @@ template <int DH>
 struct BwdCfg {
   static constexpr int kBox = 128 * 64 * 2;         // one 128-row x 64-column box
   static constexpr int kTile = (DH / 64) * kBox;    // a 128 x DH tile
-  // warps 0-7: element-wise work (warp w: tensor-memory lanes 32 (w % 4) ..,
-  // columns 64 (w / 4) .. + 63 of S and dP); warp 8: TMA; warp 9: MMA
-  static constexpr int kThreads = 320;
-  static constexpr int kWarpProducer = 8, kWarpIssuer = 9;
+  // warps 0 .. 4 kWG - 1: element-wise work (warp w: tensor-memory lanes
+  // 32 (w % 4) .., columns kCols (w / 4) .. + kCols - 1 of S and dP); then one
+  // TMA warp and one MMA warp
+  static constexpr int kWG = 2;                 // element-wise warpgroups
+  static constexpr int kCols = 128 / kWG;       // columns of S / dP per warpgroup
+  static constexpr int kChunks = kCols / 32;    // 32-column tensor-memory loads per row
+  static constexpr int kEW = 128 * kWG;         // element-wise threads
+  static constexpr int kThreads = 32 * (4 * kWG + 2);
+  static constexpr int kWarpProducer = 4 * kWG, kWarpIssuer = 4 * kWG + 1;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColA0 = 256, kColA1 = 384;
 };
 
 // Where the bf16 pairs of columns 16 kk .. 16 kk + 15 of a 128-column S or dP
-// buffer are written (P over S, dS over dP): each column half's pairs go to
-// the first 32 columns of that half, so that one warpgroup's stores never
-// land on columns the other warpgroup has still to load.
+// buffer are written (P over S, dS over dP): each warpgroup's pairs go to the
+// first half of its own kCols columns, so that one warpgroup's stores never
+// land on columns another warpgroup has still to load.
 __host__ __device__ constexpr uint32_t bwd_packed_col(int kk) {
-  return 8u * (uint32_t)kk + (kk >= 4 ? 32u : 0u);
+  constexpr int cols = BwdCfg<64>::kCols;
+  return (uint32_t)(cols * (16 * kk / cols) + (16 * kk % cols) / 2);
 }
 
 // D_i = sum_d dO[i, d] o[i, d] (fp32 products of the bf16 values) and
@@ -362,7 +368,7 @@ __device__ __forceinline__ void bwd_store32(__nv_bfloat16* dst, const uint32_t (
 // 64 wg .. 64 wg + 63).  Per step: P^T = exp2(S^T * scale*log2e - lse2[query])
 // (0 where masked), written as bf16 pairs (see bwd_packed_col) and kept in
 // fp32 registers; then dS^T = P^T o (dP^T - D[query]), as bf16 pairs over dP^T.
-// Per item: warpgroup 0 writes dV, warpgroup 1 scale * dK.
+// Per item: the first half of the warpgroups write dV, the second scale * dK.
 template <int DH>
 __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdParams& p,
                                                  uint32_t tbase, volatile int* abort, int warp,
@@ -371,8 +377,8 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
   const int wg = warp / 4;
   const int t = (warp % 4) * 32 + lane;
   const uint32_t lane_addr = tbase + ((uint32_t)((warp % 4) * 32) << 16);
-  const uint32_t colS = lane_addr + Cfg::kColS + 64 * wg;      // this half's scores
-  const uint32_t colDP = lane_addr + Cfg::kColDP + 64 * wg;
+  const uint32_t colS = lane_addr + Cfg::kColS + Cfg::kCols * wg;   // this warpgroup's scores
+  const uint32_t colDP = lane_addr + Cfg::kColDP + Cfg::kCols * wg;
   const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
   uint32_t u = 0;
   int items = 0;
@@ -389,28 +395,27 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
         if (!(ok = mbar_wait(&sm.q_full[st], (u >> 1) & 1u, abort))) break;
         if (!(ok = mbar_wait(&sm.s_full, u & 1u, abort))) break;
         tc_fence_after_sync();
-        const float4* L4 = reinterpret_cast<const float4*>(sm.lse2[st] + 64 * wg);
-        const float4* D4 = reinterpret_cast<const float4*>(sm.dlt[st] + 64 * wg);
+        const float4* L4 = reinterpret_cast<const float4*>(sm.lse2[st] + Cfg::kCols * wg);
+        const float4* D4 = reinterpret_cast<const float4*>(sm.dlt[st] + Cfg::kCols * wg);
         // visible query columns of key j: c in [clo, chi] of this half (query
         // i = 128 qb + 64 wg + c)
         const bool msk = bwd_needs_mask(p, qb, I.kb);
-        const int i0 = 128 * qb + 64 * wg;
-        int clo = 0, chi = 63;
+        const int i0 = 128 * qb + Cfg::kCols * wg;
+        int clo = 0, chi = Cfg::kCols - 1;
         if (p.causal) clo = j - i0;                                     // i >= j
         if (p.window > 0) chi = min(chi, j - i0 + p.window - 1);        // i - j < W
         chi = min(chi, p.S - 1 - i0);                                   // i < S
         const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
         if (chi < clo) clo = 1 << 30;
 
-        uint32_t x0[32], x1[32];
-        tmem_ld_32x32b_x32(colS, x0);
-        tmem_ld_32x32b_x32(colS + 32, x1);
-        tmem_ld_wait(x0);
-        tmem_ld_wait(x1);
-        float pf[64];   // P^T of this row's half (fp32)
+        uint32_t x[Cfg::kChunks][32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t* x = c ? x1 : x0;
+        for (int c = 0; c < Cfg::kChunks; ++c) tmem_ld_32x32b_x32(colS + 32 * c, x[c]);
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c) tmem_ld_wait(x[c]);
+        float pf[Cfg::kCols];   // P^T of this row's columns (fp32)
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c) {
           uint32_t w16[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
@@ -419,7 +424,7 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
             for (int h = 0; h < 2; ++h) {
               const int e = 2 * e4 + h, col = 32 * c + 2 * e;
               const float2 xs = __ffma2_rn(
-                  make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])), sl2,
+                  make_float2(__uint_as_float(x[c][2 * e]), __uint_as_float(x[c][2 * e + 1])), sl2,
                   h ? make_float2(-l.z, -l.w) : make_float2(-l.x, -l.y));
               float a = ex2_approx(xs.x), b = ex2_approx(xs.y);
               if (msk) {
@@ -440,7 +445,7 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
         if (!(ok = mbar_wait(&sm.dp_full, u & 1u, abort))) break;
         tc_fence_after_sync();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < Cfg::kChunks; ++c) {
           uint32_t y[32];
           tmem_ld_32x32b_x32(colDP + 32 * c, y);
           tmem_ld_wait(y);
@@ -468,17 +473,19 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
     }
     if (!ok) break;
 
-    // ---- epilogue: warpgroup 0 dV, warpgroup 1 scale * dK, of key j
+    // ---- epilogue: dV and scale * dK of key j
     if (!(ok = mbar_wait(&sm.acc_final, (uint32_t)items & 1u, abort))) break;
     ++items;
     tc_fence_after_sync();
     const bool store = j < p.S;
     const size_t row = ((size_t)I.bkv * p.S + j) * DH;
-    __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + row;
-    const uint32_t colA = lane_addr + (wg == 0 ? Cfg::kColA0 : Cfg::kColA1);
-    const float mul = wg == 0 ? 1.0f : p.scale;
+    constexpr int kHalf = Cfg::kWG / 2;              // warpgroups per accumulator
+    const bool is_dv = wg < kHalf;
+    __nv_bfloat16* dst = (is_dv ? p.dv : p.dk) + row;
+    const uint32_t colA = lane_addr + (is_dv ? Cfg::kColA0 : Cfg::kColA1);
+    const float mul = is_dv ? 1.0f : p.scale;
 #pragma unroll 1
-    for (int c = 0; c < DH / 32; ++c) {
+    for (int c = wg % kHalf; c < DH / 32; c += kHalf) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(colA + 32 * c, r);
       tmem_ld_wait(r);
@@ -519,8 +526,8 @@ __global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.p_full, 256);
-    mbar_init(&sm.ds_full, 256);
+    mbar_init(&sm.p_full, Cfg::kEW);
+    mbar_init(&sm.ds_full, Cfg::kEW);
     mbar_init(&sm.acc_final, 1);
     mbar_init(&sm.mma_done, 1);
     fence_mbarrier_init();
@@ -717,8 +724,8 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
   const int wg = warp / 4;
   const int t = (warp % 4) * 32 + lane;
   const uint32_t lane_addr = tbase + ((uint32_t)((warp % 4) * 32) << 16);
-  const uint32_t colS = lane_addr + Cfg::kColS + 64 * wg;
-  const uint32_t colDP = lane_addr + Cfg::kColDP + 64 * wg;
+  const uint32_t colS = lane_addr + Cfg::kColS + Cfg::kCols * wg;
+  const uint32_t colDP = lane_addr + Cfg::kColDP + Cfg::kCols * wg;
   const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
   uint32_t u = 0;
   int items = 0;
@@ -736,7 +743,7 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
       tc_fence_after_sync();
       // visible keys of query i: [klo, khi], as columns [clo, chi] of this half
       const bool msk = bwd_needs_mask(p, I.qb, kb);
-      const int j0 = 128 * kb + 64 * wg;
+      const int j0 = 128 * kb + Cfg::kCols * wg;
       int khi = p.S - 1;
       if (p.causal) khi = min(khi, i);
       const int klo = p.window > 0 ? i - p.window + 1 : 0;
@@ -745,20 +752,19 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
       const uint32_t span = chi >= clo ? (uint32_t)(chi - clo) : 0u;
       if (chi < clo) clo = 1 << 30;
 
-      uint32_t x0[32], x1[32];
-      tmem_ld_32x32b_x32(colS, x0);
-      tmem_ld_32x32b_x32(colS + 32, x1);
-      tmem_ld_wait(x0);
-      tmem_ld_wait(x1);
+      uint32_t x[Cfg::kChunks][32];
+#pragma unroll
+      for (int c = 0; c < Cfg::kChunks; ++c) tmem_ld_32x32b_x32(colS + 32 * c, x[c]);
+#pragma unroll
+      for (int c = 0; c < Cfg::kChunks; ++c) tmem_ld_wait(x[c]);
       // S is in registers: the next S may overwrite it
       tc_fence_before_sync();
       mbar_arrive(&sm.s_free);
-      float pf[64];
+      float pf[Cfg::kCols];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const uint32_t* x = e < 16 ? x0 : x1;
-        const int col = 2 * e, k = 2 * (e % 16);
-        const float2 xs = __ffma2_rn(make_float2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])),
+      for (int e = 0; e < Cfg::kCols / 2; ++e) {
+        const int col = 2 * e, c = col / 32, k = col % 32;
+        const float2 xs = __ffma2_rn(make_float2(__uint_as_float(x[c][k]), __uint_as_float(x[c][k + 1])),
                                      sl2, negL);
         float a = ex2_approx(xs.x), b = ex2_approx(xs.y);
         if (msk) {
@@ -772,7 +778,7 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
       if (!(ok = mbar_wait(&sm.dp_full, u & 1u, abort))) break;
       tc_fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < Cfg::kChunks; ++c) {
         uint32_t y[32];
         tmem_ld_32x32b_x32(colDP + 32 * c, y);
         tmem_ld_wait(y);
@@ -800,7 +806,7 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
     const bool store = i < p.S;
     const size_t row = ((size_t)I.bh * p.S + i) * DH;
 #pragma unroll 1
-    for (int c = wg * (DH / 64); c < (wg + 1) * (DH / 64); ++c) {
+    for (int c = wg; c < DH / 32; c += Cfg::kWG) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(lane_addr + Cfg::kColA0 + 32 * c, r);
       tmem_ld_wait(r);
@@ -837,9 +843,9 @@ __global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
       mbar_init(&sm.kv_empty[i], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 256);
+    mbar_init(&sm.s_free, Cfg::kEW);
     mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.ds_full, 256);
+    mbar_init(&sm.ds_full, Cfg::kEW);
     mbar_init(&sm.acc_final, 1);
     mbar_init(&sm.mma_done, 1);
     fence_mbarrier_init();
