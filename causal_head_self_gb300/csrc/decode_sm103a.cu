@@ -152,8 +152,20 @@ static cudaError_t launch_tc_dh(const CUtensorMap& mq, const CUtensorMap& mk, co
   attn_decode_tc_sm103a<DH><<<grid, DecodeTcCfg<DH>::kThreads, smem, stream>>>(mq, mk, mv, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_decode_tc_combine<DH><<<prm.B * prm.Hq, DH, 0, stream>>>(prm);
-  return cudaGetLastError();
+  // the combine kernel is a programmatic dependent launch: it is scheduled as
+  // the decode CTAs finish and waits on the grid dependency, so its launch
+  // latency overlaps the decode kernel's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(prm.B * prm.Hq);
+  cfg.blockDim = dim3(DH);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_decode_tc_combine<DH>, prm);
 }
 
 cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, const int* seqlens,

@@ -404,6 +404,9 @@ __global__ void __launch_bounds__(192, 1)
     tmem_dealloc(tbase, Cfg::kCols);
   }
   if (threadIdx.x == 0 && sm.abort_flag) atomicExch(p.error_word, 4);   // ATTN_ERR_TIMEOUT
+  // this CTA's partials are written: the combine grid may be scheduled (it
+  // still waits for this whole grid to finish before reading them)
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Merge the splits of one (b, query head): o = sum_s 2^(m_s - M) o_s /
@@ -411,6 +414,9 @@ __global__ void __launch_bounds__(192, 1)
 // in split order.  One block of DH threads per (b, query head).
 template <int DH>
 __global__ void __launch_bounds__(DH) attn_decode_tc_combine(const DecodeTcParams p) {
+  // launched as a programmatic dependent of attn_decode_tc_sm103a: wait until
+  // that grid has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bh = blockIdx.x;
   const int b = bh / p.Hq;
   const int d = threadIdx.x;
