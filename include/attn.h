@@ -159,7 +159,8 @@ int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* 
  * ATTN_ERR_INVALID_ARG for attn_status().
  * With Hq / Hkv >= 8 (MQA-like groups) and Dh <= 128 the step runs on the tensor cores
  * (the group's query heads packed as the rows of one contraction with each
- * key tile) followed by a small combine kernel; otherwise on the CUDA cores.
+ * key tile) followed by a small combine kernel (a programmatic dependent
+ * launch on the same stream); otherwise on the CUDA cores.
  * The split-KV partials live in a library-owned device workspace, allocated
  * on first use per device and grown on demand (cudaMalloc): make the first
  * call with the largest shape outside any CUDA graph capture.  Calls on one
