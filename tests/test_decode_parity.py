@@ -38,6 +38,8 @@ CASES = [
     (3, 8, 2, 2000, 64, 1, 2000, 0),
     (2, 16, 4, 5000, 64, 4000, 5000, 1000),
     (1, 32, 8, 20000, 128, 20000, 20000, 0),
+    (3, 8, 2, 12000, 128, 9000, 12000, 0),  # several 2048-key splits per sequence
+    (2, 8, 4, 12000, 64, 9000, 12000, 3000),
 ]
 
 

@@ -54,6 +54,7 @@ CASES = [
     (2, 8, 2, 640, 128, [639, 7001], 640),             # window == ring
     (1, 2, 2, 33, 128, [1000], 0),                     # a ring barely larger than a block
     (2, 8, 2, 500, 256, [1234, 499], 0),               # Dh 256: 16-key stages
+    (2, 8, 2, 8192, 128, [8192 * 2 + 5, 9000], 0),     # wrapped, four 2048-key splits to merge
 ]
 
 
