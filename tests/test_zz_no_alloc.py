@@ -27,7 +27,7 @@ def _built():
 # (B, Hq, Hkv, Tmax, Dh, lmin, lmax, window): several splits per sequence
 CASES = [
     (4, 32, 8, 4096, 128, 1000, 4096, 0),
-    (3, 8, 2, 2000, 64, 1, 2000, 300),
+    (3, 8, 2, 5000, 64, 1, 5000, 3000),
 ]
 
 
