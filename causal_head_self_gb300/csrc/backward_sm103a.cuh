@@ -29,11 +29,12 @@
 // reduced across key blocks with atomics: 7 MMAs per block pair instead of 5,
 // in exchange for a deterministic result.
 //
-// Roles: warps 0-7 run the element-wise work and the epilogues, two
-// warpgroups on the two column halves of the same 128 rows (thread t of
-// either owns tensor-memory lane t), so each does half of every step's
-// exponentials and the two halves run side by side; warp 8 lane 0 issues
-// every TMA copy, warp 9 every MMA (one elected lane).  Every wait is bounded.
+// Roles: the first 4 kWG warps run the element-wise work and the epilogues,
+// kWG warpgroups on kWG column ranges of the same 128 rows (thread t of each
+// owns tensor-memory lane t), so each does a share of every step's
+// exponentials and the shares run side by side (kWG = 2: two halves); the
+// next warp's lane 0 issues every TMA copy, the last warp every MMA (one
+// elected lane).  Every wait is bounded.
 #pragma once
 
 #include <cstdint>
@@ -365,7 +366,7 @@ __device__ __forceinline__ void bwd_store32(__nv_bfloat16* dst, const uint32_t (
 
 // Element-wise work of the dK/dV pass (warps 0-7; thread t of warpgroup wg
 // owns key row k0 + t, tensor-memory lane t, and query columns
-// 64 wg .. 64 wg + 63).  Per step: P^T = exp2(S^T * scale*log2e - lse2[query])
+// kCols wg .. kCols (wg + 1) - 1).  Per step: P^T = exp2(S^T * scale*log2e - lse2[query])
 // (0 where masked), written as bf16 pairs (see bwd_packed_col) and kept in
 // fp32 registers; then dS^T = P^T o (dP^T - D[query]), as bf16 pairs over dP^T.
 // Per item: the first half of the warpgroups write dV, the second scale * dK.
@@ -397,8 +398,8 @@ __device__ __forceinline__ void bwd_dkdv_softmax(BwdKvSmem<DH>& sm, const BwdPar
         tc_fence_after_sync();
         const float4* L4 = reinterpret_cast<const float4*>(sm.lse2[st] + Cfg::kCols * wg);
         const float4* D4 = reinterpret_cast<const float4*>(sm.dlt[st] + Cfg::kCols * wg);
-        // visible query columns of key j: c in [clo, chi] of this half (query
-        // i = 128 qb + 64 wg + c)
+        // visible query columns of key j: c in [clo, chi] of this warpgroup's
+        // columns (query i = 128 qb + kCols wg + c)
         const bool msk = bwd_needs_mask(p, qb, I.kb);
         const int i0 = 128 * qb + Cfg::kCols * wg;
         int clo = 0, chi = Cfg::kCols - 1;
@@ -712,10 +713,10 @@ __device__ __forceinline__ void bwd_dq_issuer(BwdQSmem<DH>& sm, const BwdParams&
 }
 
 // Element-wise work of the dQ pass (warps 0-7; thread t of warpgroup wg owns
-// query row 128 qb + t and key columns 64 wg .. 64 wg + 63):
+// query row 128 qb + t and key columns kCols wg .. kCols (wg + 1) - 1):
 // P = exp2(S * scale*log2e - lse2_i) (0 where masked), kept in fp32
 // registers; dS = P o (dP - D_i) as bf16 pairs over dP (see bwd_packed_col).
-// Per item: scale * dQ out, each warpgroup half of its columns.
+// Per item: scale * dQ out, the 32-column chunks dealt to the warpgroups.
 template <int DH>
 __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams& p,
                                                uint32_t tbase, volatile int* abort, int warp,
@@ -741,7 +742,7 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
     for (int kb = I.lo; kb <= I.hi; ++kb, ++u) {
       if (!(ok = mbar_wait(&sm.s_full, u & 1u, abort))) break;
       tc_fence_after_sync();
-      // visible keys of query i: [klo, khi], as columns [clo, chi] of this half
+      // visible keys of query i: [klo, khi], as columns [clo, chi] of this warpgroup's
       const bool msk = bwd_needs_mask(p, I.qb, kb);
       const int j0 = 128 * kb + Cfg::kCols * wg;
       int khi = p.S - 1;
@@ -799,7 +800,7 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
     }
     if (!ok) break;
 
-    // ---- epilogue: scale * dQ of query i, this warpgroup's half of the columns
+    // ---- epilogue: scale * dQ of query i, this warpgroup's chunks of the columns
     if (!(ok = mbar_wait(&sm.acc_final, (uint32_t)items & 1u, abort))) break;
     ++items;
     tc_fence_after_sync();
