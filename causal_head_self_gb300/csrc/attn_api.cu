@@ -404,16 +404,8 @@ extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
-  const chs::DecodePlan plan = chs::plan_decode(B, Hq, Hkv, Tmax, Dh, st->info.num_sms);
-  if ((long long)Hkv * ((Hq / Hkv) / plan.heads_per_cta) > 65535) return ATTN_ERR_INVALID_ARG;
-  // scratch layout: counters (256-byte aligned) | split partials
-  const size_t n_counters = chs::decode_counter_count(B, Hq, Hkv, plan);
-  const size_t counter_bytes = (n_counters * sizeof(int) + 255) / 256 * 256;
-  const size_t partial_bytes = chs::decode_partials_bytes(B, Hq, Dh, plan);
-  if (counter_bytes + partial_bytes > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH_LIMIT;
-  unsigned char* scratch = nullptr;
-  {
-    // set-up, once per device, with that device current
+  // the fixed array's address, looked up once per device with that device current
+  auto scratch_ptr = [&](unsigned char** out) -> int {
     std::lock_guard<std::mutex> lock(g_mutex);
     const int dev = st->info.device;
     if (!g_noalloc_ptr[dev]) {
@@ -422,8 +414,31 @@ extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void
         return ATTN_ERR_CUDA;
       g_noalloc_ptr[dev] = static_cast<unsigned char*>(ptr);
     }
-    scratch = g_noalloc_ptr[dev];
+    *out = g_noalloc_ptr[dev];
+    return ATTN_OK;
+  };
+  unsigned char* scratch = nullptr;
+  if (Dh <= 128 && Hq / Hkv >= chs::kDecodeTcMinGroup) {
+    // large query-head groups: the tensor-core path, as in attn_decode; its
+    // split partials are the scratch's only content (it keeps no counters)
+    const chs::DecodePlan plan = chs::plan_decode_tc(B, Hq, Hkv, Tmax, st->info.num_sms);
+    if ((long long)B * Hkv * ((Hq / Hkv + 127) / 128) > 65535) return ATTN_ERR_INVALID_ARG;
+    if (chs::decode_partials_bytes(B, Hq, Dh, plan) > kNoAllocScratchBytes)
+      return ATTN_ERR_SCRATCH_LIMIT;
+    if ((rc = scratch_ptr(&scratch)) != ATTN_OK) return rc;
+    cudaError_t e = chs::launch_decode_tc(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh,
+                                          window, scale_log2, plan, scratch, launch_info(st),
+                                          stream);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
+  const chs::DecodePlan plan = chs::plan_decode(B, Hq, Hkv, Tmax, Dh, st->info.num_sms);
+  if ((long long)Hkv * ((Hq / Hkv) / plan.heads_per_cta) > 65535) return ATTN_ERR_INVALID_ARG;
+  // scratch layout: counters (256-byte aligned) | split partials
+  const size_t n_counters = chs::decode_counter_count(B, Hq, Hkv, plan);
+  const size_t counter_bytes = (n_counters * sizeof(int) + 255) / 256 * 256;
+  const size_t partial_bytes = chs::decode_partials_bytes(B, Hq, Dh, plan);
+  if (counter_bytes + partial_bytes > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH_LIMIT;
+  if ((rc = scratch_ptr(&scratch)) != ATTN_OK) return rc;
   int* counters = reinterpret_cast<int*>(scratch);
   // the array keeps the previous call's contents: the counters must start at zero
   if (cudaMemsetAsync(counters, 0, n_counters * sizeof(int), stream) != cudaSuccess)

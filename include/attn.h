@@ -205,13 +205,16 @@ int attn_decode_ring(const void* q, const void* kcache, const void* vcache, cons
  *   - Its scratch (split partials and completion counters) is one fixed
  *     16 MiB device array inside this library.  Every GPU that loads the
  *     library holds it until the process exits.
- *   - A call needs 4*B*Hkv*(Hq/Hkv)/h bytes of counters (h = 4, 2 or 1
- *     query heads per CTA, rounded up to 256 bytes) plus
+ *   - It runs the kernels attn_decode runs for the same arguments (the
+ *     tensor-core path for Hq / Hkv >= 8 and Dh <= 128, the CUDA-core path
+ *     otherwise), with the same split plan, so the results are the same bits.
+ *   - On the CUDA-core path a call needs 4*B*Hkv*(Hq/Hkv)/h bytes of counters
+ *     (h = 4, 2 or 1 query heads per CTA, rounded up to 256 bytes) plus
  *     B*Hq*nsplit*(Dh+2)*4 bytes of partials (each part rounded up to 256),
- *     where nsplit is the split count attn_decode would use.  A call that
- *     needs more than 16 MiB returns ATTN_ERR_SCRATCH_LIMIT before anything
- *     runs.  (The B=16, Hq=32, Hkv=8, Tmax=32768, Dh=128 decode step needs
- *     about 7.7 MB.)
+ *     where nsplit is the split count attn_decode would use; on the
+ *     tensor-core path only the partials.  A call that needs more than
+ *     16 MiB returns ATTN_ERR_SCRATCH_LIMIT before anything runs.  (The
+ *     B=16, Hq=32, Hkv=8, Tmax=32768, Dh=128 decode step needs about 4.3 MB.)
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
  *   - Every call shares the one array, which keeps the previous call's

@@ -28,6 +28,7 @@ def _built():
 CASES = [
     (4, 32, 8, 4096, 128, 1000, 4096, 0),
     (3, 8, 2, 5000, 64, 1, 5000, 3000),
+    (4, 32, 1, 9000, 128, 3000, 9000, 0),    # MQA: the tensor-core path and its combine
 ]
 
 
@@ -43,6 +44,8 @@ def test_noalloc_matches_decode_on_two_calls(B, Hq, Hkv, Tmax, Dh, lmin, lmax, w
         o = chs.attn_decode_noalloc(q, kc, vc, sl, window=window)
         assert chs.attn_status() == chs.ATTN_OK
         assert_close(o.float().cpu().numpy(), ref, what="noalloc vs decode")
+        # the same kernels and split plan as attn_decode: the same bits
+        assert (o.float().cpu().numpy() == ref).all()
 
 
 def test_noalloc_rejects_a_call_beyond_its_scratch():
