@@ -248,7 +248,7 @@ static int decode_common(const void* q, const void* kcache, const void* vcache, 
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
-  if (!ring && Dh <= 128 && Hq / Hkv >= chs::kDecodeTcMinGroup) {
+  if (!ring && Hq / Hkv >= chs::kDecodeTcMinGroup) {
     // many query heads per cached byte: the tensor-core path (a contraction)
     const chs::DecodePlan plan = chs::plan_decode_tc(B, Hq, Hkv, Tmax, st->info.num_sms);
     if ((long long)B * Hkv * ((Hq / Hkv + 127) / 128) > 65535) return ATTN_ERR_INVALID_ARG;
@@ -418,7 +418,7 @@ extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void
     return ATTN_OK;
   };
   unsigned char* scratch = nullptr;
-  if (Dh <= 128 && Hq / Hkv >= chs::kDecodeTcMinGroup) {
+  if (Hq / Hkv >= chs::kDecodeTcMinGroup) {
     // large query-head groups: the tensor-core path, as in attn_decode; its
     // split partials are the scratch's only content (it keeps no counters)
     const chs::DecodePlan plan = chs::plan_decode_tc(B, Hq, Hkv, Tmax, st->info.num_sms);

@@ -177,9 +177,10 @@ cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, cons
                              const DeviceInfo& dev, cudaStream_t stream) {
   const int G = Hq / Hkv;
   CUtensorMap mq, mk, mv;
+  const int keys = Dh == 256 ? DecodeTcCfg<256>::kKeys : DecodeTcCfg<128>::kKeys;   // tile rows
   if (!encode_bf16_map(&mq, q, Dh, G, (long long)B * Hkv, 128) ||
-      !encode_bf16_map(&mk, kc, Dh, Tmax, (long long)B * Hkv, 128) ||
-      !encode_bf16_map(&mv, vc, Dh, Tmax, (long long)B * Hkv, 128))
+      !encode_bf16_map(&mk, kc, Dh, Tmax, (long long)B * Hkv, keys) ||
+      !encode_bf16_map(&mv, vc, Dh, Tmax, (long long)B * Hkv, keys))
     return cudaErrorInvalidValue;
   DecodeTcParams prm;
   prm.B = B;
@@ -201,8 +202,9 @@ cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, cons
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
-  return Dh == 128 ? launch_tc_dh<128>(mq, mk, mv, prm, dev.device, stream)
-                   : launch_tc_dh<64>(mq, mk, mv, prm, dev.device, stream);
+  return Dh == 256   ? launch_tc_dh<256>(mq, mk, mv, prm, dev.device, stream)
+         : Dh == 128 ? launch_tc_dh<128>(mq, mk, mv, prm, dev.device, stream)
+                     : launch_tc_dh<64>(mq, mk, mv, prm, dev.device, stream);
 }
 
 }  // namespace chs

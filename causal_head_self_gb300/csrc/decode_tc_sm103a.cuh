@@ -7,7 +7,7 @@
 // CUDA-core decode kernel becomes bound by its arithmetic.  Packed together,
 // the group's query rows form a real contraction: S = Q K^T with the group's
 // heads as the M dimension (up to 128 per CTA; fewer rows leave the rest of
-// the tile unused), 128 keys as N, Dh as K, and O = P V.  So this path is the
+// the tile unused), 128 keys (64 at Dh = 256) as N, Dh as K, and O = P V.  So this path is the
 // prefill pipeline reduced to one 128-row sub-tile without a causal mask: a
 // TMA producer streams 128-key K and V tiles of one split of the cache, one
 // warp issues tcgen05.mma (S and P.V accumulate in tensor memory), and the
@@ -17,7 +17,7 @@
 // the same log-sum-exp algebra as the CUDA-core decode.
 //
 // Key tiles are placed so that the split's last tile ends at its last key:
-// tile j starts at position k_end - 128 * (n - j), and only the first tile
+// tile j starts at position k_end - kKeys * (n - j), and only the first tile
 // can reach below k_begin (into earlier, valid cache rows, or below 0 where
 // the copy fills zeros).  Those columns are masked to -inf, so their weights
 // are exactly 0 and every V row the MMA reads is a written cache row (or a
@@ -51,20 +51,26 @@ struct DecodeTcParams {
 
 template <int DH>
 struct DecodeTcCfg {
+  // keys per K/V tile: 128, or 64 at Dh = 256 so that Q (64 KiB) and the two
+  // two-stage rings (32 KiB tiles) fit in shared memory
+  static constexpr int kKeys = DH <= 128 ? 128 : 64;
   static constexpr int kHalves = DH / 64;
-  static constexpr int kBoxBytes = 128 * 64 * 2;     // one 128 x 64 bf16 box
+  static constexpr int kQBoxBytes = 128 * 64 * 2;    // Q box: 128 rows x 64 columns
+  static constexpr int kBoxBytes = kKeys * 64 * 2;   // K/V box: kKeys rows x 64 columns
+  static constexpr int kQBytes = kHalves * kQBoxBytes;
   static constexpr int kTileBytes = kHalves * kBoxBytes;
   static constexpr int kStages = 2;                  // K ring and V ring
   static constexpr int kThreads = 192;               // warps 0-3 softmax, 4 producer, 5 MMA
   static constexpr int kWarpProducer = 4, kWarpIssuer = 5;
-  static constexpr uint32_t kCols = 512;             // S0 [0,128), S1 [128,256), O [256,256+DH)
-  static constexpr uint32_t kColS = 0, kColO = 256;  // S buffer b at kColS + 128 b
+  static constexpr uint32_t kCols = 512;             // S0, S1 (kKeys each), O [256, 256 + DH)
+  static constexpr uint32_t kColS = 0, kColO = 256;  // S buffer b at kColS + kKeys b
+  static_assert(2 * kKeys <= (int)kColO && kColO + DH <= kCols, "tensor-memory columns");
 };
 
 template <int DH>
 struct __align__(1024) DecodeTcSmem {
   using Cfg = DecodeTcCfg<DH>;
-  uint8_t q[Cfg::kTileBytes];
+  uint8_t q[Cfg::kQBytes];
   uint8_t k[Cfg::kStages][Cfg::kTileBytes];
   uint8_t v[Cfg::kStages][Cfg::kTileBytes];
   uint64_t q_full;
@@ -102,14 +108,14 @@ __device__ __forceinline__ void decode_tc_producer(DecodeTcSmem<DH>& sm, const D
                                                    int origin, int ntiles, volatile int* abort) {
   using Cfg = DecodeTcCfg<DH>;
   const uint64_t once = policy_evict_first();   // each cached row is read by one CTA
-  mbar_arrive_expect_tx(&sm.q_full, Cfg::kTileBytes);
+  mbar_arrive_expect_tx(&sm.q_full, Cfg::kQBytes);
   for (int hf = 0; hf < Cfg::kHalves; ++hf)
-    tma_load_3d(sm.q + hf * Cfg::kBoxBytes, map_q, &sm.q_full, hf * 64, 128 * rb, bg);
+    tma_load_3d(sm.q + hf * Cfg::kQBoxBytes, map_q, &sm.q_full, hf * 64, 128 * rb, bg);
   uint32_t k_loaded = 0, k_par = 0, v_loaded = 0, v_par = 0;
   for (int j = 0; j < ntiles; ++j) {
     const int st = j % Cfg::kStages;
     const uint32_t ph = (uint32_t)(j / Cfg::kStages) & 1u;
-    const int row = origin + 128 * j;   // may be negative for the first tile: zeros
+    const int row = origin + Cfg::kKeys * j;   // may be negative for the first tile: zeros
     if (!mbar_wait(&sm.k_empty[st], ph ^ 1u, abort)) break;
     if (p.fault != 3 || j != 0) {   // (the test hook withholds one tile)
       mbar_arrive_expect_tx(&sm.k_full[st], Cfg::kTileBytes);
@@ -145,7 +151,7 @@ template <int DH>
 __device__ __forceinline__ void decode_tc_issuer(DecodeTcSmem<DH>& sm, uint32_t tbase, int ntiles,
                                                  volatile int* abort) {
   using Cfg = DecodeTcCfg<DH>;
-  constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t idesc_qk = idesc_bf16_f32(128, Cfg::kKeys, false, false);
   constexpr uint32_t idesc_pv = idesc_bf16_f32(128, DH, false, true);
   constexpr uint64_t kKmajor = smem_desc_sw128(0, 16, 1024);                // Q, K
   constexpr uint64_t kMnMajor = smem_desc_sw128(0, Cfg::kBoxBytes, 1024);   // V
@@ -158,12 +164,14 @@ __device__ __forceinline__ void decode_tc_issuer(DecodeTcSmem<DH>& sm, uint32_t 
     const uint32_t ph = (uint32_t)(j / Cfg::kStages) & 1u;
     if (!__all_sync(0xffffffffu, mbar_wait(&sm.k_full[st], ph, abort))) return false;
     tc_fence_after_sync();
-    const uint32_t dS = tbase + Cfg::kColS + 128u * (uint32_t)(j & 1);
+    const uint32_t dS = tbase + Cfg::kColS + (uint32_t)Cfg::kKeys * (uint32_t)(j & 1);
     const uint64_t b = dk + (uint64_t)(st * (Cfg::kTileBytes >> 4));
 #pragma unroll
     for (int kk = 0; kk < DH / 16; ++kk) {
-      const uint32_t off = ((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4;
-      mma_bf16_ss_warp(dS, dq + off, b + off, idesc_qk, kk > 0 ? 1u : 0u);
+      // 16 columns (32 bytes) of Dh per MMA; a 64-column box holds 4 steps
+      const uint32_t offq = ((kk / 4) * Cfg::kQBoxBytes + (kk % 4) * 32) >> 4;
+      const uint32_t offk = ((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4;
+      mma_bf16_ss_warp(dS, dq + offq, b + offk, idesc_qk, kk > 0 ? 1u : 0u);
     }
     mma_commit_warp(&sm.s_full[j & 1]);
     mma_commit_warp(&sm.k_empty[st]);
@@ -181,10 +189,10 @@ __device__ __forceinline__ void decode_tc_issuer(DecodeTcSmem<DH>& sm, uint32_t 
       break;
     tc_fence_after_sync();
     // O (+)= P V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
-    const uint32_t dP = tbase + Cfg::kColS + 128u * (uint32_t)(j & 1);
+    const uint32_t dP = tbase + Cfg::kColS + (uint32_t)Cfg::kKeys * (uint32_t)(j & 1);
     const uint64_t b = dv + (uint64_t)(st * (Cfg::kTileBytes >> 4));
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
+    for (int kk = 0; kk < Cfg::kKeys / 16; ++kk)
       mma_bf16_ts_warp(dO, dP + kk * 8, b + kk * (2048 >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
     mma_commit_warp(&sm.pv_done);
     mma_commit_warp(&sm.v_empty[st]);
@@ -215,13 +223,13 @@ __device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const De
   for (int j = 0; j < ntiles; ++j) {
     if (!(ok = mbar_wait(&sm.s_full[j & 1], (uint32_t)(j >> 1) & 1u, abort))) break;
     tc_fence_after_sync();
-    const uint32_t colS = lane_addr + Cfg::kColS + 128u * (uint32_t)(j & 1);
+    const uint32_t colS = lane_addr + Cfg::kColS + (uint32_t)Cfg::kKeys * (uint32_t)(j & 1);
     if (j == 0 && clo0 > 0) {
       // the first tile reaches below the split: its first clo0 columns are
       // not this split's keys (a whole-warp chunk below them is filled
       // without being read; the chunk that straddles is read and masked)
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < Cfg::kKeys; c0 += 32) {
         if (c0 >= clo0) break;
         uint32_t y[32];
         if (c0 + 31 < clo0) {
@@ -233,31 +241,28 @@ __device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const De
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             y[e] = __float_as_uint(keep_if_le(__uint_as_float(y[e]), (uint32_t)(c0 + e - clo0),
-                                              (uint32_t)(127 - clo0)));
+                                              (uint32_t)(Cfg::kKeys - 1 - clo0)));
         }
         tmem_st_32x32b_x32(colS + c0, y);
       }
       tmem_st_wait();
     }
-    uint32_t r0[32], r1[32], r2[32], r3[32];
-    float mc0, mc1, mc2, mc3;
-    tmem_ld_max_32x32b_x32(colS + 0, r0, mc0);
-    tmem_ld_max_32x32b_x32(colS + 32, r1, mc1);
-    tmem_ld_max_32x32b_x32(colS + 64, r2, mc2);
-    tmem_ld_max_32x32b_x32(colS + 96, r3, mc3);
-    tmem_ld_wait(r0, mc0);
-    tmem_ld_wait(r1, mc1);
-    tmem_ld_wait(r2, mc2);
-    tmem_ld_wait(r3, mc3);
-    float x[128];
+    constexpr int kChunks = Cfg::kKeys / 32;
+    uint32_t r[kChunks][32];
+    float mc[kChunks];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      x[c] = __uint_as_float(r0[c]);
-      x[32 + c] = __uint_as_float(r1[c]);
-      x[64 + c] = __uint_as_float(r2[c]);
-      x[96 + c] = __uint_as_float(r3[c]);
-    }
-    const float m_tile = fmaxf(fmaxf(mc0, mc1), fmaxf(mc2, mc3)) * sl2;
+    for (int c = 0; c < kChunks; ++c) tmem_ld_max_32x32b_x32(colS + 32 * c, r[c], mc[c]);
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) tmem_ld_wait(r[c], mc[c]);
+    float x[Cfg::kKeys];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(r[c][e]);
+    float mt = mc[0];
+#pragma unroll
+    for (int c = 1; c < kChunks; ++c) mt = fmaxf(mt, mc[c]);
+    const float m_tile = mt * sl2;
     // lazy maximum (raised only past +8 in log2 units; exact either way)
     const float m_new = fmaxf(m_run, m_tile);
     const bool fresh = m_run == -INFINITY;
@@ -268,7 +273,7 @@ __device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const De
     const float2 scale2 = make_float2(sl2, sl2), neg_m2 = make_float2(-msub, -msub);
     float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
+    for (int c4 = 0; c4 < kChunks; ++c4) {
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
@@ -278,7 +283,7 @@ __device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const De
         ls[e & 1] = __fadd2_rn(ls[e & 1], pp);
         pk[e] = pack_bf16x2(pp.x, pp.y);
       }
-      tmem_st_32x32b_x16(colS + 16 * c4, pk);   // P over the first 64 columns of S
+      tmem_st_32x32b_x16(colS + 16 * c4, pk);   // P over the first kKeys / 2 columns of S
     }
     const float lsum = (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
     // a raised maximum rescales the row's O, once P.V of the previous tile
@@ -350,8 +355,8 @@ __global__ void __launch_bounds__(192, 1)
   int k_begin, k_end;
   decode_tc_range(L, p.window, split, p.chunk, k_begin, k_end);
   if (k_begin >= k_end) return;               // no visible key in this split
-  const int ntiles = (k_end - k_begin + 127) / 128;
-  const int origin = k_end - 128 * ntiles;    // position of the first tile's first key
+  const int ntiles = (k_end - k_begin + Cfg::kKeys - 1) / Cfg::kKeys;
+  const int origin = k_end - Cfg::kKeys * ntiles;   // position of the first tile's first key
   const int rows = min(128, p.G - 128 * rb);  // real query rows of this CTA
   const int active_warps = (rows + 31) / 32;
 

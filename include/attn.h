@@ -157,7 +157,7 @@ int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* 
  * [max(0, seqlens[b] - window), seqlens[b]) (all of them when window <= 0).
  * A seqlens entry outside [1, Tmax] zeroes that sequence's output and latches
  * ATTN_ERR_INVALID_ARG for attn_status().
- * With Hq / Hkv >= 8 (MQA-like groups) and Dh <= 128 the step runs on the tensor cores
+ * With Hq / Hkv >= 8 (MQA-like groups) the step runs on the tensor cores
  * (the group's query heads packed as the rows of one contraction with each
  * key tile) followed by a small combine kernel (a programmatic dependent
  * launch on the same stream); otherwise on the CUDA cores.

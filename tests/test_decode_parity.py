@@ -117,7 +117,7 @@ def test_many_sequences_with_one_key_each():
 
 @pytest.mark.parametrize("B,Hq,Hkv,Tmax,lmin,lmax,window", [
     (3, 8, 2, 3000, 1, 3000, 0),
-    (2, 16, 1, 1000, 900, 1000, 300),   # MQA at Dh 256 stays on the CUDA cores
+    (2, 16, 1, 1000, 900, 1000, 300),   # MQA at Dh 256: the tensor-core path, 64-key tiles
     (2, 4, 4, 700, 1, 700, 0),
 ])
 def test_head_size_256(B, Hq, Hkv, Tmax, lmin, lmax, window):

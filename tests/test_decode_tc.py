@@ -36,6 +36,12 @@ CASES = [
     (3, 64, 4, 300, 128, 1, 300, 0),          # group of 16, short caches
     (2, 32, 1, 20000, 128, 12000, 20000, 0),  # many splits per sequence
     (2, 40, 5, 777, 128, 129, 777, 128),      # window of exactly one tile
+    # head size 256: 64-key tiles
+    (4, 8, 1, 5000, 256, 1, 5000, 0),         # 8 heads on one K/V head, lengths from 1 key up
+    (2, 16, 2, 3000, 256, 200, 3000, 700),    # group of 8, window
+    (1, 200, 1, 1000, 256, 1000, 1000, 0),    # two row blocks
+    (2, 32, 1, 20000, 256, 12000, 20000, 0),  # many splits per sequence
+    (2, 40, 5, 777, 256, 65, 777, 64),        # window of exactly one 64-key tile
 ]
 
 
@@ -57,9 +63,10 @@ def test_tc_path_agrees_with_the_cuda_core_path():
     assert_close(a, b, what="tensor-core vs CUDA-core decode")
 
 
-def test_tc_cache_rows_past_the_length_are_not_read():
+@pytest.mark.parametrize("Dh", [128, 256])
+def test_tc_cache_rows_past_the_length_are_not_read(Dh):
     """NaN in every cache row at or past seqlens[b] must not reach the output."""
-    q, kc, vc, sl = inputs.decode_inputs(2, 32, 1, 1000, 128, 130, 700, seed=62)
+    q, kc, vc, sl = inputs.decode_inputs(2, 32, 1, 1000, Dh, 130, 700, seed=62)
     ref = oracle.decode(q, kc, vc, sl)   # (the oracle touches every row, weighting hidden ones 0)
     for b, L in enumerate(sl.tolist()):
         kc[b, :, L:] = float("nan")
