@@ -160,7 +160,7 @@ static chs::DeviceInfo launch_info(const DeviceState* st) {
 }
 
 int attn_debug_inject_fault(int kind) {
-  if (kind < 0 || kind > 3) return ATTN_ERR_INVALID_ARG;
+  if (kind < 0 || kind > 4) return ATTN_ERR_INVALID_ARG;
   g_fault.store(kind, std::memory_order_relaxed);
   return ATTN_OK;
 }

@@ -77,6 +77,7 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);
   prm.error_word = dev.error_word;
+  prm.fault = dev.fault;
   return Dh == 128 ? launch_bwd_dh<128>(mq, mk, mv, mdo, prm, o, dout, lse, lse2, delta, dev, stream)
                    : launch_bwd_dh<64>(mq, mk, mv, mdo, prm, o, dout, lse, lse2, delta, dev, stream);
 }

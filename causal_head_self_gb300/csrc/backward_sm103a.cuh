@@ -60,6 +60,7 @@ struct BwdParams {
   __nv_bfloat16* dk;      // [B, Hkv, S, DH]
   __nv_bfloat16* dv;      // [B, Hkv, S, DH]
   int* error_word;
+  int fault;              // test hook: 4 = the dK/dV pass never loads its first K/V block
 };
 
 template <int DH>
@@ -235,9 +236,11 @@ __device__ __forceinline__ void bwd_dkdv_producer(BwdKvSmem<DH>& sm, const BwdPa
     const BwdKvItem I = bwd_kv_item_of(p, w);
     if (items > 0 && !(ok = mbar_wait(&sm.kv_empty, (uint32_t)(items - 1) & 1u, abort))) break;
     mbar_arrive_expect_tx(&sm.kv_full, 2 * Cfg::kTile);
-    for (int hf = 0; hf < kBoxes; ++hf) {
-      tma_load_3d(sm.k + hf * Cfg::kBox, map_k, &sm.kv_full, 64 * hf, 128 * I.kb, I.bkv);
-      tma_load_3d(sm.v + hf * Cfg::kBox, map_v, &sm.kv_full, 64 * hf, 128 * I.kb, I.bkv);
+    if (p.fault != 4 || it != 0) {   // (the test hook withholds one K/V block)
+      for (int hf = 0; hf < kBoxes; ++hf) {
+        tma_load_3d(sm.k + hf * Cfg::kBox, map_k, &sm.kv_full, 64 * hf, 128 * I.kb, I.bkv);
+        tma_load_3d(sm.v + hf * Cfg::kBox, map_v, &sm.kv_full, 64 * hf, 128 * I.kb, I.bkv);
+      }
     }
     ++items;
     for (int hh = 0; ok && hh < p.group; ++hh) {

@@ -236,7 +236,7 @@ int attn_status(cudaStream_t stream);
 /*
  * attn_debug_inject_fault -- test hook for the failure path; the pages
  * describe no such call.  Every later attn_fwd / attn_decode /
- * attn_decode_noalloc launch in this process runs with the given fault until
+ * attn_decode_noalloc / attn_bwd launch in this process runs with the given fault until
  * it is reset with kind 0:
  *   0  none (the default)
  *   1  attn_fwd: the producer never loads the first K tile of each CTA's
@@ -245,6 +245,8 @@ int attn_status(cudaStream_t stream);
  *      block of each CTA
  *   3  attn_decode (tensor-core path, Hq / Hkv >= 8): the producer never loads
  *      the first K tile of each CTA
+ *   4  attn_bwd: the dK/dV pass's producer never loads the K/V block of each
+ *      CTA's first work item
  * A faulted launch ends by itself after its waits give up (about 2 s): no
  * GPU fault, trap or hang.  attn_status() then returns ATTN_ERR_TIMEOUT and
  * clears it; the outputs of that launch are undefined, and the next launch
