@@ -311,8 +311,9 @@ def chunk_flops(w):
 def time_next_rows(chs, dev, flush, stream, peaks):
     """The rows beyond the headline step, each on its own workload (median of
     10 launches after 3 warm-ups, L2 flushed before each): chunked prefill,
-    rolling-buffer decode, head size 256 prefill, MQA decode (tensor cores),
-    and the backward pass (2.5x the forward's FLOPs)."""
+    rolling-buffer decode, head size 256 prefill, MQA decode on the tensor
+    cores at head sizes 128 and 256, and the backward pass (2.5x the
+    forward's FLOPs)."""
     out = {}
     bf16, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
 
@@ -358,6 +359,17 @@ def time_next_rows(chs, dev, flush, stream, peaks):
                             "frac_hbm": by / t / 1e9 / hbm,
                             "tflops": decode_flops(w, sl.numpy()) / t / 1e12,
                             "tokens_per_s": w["B"] / t, "ms_per_launch": t * 1e3}
+    del q, kc, vc, sld
+
+    name = "decode_mqa_b16_h8kv1_t32768_d256"
+    w = inputs.WORKLOADS[name]
+    q, kc, vc, sl = inputs.workload_inputs(name)
+    by = decode_bytes(w, sl.numpy())
+    q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
+    t = _time_launches(lambda: chs.attn_decode(q, kc, vc, sld), flush, stream)
+    out["F3_mqa_decode_d256"] = {"workload": name, "value": by / t / 1e9, "unit": "GB/s",
+                                 "frac_hbm": by / t / 1e9 / hbm, "tokens_per_s": w["B"] / t,
+                                 "ms_per_launch": t * 1e3}
     del q, kc, vc, sld
 
     name = "backward_mha_b1_h32_s4096_d128"

@@ -53,6 +53,9 @@ WORKLOADS = {
     # MQA decode: 32 query heads on one K/V head (the tensor-core decode path)
     "decode_mqa_b16_h32kv1_t32768_d128": dict(kind="decode", B=16, Hq=32, Hkv=1, Tmax=32768,
                                               Dh=128, lmin=16384, lmax=32768, window=0, seed=10),
+    # MQA decode at head size 256: 8 query heads on 1 K/V head (the Gemma-2B shape)
+    "decode_mqa_b16_h8kv1_t32768_d256": dict(kind="decode", B=16, Hq=8, Hkv=1, Tmax=32768,
+                                             Dh=256, lmin=16384, lmax=32768, window=0, seed=12),
     # one decode step for 16 sequences against caches of 16384..32768 keys
     "decode_gqa_b16_h32kv8_t32768_d128": dict(kind="decode", B=16, Hq=32, Hkv=8, Tmax=32768,
                                               Dh=128, lmin=16384, lmax=32768, window=0, seed=4),
