@@ -6,8 +6,10 @@
 // kernel does not fit.  This kernel runs one 128-row sub-tile per work item
 // and keeps the tensor core busy differently: S is double-buffered, so the
 // S MMA of the next key tile runs while the softmax works on the current one.
-// Key tiles are 64 keys wide, so that Q (64 KiB) and two-stage K and V rings
-// of 32 KiB tiles fit in shared memory; tensor memory holds S0 [0,64),
+// Key tiles are 64 keys wide, so that Q (64 KiB), a two-stage K ring and a
+// three-stage V ring of 32 KiB tiles fit in shared memory (224 KiB; the third
+// V stage lets a V tile load while the two P.V before it run); tensor memory
+// holds S0 [0,64),
 // S1 [64,128) and O [256,512).  P (bf16) is written over the first 32 columns
 // of its S buffer and read from there by the P.V MMA.
 //
@@ -49,7 +51,8 @@ struct Prefill256Cfg {
   static constexpr int kKBox = kKeys * 64 * 2;         // K/V box: 64 rows x 64 columns
   static constexpr int kQBytes = 4 * kQBox;            // 64 KiB
   static constexpr int kTileBytes = 4 * kKBox;         // 32 KiB
-  static constexpr int kStages = 2;
+  static constexpr int kStagesK = 2;   // K tiles: S(t) is issued two tiles ahead
+  static constexpr int kStagesV = 3;   // V tiles: a third stage hides the load behind two P.V
   static constexpr int kThreads = 192;   // warps 0-3 softmax, 4 producer, 5 MMA issuer
   static constexpr int kWarpProducer = 4, kWarpIssuer = 5;
   static constexpr uint32_t kColS = 0, kColO = 256;    // S buffer b at kColS + 64 b
@@ -58,11 +61,11 @@ struct Prefill256Cfg {
 struct __align__(1024) Prefill256Smem {
   using Cfg = Prefill256Cfg;
   uint8_t q[Cfg::kQBytes];
-  uint8_t k[Cfg::kStages][Cfg::kTileBytes];
-  uint8_t v[Cfg::kStages][Cfg::kTileBytes];
+  uint8_t k[Cfg::kStagesK][Cfg::kTileBytes];
+  uint8_t v[Cfg::kStagesV][Cfg::kTileBytes];
   uint64_t q_full, q_empty;
-  uint64_t k_full[Cfg::kStages], k_empty[Cfg::kStages];
-  uint64_t v_full[Cfg::kStages], v_empty[Cfg::kStages];
+  uint64_t k_full[Cfg::kStagesK], k_empty[Cfg::kStagesK];
+  uint64_t v_full[Cfg::kStagesV], v_empty[Cfg::kStagesV];
   uint64_t s_full[2], p_full[2], pv_done, o_final, mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -140,8 +143,8 @@ __device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Pr
       tma_load_3d(sm.q + hf * Cfg::kQBox, map_q, &sm.q_full, hf * 64, tile.q0, tile.bh);
     ++nq;
     for (int j = tile.lo; j <= tile.hi; ++j, ++t) {
-      const int st = (int)(t % Cfg::kStages);
-      const uint32_t ph = (t / Cfg::kStages) & 1u;
+      const int st = (int)(t % Cfg::kStagesK);
+      const uint32_t ph = (t / Cfg::kStagesK) & 1u;
       if (!(ok = mbar_wait(&sm.k_empty[st], ph ^ 1u, abort))) break;
       mbar_arrive_expect_tx(&sm.k_full[st], Cfg::kTileBytes);
       if (p.fault != 1 || it != 0 || j != tile.lo) {   // (the test hook withholds one tile)
@@ -151,21 +154,23 @@ __device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Pr
       }
       k_loaded |= 1u << st;
       k_par = (k_par & ~(1u << st)) | (ph << st);
-      if (!(ok = mbar_wait(&sm.v_empty[st], ph ^ 1u, abort))) break;
-      mbar_arrive_expect_tx(&sm.v_full[st], Cfg::kTileBytes);
+      const int sv = (int)(t % Cfg::kStagesV);
+      const uint32_t pv = (t / Cfg::kStagesV) & 1u;
+      if (!(ok = mbar_wait(&sm.v_empty[sv], pv ^ 1u, abort))) break;
+      mbar_arrive_expect_tx(&sm.v_full[sv], Cfg::kTileBytes);
       for (int hf = 0; hf < 4; ++hf)
-        tma_load_3d_hint(sm.v[st] + hf * Cfg::kKBox, map_v, &sm.v_full[st], hf * 64, 64 * j,
+        tma_load_3d_hint(sm.v[sv] + hf * Cfg::kKBox, map_v, &sm.v_full[sv], hf * 64, 64 * j,
                          tile.bh_kv, keep);
-      v_loaded |= 1u << st;
-      v_par = (v_par & ~(1u << st)) | (ph << st);
+      v_loaded |= 1u << sv;
+      v_par = (v_par & ~(1u << sv)) | (pv << sv);
     }
   }
   // every copy this thread started has landed before the CTA may exit
   if (nq > 0) mbar_wait_drain_256(&sm.q_full, (uint32_t)(nq - 1) & 1u);
-  for (int i = 0; i < Cfg::kStages; ++i) {
+  for (int i = 0; i < Cfg::kStagesK; ++i)
     if (k_loaded & (1u << i)) mbar_wait_drain_256(&sm.k_full[i], (k_par >> i) & 1u);
+  for (int i = 0; i < Cfg::kStagesV; ++i)
     if (v_loaded & (1u << i)) mbar_wait_drain_256(&sm.v_full[i], (v_par >> i) & 1u);
-  }
 }
 
 // MMA issuer (one converged warp, one elected lane per instruction).  Per
@@ -186,8 +191,8 @@ __device__ __forceinline__ void prefill256_issuer(Prefill256Smem& sm, const Pref
   // the CTA owns all 512 columns, so its allocation starts at column 0
   constexpr uint32_t dO = Cfg::kColO;
   auto issue_s = [&](uint32_t t) -> bool {
-    const int st = (int)(t % Cfg::kStages);
-    const uint32_t ph = (t / Cfg::kStages) & 1u;
+    const int st = (int)(t % Cfg::kStagesK);
+    const uint32_t ph = (t / Cfg::kStagesK) & 1u;
     if (!__all_sync(0xffffffffu, mbar_wait(&sm.k_full[st], ph, abort))) return false;
     tc_fence_after_sync();
     const uint32_t dS = Cfg::kColS + 64u * (t & 1u);
@@ -218,8 +223,8 @@ __device__ __forceinline__ void prefill256_issuer(Prefill256Smem& sm, const Pref
     if (n > 1 && !(ok = issue_s(t + 1))) break;
     if (n <= 2) mma_commit_warp(&sm.q_empty);   // this item's last S is issued
     for (int i = 0; ok && i < n; ++i, ++t) {
-      const int st = (int)(t % Cfg::kStages);
-      const uint32_t ph = (t / Cfg::kStages) & 1u;
+      const int st = (int)(t % Cfg::kStagesV);
+      const uint32_t ph = (t / Cfg::kStagesV) & 1u;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], ph, abort)))) break;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_full[t & 1u], (t >> 1) & 1u, abort))))
         break;
@@ -420,9 +425,11 @@ __global__ void __launch_bounds__(Prefill256Cfg::kThreads, 1)
     sm.abort_flag = 0;
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
-    for (int i = 0; i < Cfg::kStages; ++i) {
+    for (int i = 0; i < Cfg::kStagesK; ++i) {
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], 1);
+    }
+    for (int i = 0; i < Cfg::kStagesV; ++i) {
       mbar_init(&sm.v_full[i], 1);
       mbar_init(&sm.v_empty[i], 1);
     }
