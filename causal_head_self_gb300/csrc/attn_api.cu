@@ -248,7 +248,7 @@ static int decode_common(const void* q, const void* kcache, const void* vcache, 
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
-  if (!ring && Hq / Hkv >= chs::kDecodeTcMinGroup) {
+  if (Hq / Hkv >= chs::kDecodeTcMinGroup) {
     // many query heads per cached byte: the tensor-core path (a contraction)
     const chs::DecodePlan plan = chs::plan_decode_tc(B, Hq, Hkv, Tmax, st->info.num_sms);
     if ((long long)B * Hkv * ((Hq / Hkv + 127) / 128) > 65535) return ATTN_ERR_INVALID_ARG;
@@ -261,8 +261,8 @@ static int decode_common(const void* q, const void* kcache, const void* vcache, 
       partials = st->partials;
     }
     cudaError_t e = chs::launch_decode_tc(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh,
-                                          window, scale_log2, plan, partials, launch_info(st),
-                                          stream);
+                                          window, ring, scale_log2, plan, partials,
+                                          launch_info(st), stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
   const chs::DecodePlan plan = chs::plan_decode(B, Hq, Hkv, Tmax, Dh, st->info.num_sms);
@@ -427,8 +427,8 @@ extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void
       return ATTN_ERR_SCRATCH_LIMIT;
     if ((rc = scratch_ptr(&scratch)) != ATTN_OK) return rc;
     cudaError_t e = chs::launch_decode_tc(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh,
-                                          window, scale_log2, plan, scratch, launch_info(st),
-                                          stream);
+                                          window, 0, scale_log2, plan, scratch,
+                                          launch_info(st), stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
   const chs::DecodePlan plan = chs::plan_decode(B, Hq, Hkv, Tmax, Dh, st->info.num_sms);

@@ -105,6 +105,7 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
   prm.Hkv = Hkv;
   prm.Tmax = Tmax;
   prm.window = window;
+  prm.ring = ring;
   prm.nsplit = plan.nsplit;
   prm.chunk = plan.chunk;
   prm.scale_log2 = scale_log2;
@@ -173,7 +174,7 @@ static cudaError_t launch_tc_dh(const CUtensorMap& mq, const CUtensorMap& mk, co
 
 cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, const int* seqlens,
                              void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,
-                             float scale_log2, const DecodePlan& plan, void* partials,
+                             int ring, float scale_log2, const DecodePlan& plan, void* partials,
                              const DeviceInfo& dev, cudaStream_t stream) {
   const int G = Hq / Hkv;
   CUtensorMap mq, mk, mv;
@@ -189,6 +190,7 @@ cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, cons
   prm.G = G;
   prm.Tmax = Tmax;
   prm.window = window;
+  prm.ring = ring;
   prm.nsplit = plan.nsplit;
   prm.chunk = plan.chunk;
   prm.row_blocks = (G + 127) / 128;

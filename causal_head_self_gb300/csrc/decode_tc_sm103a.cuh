@@ -37,6 +37,7 @@ namespace chs {
 
 struct DecodeTcParams {
   int B, Hq, Hkv, G, Tmax, window;
+  int ring;                 // 1: position t of a sequence sits at cache row t % Tmax
   int nsplit, chunk;        // chunk: keys per split, a multiple of 128
   int row_blocks;           // ceil(G / 128): CTAs per (b, K/V head, split)
   float scale_log2;
@@ -81,12 +82,60 @@ struct __align__(1024) DecodeTcSmem {
   int abort_flag;
 };
 
-// The keys of split `split` of a sequence of L keys: [k_begin, k_end).
-__device__ __forceinline__ void decode_tc_range(int L, int window, int split, int chunk,
+// The first visible position of a sequence of L keys.  In ring mode the
+// cache holds the last Tmax positions, and window <= 0 means a window of Tmax.
+__device__ __forceinline__ int decode_tc_lo(const DecodeTcParams& p, int L) {
+  const int w = p.window > 0 ? p.window : (p.ring ? p.Tmax : 0);
+  return w > 0 ? max(0, L - w) : 0;
+}
+
+// The key positions of split `split` of a sequence of L keys: [k_begin, k_end).
+// Linear caches: splits at multiples of chunk; ring caches: counted from the
+// first visible position.
+__device__ __forceinline__ void decode_tc_range(const DecodeTcParams& p, int L, int split,
                                                 int& k_begin, int& k_end) {
-  const int lo = window > 0 ? max(0, L - window) : 0;
-  k_begin = max(split * chunk, lo);
-  k_end = min((split + 1) * chunk, L);
+  const int lo = decode_tc_lo(p, L);
+  if (p.ring) {
+    k_begin = lo + split * p.chunk;
+    k_end = min(k_begin + p.chunk, L);
+  } else {
+    k_begin = max(split * p.chunk, lo);
+    k_end = min((split + 1) * p.chunk, L);
+  }
+}
+
+// Where a split's keys sit in the cache, as at most two runs of contiguous
+// rows (a ring wraps at most once within a split: its visible positions
+// span at most Tmax), each cut into tiles that end at the run's last row.
+// Tile j < n1 starts at row origin1 + kKeys j, tile j >= n1 at row
+// origin2 + kKeys (j - n1).  Only each run's first tile reaches below the
+// run (rows of other positions, or below row 0 where the copy fills zeros):
+// its first clo1 (resp. clo2) columns are masked.
+struct DecodeTcSpan {
+  int n1, origin1, clo1;
+  int ntiles, origin2, clo2;
+};
+
+template <int KEYS>
+__device__ __forceinline__ DecodeTcSpan decode_tc_span(const DecodeTcParams& p, int k_begin,
+                                                       int k_end) {
+  DecodeTcSpan sp;
+  int r_begin = k_begin, r_end1 = k_end, len2 = 0;
+  if (p.ring) {
+    r_begin = k_begin % p.Tmax;                            // row of the first key
+    const int wrap = k_begin - r_begin + p.Tmax;           // first position back at row 0
+    const int e1 = min(k_end, wrap);
+    r_end1 = r_begin + (e1 - k_begin);
+    len2 = k_end - e1;
+  }
+  sp.n1 = (r_end1 - r_begin + KEYS - 1) / KEYS;
+  sp.origin1 = r_end1 - KEYS * sp.n1;
+  sp.clo1 = r_begin - sp.origin1;
+  const int n2 = (len2 + KEYS - 1) / KEYS;
+  sp.origin2 = len2 - KEYS * n2;
+  sp.clo2 = -sp.origin2;
+  sp.ntiles = sp.n1 + n2;
+  return sp;
 }
 
 // Drain wait used at teardown: ignores the abort flag, bounded by time.
@@ -105,17 +154,18 @@ __device__ __forceinline__ void decode_tc_producer(DecodeTcSmem<DH>& sm, const D
                                                    const CUtensorMap* map_q,
                                                    const CUtensorMap* map_k,
                                                    const CUtensorMap* map_v, int bg, int rb,
-                                                   int origin, int ntiles, volatile int* abort) {
+                                                   const DecodeTcSpan& sp, volatile int* abort) {
   using Cfg = DecodeTcCfg<DH>;
   const uint64_t once = policy_evict_first();   // each cached row is read by one CTA
   mbar_arrive_expect_tx(&sm.q_full, Cfg::kQBytes);
   for (int hf = 0; hf < Cfg::kHalves; ++hf)
     tma_load_3d(sm.q + hf * Cfg::kQBoxBytes, map_q, &sm.q_full, hf * 64, 128 * rb, bg);
   uint32_t k_loaded = 0, k_par = 0, v_loaded = 0, v_par = 0;
-  for (int j = 0; j < ntiles; ++j) {
+  for (int j = 0; j < sp.ntiles; ++j) {
     const int st = j % Cfg::kStages;
     const uint32_t ph = (uint32_t)(j / Cfg::kStages) & 1u;
-    const int row = origin + Cfg::kKeys * j;   // may be negative for the first tile: zeros
+    // may be negative for a run's first tile: zeros
+    const int row = j < sp.n1 ? sp.origin1 + Cfg::kKeys * j : sp.origin2 + Cfg::kKeys * (j - sp.n1);
     if (!mbar_wait(&sm.k_empty[st], ph ^ 1u, abort)) break;
     if (p.fault != 3 || j != 0) {   // (the test hook withholds one tile)
       mbar_arrive_expect_tx(&sm.k_full[st], Cfg::kTileBytes);
@@ -211,8 +261,8 @@ __device__ __forceinline__ void decode_tc_issuer(DecodeTcSmem<DH>& sm, uint32_t 
 template <int DH>
 __device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const DecodeTcParams& p,
                                                   uint32_t tbase, int warp, int lane, int b,
-                                                  int head0, int rows, int split, int clo0,
-                                                  int ntiles, volatile int* abort) {
+                                                  int head0, int rows, int split,
+                                                  const DecodeTcSpan& sp, volatile int* abort) {
   using Cfg = DecodeTcCfg<DH>;
   const int t = warp * 32 + lane;
   const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
@@ -220,12 +270,13 @@ __device__ __forceinline__ void decode_tc_softmax(DecodeTcSmem<DH>& sm, const De
   const float sl2 = p.scale_log2;
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
-  for (int j = 0; j < ntiles; ++j) {
+  for (int j = 0; j < sp.ntiles; ++j) {
     if (!(ok = mbar_wait(&sm.s_full[j & 1], (uint32_t)(j >> 1) & 1u, abort))) break;
     tc_fence_after_sync();
     const uint32_t colS = lane_addr + Cfg::kColS + (uint32_t)Cfg::kKeys * (uint32_t)(j & 1);
-    if (j == 0 && clo0 > 0) {
-      // the first tile reaches below the split: its first clo0 columns are
+    const int clo0 = j == 0 ? sp.clo1 : (j == sp.n1 ? sp.clo2 : 0);
+    if (clo0 > 0) {
+      // a run's first tile reaches below the run: its first clo0 columns are
       // not this split's keys (a whole-warp chunk below them is filled
       // without being read; the chunk that straddles is read and masked)
 #pragma unroll 1
@@ -351,12 +402,12 @@ __global__ void __launch_bounds__(192, 1)
   const int bg = blockIdx.y / p.row_blocks;   // b * Hkv + g
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int L = p.seqlens[b];
-  if (L < 1 || L > p.Tmax) return;            // the combine kernel reports it
+  if (L < 1 || (!p.ring && L > p.Tmax)) return;   // the combine kernel reports it
   int k_begin, k_end;
-  decode_tc_range(L, p.window, split, p.chunk, k_begin, k_end);
+  decode_tc_range(p, L, split, k_begin, k_end);
   if (k_begin >= k_end) return;               // no visible key in this split
-  const int ntiles = (k_end - k_begin + Cfg::kKeys - 1) / Cfg::kKeys;
-  const int origin = k_end - Cfg::kKeys * ntiles;   // position of the first tile's first key
+  const DecodeTcSpan sp = decode_tc_span<Cfg::kKeys>(p, k_begin, k_end);
+  const int ntiles = sp.ntiles;
   const int rows = min(128, p.G - 128 * rb);  // real query rows of this CTA
   const int active_warps = (rows + 31) / 32;
 
@@ -392,13 +443,13 @@ __global__ void __launch_bounds__(192, 1)
       prefetch_tensormap(&map_q);
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
-      decode_tc_producer<DH>(sm, p, &map_q, &map_k, &map_v, bg, rb, origin, ntiles, abort);
+      decode_tc_producer<DH>(sm, p, &map_q, &map_k, &map_v, bg, rb, sp, abort);
     }
   } else if (warp == Cfg::kWarpIssuer) {
     decode_tc_issuer<DH>(sm, tbase, ntiles, abort);
   } else if (warp < active_warps) {
-    decode_tc_softmax<DH>(sm, p, tbase, warp, lane, b, g * p.G + 128 * rb, rows, split,
-                          k_begin - origin, ntiles, abort);
+    decode_tc_softmax<DH>(sm, p, tbase, warp, lane, b, g * p.G + 128 * rb, rows, split, sp,
+                          abort);
   }
 
   __syncwarp();
@@ -426,14 +477,15 @@ __global__ void __launch_bounds__(DH) attn_decode_tc_combine(const DecodeTcParam
   const int b = bh / p.Hq;
   const int d = threadIdx.x;
   const int L = p.seqlens[b];
-  if (L < 1 || L > p.Tmax) {
-    // a sequence length outside [1, Tmax]: zero output, latch the error
+  if (L < 1 || (!p.ring && L > p.Tmax)) {
+    // a sequence length outside [1, Tmax] (ring: below 1): zero output, latch the error
     p.o[(size_t)bh * DH + d] = __float2bfloat16(0.f);
     if (d == 0) atomicExch(p.error_word, 1);   // ATTN_ERR_INVALID_ARG
     return;
   }
-  const int lo = p.window > 0 ? max(0, L - p.window) : 0;
-  const int s_first = lo / p.chunk, s_last = (L - 1) / p.chunk;
+  const int lo = decode_tc_lo(p, L);
+  const int s_first = p.ring ? 0 : lo / p.chunk;
+  const int s_last = p.ring ? (L - 1 - lo) / p.chunk : (L - 1) / p.chunk;
   const float* mp = p.m_part + (size_t)bh * p.nsplit;
   const float* lp = p.l_part + (size_t)bh * p.nsplit;
   const float* op = p.o_part + (size_t)bh * p.nsplit * DH;

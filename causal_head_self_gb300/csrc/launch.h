@@ -71,12 +71,13 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
 
 // Tensor-core decode for large query-head groups (Hq / Hkv >= kDecodeTcMinGroup):
 // splits of whole 128-key tiles, one CTA per (split, b, K/V head, 128 heads),
-// then a combine kernel.  Linear caches only.
+// then a combine kernel.  Linear caches, and rings (ring = 1: position t at
+// row t % Tmax, window <= Tmax, window <= 0 meaning Tmax).
 constexpr int kDecodeTcMinGroup = 8;
 DecodePlan plan_decode_tc(int B, int Hq, int Hkv, int Tmax, int num_sms);
 cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, const int* seqlens,
                              void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,
-                             float scale_log2, const DecodePlan& plan, void* partials,
+                             int ring, float scale_log2, const DecodePlan& plan, void* partials,
                              const DeviceInfo& dev, cudaStream_t stream);
 
 // Backward pass (Dh 64 or 128): dq [B, Hq, S, Dh], dk and dv [B, Hkv, S, Dh]

@@ -55,6 +55,13 @@ CASES = [
     (1, 2, 2, 33, 128, [1000], 0),                     # a ring barely larger than a block
     (2, 8, 2, 500, 256, [1234, 499], 0),               # Dh 256: 16-key stages
     (2, 8, 2, 8192, 128, [8192 * 2 + 5, 9000], 0),     # wrapped, four 2048-key splits to merge
+    # groups of 8 or more query heads: the tensor-core decode on the ring
+    (2, 32, 1, 4096, 128, [4096 * 3 + 17, 5000], 2048), # MQA, window shorter than the ring
+    (3, 16, 2, 1000, 128, [100, 1000, 3333], 0),       # not wrapped, full, wrapped
+    (2, 8, 1, 777, 128, [10000, 777 * 2], 500),        # ring not a multiple of a tile
+    (1, 32, 1, 33, 128, [1000], 0),                    # a ring smaller than one tile
+    (2, 16, 2, 700, 256, [2345, 699], 0),              # Dh 256: 64-key tiles
+    (2, 16, 1, 8192, 64, [8192 * 2 + 5, 9000], 0),     # Dh 64, several splits across the wrap
 ]
 
 
@@ -68,8 +75,9 @@ def test_ring_decode_against_oracle(B, Hq, Hkv, C, Dh, lens, window):
     assert_close(got, ref, what=f"ring {(B, Hq, Hkv, C, Dh, lens, window)}")
 
 
-def test_unwrapped_ring_is_plain_decode_bitwise():
-    q, k, v, kr, vr, sl = _ring_case(3, 8, 2, 2048, 128, [1, 700, 2048], seed=41)
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (32, 1)])   # CUDA-core and tensor-core kernels
+def test_unwrapped_ring_is_plain_decode_bitwise(Hq, Hkv):
+    q, k, v, kr, vr, sl = _ring_case(3, Hq, Hkv, 2048, 128, [1, 700, 2048], seed=41)
     d = torch.device("cuda")
     a = chs.attn_decode(q.to(d), kr.to(d), vr.to(d), sl.to(d))
     b = chs.attn_decode_ring(q.to(d), kr.to(d), vr.to(d), sl.to(d))
