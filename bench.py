@@ -340,6 +340,20 @@ def time_next_rows(chs, dev, flush, stream, peaks):
                              "ms_per_launch": t * 1e3}
     del q, kc, vc, sld
 
+    name = "ring_decode_mqa_b16_h32kv1_c4096_d128"
+    w = inputs.WORKLOADS[name]
+    q, kc, vc, sl = inputs.decode_inputs(w["B"], w["Hq"], w["Hkv"], w["Tmax"], w["Dh"], w["lmin"],
+                                         w["lmax"], w["seed"])
+    q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
+    t = _time_launches(lambda: chs.attn_decode_ring(q, kc, vc, sld, window=w["window"]),
+                       flush, stream)
+    keys = np.minimum(sl.numpy().astype(np.int64), w["window"]).sum()
+    by = keys * w["Hkv"] * w["Dh"] * 2 * 2 + 2 * q.numel() * 2 + sl.numel() * 4
+    out["F2_ring_decode_mqa"] = {"workload": name, "value": by / t / 1e9, "unit": "GB/s",
+                                 "frac_hbm": by / t / 1e9 / hbm, "tokens_per_s": w["B"] / t,
+                                 "ms_per_launch": t * 1e3}
+    del q, kc, vc, sld
+
     name = "prefill_gqa_b1_h16kv8_s8192_d256"
     w = inputs.WORKLOADS[name]
     q, k, v = (x.to(dev) for x in inputs.workload_inputs(name))

@@ -50,6 +50,10 @@ WORKLOADS = {
     "ring_decode_gqa_b16_h32kv8_c4096_d128": dict(kind="ring", B=16, Hq=32, Hkv=8, Tmax=4096,
                                                   Dh=128, lmin=16384, lmax=32768, window=4096,
                                                   seed=9),
+    # the same rolling-buffer decode with 32 query heads on one K/V head (tensor cores)
+    "ring_decode_mqa_b16_h32kv1_c4096_d128": dict(kind="ring", B=16, Hq=32, Hkv=1, Tmax=4096,
+                                                  Dh=128, lmin=16384, lmax=32768, window=4096,
+                                                  seed=13),
     # MQA decode: 32 query heads on one K/V head (the tensor-core decode path)
     "decode_mqa_b16_h32kv1_t32768_d128": dict(kind="decode", B=16, Hq=32, Hkv=1, Tmax=32768,
                                               Dh=128, lmin=16384, lmax=32768, window=0, seed=10),
