@@ -12,8 +12,8 @@ all ranks.  The decode leg is reported beside it in KV-cache GB/s (every
 valid K/V byte counted once, plus q and o) and tokens/s.  L2 is flushed (a
 256 MiB write) before every step, outside the timed kernels.
 
---impl reference times the float64 CPU oracle (the reference this build is
-checked against) on a bounded sample of the same workloads.
+--impl reference times the float64 CPU oracle (the reference the CUDA path
+is checked against) on a bounded sample of the same workloads.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 """
@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -126,11 +127,19 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.tmp = False
 
     def __enter__(self):
-        out_dir = os.path.join(ROOT, "gpurun_out")
-        os.makedirs(out_dir, exist_ok=True)
-        self.path = os.path.join(out_dir, f"clocks_gpu{self.gpu}.csv")
+        # the raw samples go to $CHS_CLOCKS_CSV when it is set (kept for
+        # inspection), otherwise to a temporary file removed after the summary
+        keep = os.environ.get("CHS_CLOCKS_CSV")
+        if keep:
+            self.path = keep.replace("{gpu}", str(self.gpu))
+            self.tmp = False
+        else:
+            fd, self.path = tempfile.mkstemp(prefix=f"clocks_gpu{self.gpu}_", suffix=".csv")
+            os.close(fd)
+            self.tmp = True
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -169,6 +178,9 @@ class ClockSampler:
             for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
+        if self.tmp:
+            os.remove(self.path)
+            self.path = None
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
