@@ -298,7 +298,7 @@ def run_reference(args, rank, world):
     }
 
 
-def _time_launches(fn, flush, stream, iters=10, warmup=3):
+def _time_launches(fn, flush, stream, iters=20, warmup=3):
     """Median CUDA-event time (s) of fn() on `stream`, L2 flushed before each."""
     for _ in range(warmup):
         fn()
@@ -320,9 +320,34 @@ def chunk_flops(w):
     return 4 * w["Dh"] * w["B"] * w["Hq"] * pairs
 
 
+PREFILL_CONFIGS = ("prefill_mha_b1_h32_s4096_d128", "prefill_mha_b1_h32_s4096_d128_noncausal",
+                   "prefill_gqa_b1_h32kv8_s32768_d128_w4096")
+
+
+def time_prefill_configs(chs, dev, flush, stream, peaks):
+    """The larger prefill shapes beside the headline one (median of 20
+    launches after 3 warm-ups, L2 flushed before each): causal MHA at S=4096,
+    its non-causal variant, and windowed GQA at S=32768 (window 4096).
+    TFLOP/s count only the visible (unmasked) pairs."""
+    out = {}
+    for name in PREFILL_CONFIGS:
+        w = inputs.WORKLOADS[name]
+        q, k, v = (x.to(dev) for x in inputs.workload_inputs(name))
+        o = torch.empty_like(q)
+        t = _time_launches(lambda: chs.attn_fwd(q, k, v, o, causal=bool(w["causal"]),
+                                                window=w["window"]), flush, stream)
+        tf = prefill_flops(w) / t / 1e12
+        out[name] = {"value": tf, "unit": "TFLOP/s", "frac_bf16": tf / peaks["bf16_tflops"],
+                     "ms_per_launch": t * 1e3}
+        del q, k, v, o
+    if chs.attn_status() != chs.ATTN_OK:
+        raise RuntimeError("device error while timing the prefill shapes")
+    return out
+
+
 def time_next_rows(chs, dev, flush, stream, peaks):
     """The rows beyond the headline step, each on its own workload (median of
-    10 launches after 3 warm-ups, L2 flushed before each): chunked prefill,
+    20 launches after 3 warm-ups, L2 flushed before each): chunked prefill,
     rolling-buffer decode, head size 256 prefill, MQA decode on the tensor
     cores at head sizes 128 and 256, and the backward pass (2.5x the
     forward's FLOPs)."""
@@ -507,6 +532,7 @@ def run_gpu(args, rank, world, local_rank):
     if rank != 0:
         return None
     del qp, kp, vp, op, qdp, kcp, vcp, slp, odp
+    shapes = time_prefill_configs(chs, dev, flush, stream, read_peaks()[0])
     extras = time_next_rows(chs, dev, flush, stream, read_peaks()[0])
 
     # ---------------------------------------------------------- report
@@ -569,6 +595,7 @@ def run_gpu(args, rank, world, local_rank):
                            "h2d_bytes_per_step": sum(x.numel() * x.element_size()
                                                      for x in (qdh, kch, vch, slh)),
                            "d2h_bytes_per_step": od.numel() * od.element_size()}},
+        "prefill_shapes": shapes,
         "next_rows": extras,
         "gpu_launches": 2 * K,   # one prefill and one decode kernel per step
         "clocks": clocks.summary(),
