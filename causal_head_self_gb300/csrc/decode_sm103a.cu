@@ -111,7 +111,6 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
   prm.scale_log2 = scale_log2;
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
-  prm.ring = ring;
   if (Dh == 256) return launch_hpb<256>(prm, plan.heads_per_cta, dev.device, stream);
   return Dh == 128 ? launch_hpb<128>(prm, plan.heads_per_cta, dev.device, stream)
                    : launch_hpb<64>(prm, plan.heads_per_cta, dev.device, stream);

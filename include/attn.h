@@ -37,6 +37,15 @@
  *   - The same inputs give bit-identical outputs (no atomics in any
  *     reduction; the decode split plan depends only on the arguments and
  *     the device's SM count).
+ *   - Workspaces (the decode split partials and completion counters, the
+ *     backward pass's per-row statistics) belong to the library, one set
+ *     per device, grown under a lock and never shrunk.  They are shared by
+ *     every stream of the device: calls that use them (attn_decode,
+ *     attn_decode_ring, attn_bwd) may be issued from several host threads,
+ *     but must not run concurrently on different streams of one device.
+ *     attn_decode_noalloc works in caller-owned scratch and has no such
+ *     limit.  Growing a workspace is refused inside a stream capture
+ *     (ATTN_ERR_NO_MEMORY): make one call outside the capture first.
  */
 #ifndef CAUSAL_HEAD_SELF_ATTN_H_
 #define CAUSAL_HEAD_SELF_ATTN_H_
