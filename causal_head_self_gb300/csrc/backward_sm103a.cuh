@@ -23,8 +23,10 @@
 //                      them), and dV += P^T dO, dK += dS^T Q accumulate in
 //                      tensor memory (M = 128 keys);
 //   attn_bwd_dq        one CTA per 128-row query block: Q and dO stay, the
-//                      key blocks stream past; S = Q K^T and dP = dO V^T,
-//                      dS as above, dQ += dS K (M = 128 queries).
+//                      key blocks stream past; S = Q K^T and dP = dO V^T
+//                      (two dP buffers, so the next block's S and dP run
+//                      while dS is formed), dS as above, dQ += dS K
+//                      (M = 128 queries).
 // dQ is computed by its own pass (recomputing S and dP) instead of being
 // reduced across key blocks with atomics: 7 MMAs per block pair instead of 5,
 // in exchange for a deterministic result.
@@ -77,6 +79,10 @@ struct BwdCfg {
   static constexpr int kThreads = 32 * (4 * kWG + 2);
   static constexpr int kWarpProducer = 4 * kWG, kWarpIssuer = 4 * kWG + 1;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColA0 = 256, kColA1 = 384;
+  // the dQ pass has one accumulator (dQ at kColA0): its second dP buffer
+  // takes the columns of the dK/dV pass's second accumulator
+  static constexpr uint32_t kColDP1 = kColA1;
+  static_assert(kColA0 + DH <= kColDP1, "dQ accumulator and the second dP buffer");
 };
 
 // Where the bf16 pairs of columns 16 kk .. 16 kk + 15 of a 128-column S or dP
@@ -570,13 +576,16 @@ __global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
 template <int DH>
 struct __align__(1024) BwdQSmem {
   using Cfg = BwdCfg<DH>;
+  static constexpr int kStagesK = 3, kStagesV = 2;
   uint8_t q[Cfg::kTile];           // this item's query block (stays)
   uint8_t dO[Cfg::kTile];          // and its output gradient
-  uint8_t k[2][Cfg::kTile];        // key blocks, two stages
-  uint8_t v[2][Cfg::kTile];        // value blocks
+  uint8_t k[kStagesK][Cfg::kTile];   // key blocks: read by S(n) and dQ(n)
+  uint8_t v[kStagesV][Cfg::kTile];   // value blocks: read by dP(n) only
   uint64_t q_full, q_empty;
-  uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full, s_free, dp_full, ds_full, acc_final, mma_done;
+  uint64_t k_full[kStagesK], k_empty[kStagesK];
+  uint64_t v_full[kStagesV], v_empty[kStagesV];
+  uint64_t s_full, s_free, acc_final, mma_done;
+  uint64_t dp_full[2], ds_full[2];   // per dP / dS buffer
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -605,9 +614,11 @@ __device__ __forceinline__ void bwd_dq_producer(BwdQSmem<DH>& sm, const BwdParam
                                                 const CUtensorMap* map_v,
                                                 const CUtensorMap* map_do, volatile int* abort) {
   using Cfg = BwdCfg<DH>;
+  using Smem = BwdQSmem<DH>;
   constexpr int kBoxes = DH / 64;
   const uint64_t keep = policy_evict_last();   // key blocks are re-read by other query blocks
-  uint32_t u = 0, loaded = 0, par = 0;
+  uint32_t u = 0, k_loaded = 0, k_par = 0, v_loaded = 0, v_par = 0;
+  uint32_t ks = 0, kph = 0;   // K stage and its phase for block u (u % 3, (u / 3) & 1)
   int items = 0;
   bool ok = true;
   for (int it = 0; ok; ++it) {
@@ -622,33 +633,45 @@ __device__ __forceinline__ void bwd_dq_producer(BwdQSmem<DH>& sm, const BwdParam
     }
     ++items;
     for (int kb = I.lo; kb <= I.hi; ++kb, ++u) {
-      const int st = (int)(u & 1u);
-      const uint32_t ph = (u >> 1) & 1u;
-      if (!(ok = mbar_wait(&sm.kv_empty[st], ph ^ 1u, abort))) break;
-      mbar_arrive_expect_tx(&sm.kv_full[st], 2 * Cfg::kTile);
-      for (int hf = 0; hf < kBoxes; ++hf) {
-        tma_load_3d_hint(sm.k[st] + hf * Cfg::kBox, map_k, &sm.kv_full[st], 64 * hf, 128 * kb,
+      if (!(ok = mbar_wait(&sm.k_empty[ks], kph ^ 1u, abort))) break;
+      mbar_arrive_expect_tx(&sm.k_full[ks], Cfg::kTile);
+      for (int hf = 0; hf < kBoxes; ++hf)
+        tma_load_3d_hint(sm.k[ks] + hf * Cfg::kBox, map_k, &sm.k_full[ks], 64 * hf, 128 * kb,
                          I.bkv, keep);
-        tma_load_3d_hint(sm.v[st] + hf * Cfg::kBox, map_v, &sm.kv_full[st], 64 * hf, 128 * kb,
+      k_loaded |= 1u << ks;
+      k_par = (k_par & ~(1u << ks)) | (kph << ks);
+      if (++ks == Smem::kStagesK) { ks = 0; kph ^= 1u; }
+      const uint32_t vs = u & 1u, vph = (u >> 1) & 1u;
+      if (!(ok = mbar_wait(&sm.v_empty[vs], vph ^ 1u, abort))) break;
+      mbar_arrive_expect_tx(&sm.v_full[vs], Cfg::kTile);
+      for (int hf = 0; hf < kBoxes; ++hf)
+        tma_load_3d_hint(sm.v[vs] + hf * Cfg::kBox, map_v, &sm.v_full[vs], 64 * hf, 128 * kb,
                          I.bkv, keep);
-      }
-      loaded |= 1u << st;
-      par = (par & ~(1u << st)) | (ph << st);
+      v_loaded |= 1u << vs;
+      v_par = (v_par & ~(1u << vs)) | (vph << vs);
     }
   }
   if (items > 0) bwd_wait_drain(&sm.q_full, (uint32_t)(items - 1) & 1u);
-  for (int i = 0; i < 2; ++i)
-    if (loaded & (1u << i)) bwd_wait_drain(&sm.kv_full[i], (par >> i) & 1u);
+  for (int i = 0; i < Smem::kStagesK; ++i)
+    if (k_loaded & (1u << i)) bwd_wait_drain(&sm.k_full[i], (k_par >> i) & 1u);
+  for (int i = 0; i < Smem::kStagesV; ++i)
+    if (v_loaded & (1u << i)) bwd_wait_drain(&sm.v_full[i], (v_par >> i) & 1u);
 }
 
 // MMA issue order per item of N key blocks: S(0), dP(0), then per block n:
-// S(n+1) once the element-wise warps have read S(n), dQ(n) once dS(n) is
-// written, dP(n+1) (its columns held dS(n), which dQ(n), issued before it,
-// reads).
+// S(n+1) once the element-wise warps have read S(n), dP(n+1) into the other
+// of two dP buffers, then dQ(n) once dS(n) is written over dP(n).  With two
+// buffers the next block's S and dP run on the tensor core while the
+// element-wise warps turn dP(n) into dS(n), and dQ(n) is the only MMA that
+// waits for them; dP(n+2) reuses dP(n)'s columns after dQ(n), issued before
+// it, has read dS(n) there.  A value block is released when its dP is done,
+// a key block only after dQ: three key stages let block n+2's keys load
+// while blocks n and n+1 are in use.
 template <int DH>
 __device__ __forceinline__ void bwd_dq_issuer(BwdQSmem<DH>& sm, const BwdParams& p,
                                               volatile int* abort) {
   using Cfg = BwdCfg<DH>;
+  using Smem = BwdQSmem<DH>;
   constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t idesc_acc = idesc_bf16_f32(128, DH, false, true);
   constexpr uint64_t kKmajor = smem_desc_sw128(0, 16, 1024);
@@ -679,35 +702,44 @@ __device__ __forceinline__ void bwd_dq_issuer(BwdQSmem<DH>& sm, const BwdParams&
     const int N = I.hi - I.lo + 1;
     if (!(ok = wait_all(&sm.q_full, (uint32_t)items & 1u))) break;
     ++items;
-    if (!(ok = wait_all(&sm.kv_full[u & 1u], (u >> 1) & 1u))) break;
+    // block u (counted across items) uses K stage u % 3, V stage u & 1 and
+    // dP buffer u & 1
+    auto col_dp = [](uint32_t b) { return b ? Cfg::kColDP1 : Cfg::kColDP; };
+    auto kst = [](uint32_t x) { return x % (uint32_t)Smem::kStagesK; };
+    auto kph = [](uint32_t x) { return (x / (uint32_t)Smem::kStagesK) & 1u; };
+    if (!(ok = wait_all(&sm.k_full[kst(u)], kph(u)))) break;
     tc_fence_after_sync();
-    mma_nt(Cfg::kColS, dq_, dk_k + (u & 1u) * kStage);
+    mma_nt(Cfg::kColS, dq_, dk_k + kst(u) * kStage);
     mma_commit_warp(&sm.s_full);
-    mma_nt(Cfg::kColDP, ddo_, dv_k + (u & 1u) * kStage);
-    mma_commit_warp(&sm.dp_full);
+    if (!(ok = wait_all(&sm.v_full[u & 1u], (u >> 1) & 1u))) break;
+    tc_fence_after_sync();
+    mma_nt(col_dp(u & 1u), ddo_, dv_k + (u & 1u) * kStage);
+    mma_commit_warp(&sm.dp_full[u & 1u]);
+    mma_commit_warp(&sm.v_empty[u & 1u]);
     if (N == 1) mma_commit_warp(&sm.q_empty);
     for (int n = 0; n < N; ++n, ++u) {
-      const uint64_t st = u & 1u, st1 = (u + 1) & 1u;
+      const uint32_t st = u & 1u, st1 = (u + 1) & 1u;
       if (n + 1 < N) {
         if (!(ok = wait_all(&sm.s_free, u & 1u))) break;
-        if (!(ok = wait_all(&sm.kv_full[st1], ((u + 1) >> 1) & 1u))) break;
+        if (!(ok = wait_all(&sm.k_full[kst(u + 1)], kph(u + 1)))) break;
         tc_fence_after_sync();
-        mma_nt(Cfg::kColS, dq_, dk_k + st1 * kStage);                    // S(n+1) = Q K^T
+        mma_nt(Cfg::kColS, dq_, dk_k + kst(u + 1) * kStage);             // S(n+1) = Q K^T
         mma_commit_warp(&sm.s_full);
+        if (!(ok = wait_all(&sm.v_full[st1], ((u + 1) >> 1) & 1u))) break;
+        tc_fence_after_sync();
+        mma_nt(col_dp(st1), ddo_, dv_k + st1 * kStage);                  // dP(n+1) = dO V^T
+        mma_commit_warp(&sm.dp_full[st1]);
+        mma_commit_warp(&sm.v_empty[st1]);
+        if (n + 2 == N) mma_commit_warp(&sm.q_empty);
       }
-      if (!(ok = wait_all(&sm.ds_full, u & 1u))) break;
+      if (!(ok = wait_all(&sm.ds_full[st], (u >> 1) & 1u))) break;
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < 128 / 16; ++kk)                              // dQ += dS K
-        mma_bf16_ts_warp(Cfg::kColA0, Cfg::kColDP + bwd_packed_col(kk),
-                         dk_mn + st * kStage + kk * (2048 >> 4),
+        mma_bf16_ts_warp(Cfg::kColA0, col_dp(st) + bwd_packed_col(kk),
+                         dk_mn + kst(u) * kStage + kk * (2048 >> 4),
                          idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_warp(&sm.kv_empty[st]);
-      if (n + 1 < N) {
-        mma_nt(Cfg::kColDP, ddo_, dv_k + st1 * kStage);                  // dP(n+1) = dO V^T
-        mma_commit_warp(&sm.dp_full);
-        if (n + 2 == N) mma_commit_warp(&sm.q_empty);
-      }
+      mma_commit_warp(&sm.k_empty[kst(u)]);
     }
     if (ok) mma_commit_warp(&sm.acc_final);
   }
@@ -729,7 +761,8 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
   const int t = (warp % 4) * 32 + lane;
   const uint32_t lane_addr = tbase + ((uint32_t)((warp % 4) * 32) << 16);
   const uint32_t colS = lane_addr + Cfg::kColS + Cfg::kCols * wg;
-  const uint32_t colDP = lane_addr + Cfg::kColDP + Cfg::kCols * wg;
+  const uint32_t colDP0 = lane_addr + Cfg::kColDP + Cfg::kCols * wg;    // dP buffer 0
+  const uint32_t colDP1 = lane_addr + Cfg::kColDP1 + Cfg::kCols * wg;   // dP buffer 1
   const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
   uint32_t u = 0;
   int items = 0;
@@ -779,7 +812,9 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
         pf[col + 1] = b;
       }
 
-      if (!(ok = mbar_wait(&sm.dp_full, u & 1u, abort))) break;
+      const uint32_t b = u & 1u;   // this block's dP buffer
+      const uint32_t colDP = b ? colDP1 : colDP0;
+      if (!(ok = mbar_wait(&sm.dp_full[b], (u >> 1) & 1u, abort))) break;
       tc_fence_after_sync();
 #pragma unroll
       for (int c = 0; c < Cfg::kChunks; ++c) {
@@ -799,7 +834,7 @@ __device__ __forceinline__ void bwd_dq_softmax(BwdQSmem<DH>& sm, const BwdParams
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&sm.ds_full);
+      mbar_arrive(&sm.ds_full[b]);
     }
     if (!ok) break;
 
@@ -842,14 +877,20 @@ __global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
     sm.abort_flag = 0;
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.kv_full[i], 1);
-      mbar_init(&sm.kv_empty[i], 1);
+    for (int i = 0; i < Smem::kStagesK; ++i) {
+      mbar_init(&sm.k_full[i], 1);
+      mbar_init(&sm.k_empty[i], 1);
+    }
+    for (int i = 0; i < Smem::kStagesV; ++i) {
+      mbar_init(&sm.v_full[i], 1);
+      mbar_init(&sm.v_empty[i], 1);
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_free, Cfg::kEW);
-    mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.ds_full, Cfg::kEW);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.dp_full[i], 1);
+      mbar_init(&sm.ds_full[i], Cfg::kEW);
+    }
     mbar_init(&sm.acc_final, 1);
     mbar_init(&sm.mma_done, 1);
     fence_mbarrier_init();
