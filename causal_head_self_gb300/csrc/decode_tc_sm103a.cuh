@@ -94,14 +94,12 @@ __device__ __forceinline__ int decode_tc_lo(const DecodeTcParams& p, int L) {
 // first visible position.
 __device__ __forceinline__ void decode_tc_range(const DecodeTcParams& p, int L, int split,
                                                 int& k_begin, int& k_end) {
-  const int lo = decode_tc_lo(p, L);
-  if (p.ring) {
-    k_begin = lo + split * p.chunk;
-    k_end = min(k_begin + p.chunk, L);
-  } else {
-    k_begin = max(split * p.chunk, lo);
-    k_end = min((split + 1) * p.chunk, L);
-  }
+  // (64-bit: positions may come within a chunk of 2^31)
+  const long long lo = decode_tc_lo(p, L), c = p.chunk;
+  const long long b = p.ring ? lo + split * c : max(split * c, lo);
+  const long long e = p.ring ? b + c : (split + 1) * c;
+  k_begin = (int)min(b, (long long)L);
+  k_end = (int)min(e, (long long)L);
 }
 
 // Where a split's keys sit in the cache, as at most two runs of contiguous
@@ -123,8 +121,9 @@ __device__ __forceinline__ DecodeTcSpan decode_tc_span(const DecodeTcParams& p, 
   int r_begin = k_begin, r_end1 = k_end, len2 = 0;
   if (p.ring) {
     r_begin = k_begin % p.Tmax;                            // row of the first key
-    const int wrap = k_begin - r_begin + p.Tmax;           // first position back at row 0
-    const int e1 = min(k_end, wrap);
+    // first position back at row 0 (64-bit: it may lie past 2^31 - 1)
+    const long long wrap = (long long)k_begin - r_begin + p.Tmax;
+    const int e1 = (int)min((long long)k_end, wrap);
     r_end1 = r_begin + (e1 - k_begin);
     len2 = k_end - e1;
   }

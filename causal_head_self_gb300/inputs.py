@@ -82,6 +82,19 @@ def prefill_inputs(B, Hq, Hkv, S, Dh, seed):
     return q, k, v
 
 
+def device_normal_bf16(shape, seed, device):
+    """i.i.d. N(0, 1) drawn on `device` by torch's generator, rounded to bf16:
+    for tensors too large to draw on the host.  Drawn one slice of the first
+    two axes at a time, so no full-size float32 copy is ever held."""
+    gen = torch.Generator(device=device).manual_seed(int(seed))
+    out = torch.empty(tuple(shape), dtype=torch.bfloat16, device=device)
+    for i in range(shape[0]):
+        for j in range(shape[1]):
+            out[i, j] = torch.randn(tuple(shape[2:]), generator=gen, device=device,
+                                    dtype=torch.float32).to(torch.bfloat16)
+    return out
+
+
 def grad_inputs(shape, seed):
     """An upstream gradient dL/do of the given shape: i.i.d. N(0, 1), bf16 on
     the host (its own generator, so adding it changes no other draw)."""
