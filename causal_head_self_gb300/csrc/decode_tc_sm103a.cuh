@@ -60,7 +60,7 @@ struct DecodeTcCfg {
   static constexpr int kBoxBytes = kKeys * 64 * 2;   // K/V box: kKeys rows x 64 columns
   static constexpr int kQBytes = kHalves * kQBoxBytes;
   static constexpr int kTileBytes = kHalves * kBoxBytes;
-  static constexpr int kStages = 2;                  // K ring and V ring
+  static constexpr int kStages = DH <= 128 ? 3 : 2;  // K ring and V ring (smem: 224 KiB at Dh 128)
   static constexpr int kThreads = 192;               // warps 0-3 softmax, 4 producer, 5 MMA
   static constexpr int kWarpProducer = 4, kWarpIssuer = 5;
   static constexpr uint32_t kCols = 512;             // S0, S1 (kKeys each), O [256, 256 + DH)
