@@ -43,9 +43,10 @@
  *     every stream of the device: calls that use them (attn_decode,
  *     attn_decode_ring, attn_bwd) may be issued from several host threads,
  *     but must not run concurrently on different streams of one device.
- *     attn_decode_noalloc works in caller-owned scratch and has no such
- *     limit.  Growing a workspace is refused inside a stream capture
- *     (ATTN_ERR_NO_MEMORY): make one call outside the capture first.
+ *     attn_decode_noalloc uses a fixed array of its own instead, under the
+ *     same rule (see there).  Growing a workspace is refused inside a
+ *     stream capture (ATTN_ERR_NO_MEMORY): make one call outside the
+ *     capture first.
  */
 #ifndef CAUSAL_HEAD_SELF_ATTN_H_
 #define CAUSAL_HEAD_SELF_ATTN_H_
@@ -215,8 +216,9 @@ int attn_decode_ring(const void* q, const void* kcache, const void* vcache, cons
  *     16 MiB device array inside this library.  Every GPU that loads the
  *     library holds it until the process exits.
  *   - It runs the kernels attn_decode runs for the same arguments (the
- *     tensor-core path for Hq / Hkv >= 8 and Dh <= 128, the CUDA-core path
- *     otherwise), with the same split plan, so the results are the same bits.
+ *     tensor-core path for Hq / Hkv >= 8 at every head size, the CUDA-core
+ *     path otherwise), with the same split plan, so the results are the
+ *     same bits.
  *   - On the CUDA-core path a call needs 4*B*Hkv*(Hq/Hkv)/h bytes of counters
  *     (h = 4, 2 or 1 query heads per CTA, rounded up to 256 bytes) plus
  *     B*Hq*nsplit*(Dh+2)*4 bytes of partials (each part rounded up to 256),
