@@ -140,14 +140,15 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(prefix=f"clocks_gpu{self.gpu}_", suffix=".csv")
             os.close(fd)
             self.tmp = True
+        self.fh = open(self.path, "w")
         try:
-            self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
-        except OSError:
+        except OSError:   # no nvidia-smi: the summary reports "unsampled"
             self.proc = None
+            self.fh.close()
         time.sleep(0.3)
         return self
 
