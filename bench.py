@@ -140,15 +140,17 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(prefix=f"clocks_gpu{self.gpu}_", suffix=".csv")
             os.close(fd)
             self.tmp = True
-        self.fh = open(self.path, "w")
+        self.fh = None
         try:
+            self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
-        except OSError:   # no nvidia-smi: the summary reports "unsampled"
+        except OSError:   # no nvidia-smi, or no file: the summary reports "unsampled"
             self.proc = None
-            self.fh.close()
+            if self.fh is not None:
+                self.fh.close()
         time.sleep(0.3)
         return self
 
