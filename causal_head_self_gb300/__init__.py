@@ -7,7 +7,7 @@ with its in-kernel log-sum-exp combine, ``attn_bwd`` the backward pass (given
 ``attn_fwd_lse``'s output and log-sum-exps).  There is no CPU or PyTorch fallback: without the
 built library every call raises.
 """
-from ._binding import (ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_NO_MEMORY,  # noqa: F401
+from ._binding import (ATTN_ERR_CHECK, ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_NO_MEMORY,  # noqa: F401
                        ATTN_ERR_SCRATCH_LIMIT, ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED, ATTN_OK,
                        AttnError, attn_bwd, attn_debug_inject_fault, attn_decode,
                        attn_decode_noalloc, attn_decode_ring, attn_fwd, attn_fwd_chunk,

@@ -14,7 +14,11 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libattn_sm103a.so")
+# CHS_ATTN_CHECK=1 selects the range-checked build of the same library
+# (build.build(check=True)); it runs the same kernels with every copy they
+# issue checked, a failed check reported as ATTN_ERR_CHECK
+LIB_PATH = os.path.join(_PKG, "libattn_sm103a_check.so" if os.environ.get("CHS_ATTN_CHECK") == "1"
+                        else "libattn_sm103a.so")
 
 ATTN_OK = 0
 ATTN_ERR_INVALID_ARG = 1
@@ -23,6 +27,7 @@ ATTN_ERR_CUDA = 3
 ATTN_ERR_TIMEOUT = 4
 ATTN_ERR_NO_MEMORY = 5
 ATTN_ERR_SCRATCH_LIMIT = 6
+ATTN_ERR_CHECK = 7
 
 # every symbol include/attn.h declares
 ABI_SYMBOLS = ("attn_fwd", "attn_fwd_lse", "attn_fwd_chunk", "attn_bwd", "attn_decode",

@@ -146,6 +146,7 @@ const char* attn_error_string(int code) {
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
     case ATTN_ERR_NO_MEMORY: return "ATTN_ERR_NO_MEMORY";
     case ATTN_ERR_SCRATCH_LIMIT: return "ATTN_ERR_SCRATCH_LIMIT";
+    case ATTN_ERR_CHECK: return "ATTN_ERR_CHECK";
     default: return "ATTN_ERR_UNKNOWN";
   }
 }

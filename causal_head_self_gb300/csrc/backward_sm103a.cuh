@@ -241,8 +241,12 @@ __device__ __forceinline__ void bwd_dkdv_producer(BwdKvSmem<DH>& sm, const BwdPa
     if (w >= p.num_items) break;
     const BwdKvItem I = bwd_kv_item_of(p, w);
     if (items > 0 && !(ok = mbar_wait(&sm.kv_empty, (uint32_t)(items - 1) & 1u, abort))) break;
-    mbar_arrive_expect_tx(&sm.kv_full, 2 * Cfg::kTile);
-    if (p.fault != 4 || it != 0) {   // (the test hook withholds one K/V block)
+    // (checked builds: a key block of the sequence, of a K/V head of the batch)
+    const bool kv_in_range = attn_check(I.kb >= 0 && 128 * I.kb < p.S && I.bkv >= 0 &&
+                                            I.bkv < p.B * p.Hkv,
+                                        p.error_word);
+    mbar_arrive_expect_tx(&sm.kv_full, kv_in_range ? 2u * Cfg::kTile : 0u);
+    if (kv_in_range && (p.fault != 4 || it != 0)) {   // (the test hook withholds one K/V block)
       for (int hf = 0; hf < kBoxes; ++hf) {
         tma_load_3d(sm.k + hf * Cfg::kBox, map_k, &sm.kv_full, 64 * hf, 128 * I.kb, I.bkv);
         tma_load_3d(sm.v + hf * Cfg::kBox, map_v, &sm.kv_full, 64 * hf, 128 * I.kb, I.bkv);
@@ -255,16 +259,23 @@ __device__ __forceinline__ void bwd_dkdv_producer(BwdKvSmem<DH>& sm, const BwdPa
         const int st = (int)(u & 1u);
         const uint32_t ph = (u >> 1) & 1u;
         if (!(ok = mbar_wait(&sm.q_empty[st], ph ^ 1u, abort))) break;
-        mbar_arrive_expect_tx(&sm.q_full[st], 2 * Cfg::kTile + 2 * 512);
-        for (int hf = 0; hf < kBoxes; ++hf) {
+        const size_t row0 = (size_t)bh * p.S_pad + 128 * qb;
+        // (checked builds: a query block of the sequence, of a query head of
+        // the batch, whose per-row statistics lie inside the workspace)
+        const bool in_range = attn_check(qb >= 0 && 128 * qb < p.S && bh >= 0 && bh < p.B * p.Hq &&
+                                             row0 + 128 <= (size_t)p.B * p.Hq * p.S_pad,
+                                         p.error_word);
+        mbar_arrive_expect_tx(&sm.q_full[st], in_range ? 2u * Cfg::kTile + 2u * 512u : 0u);
+        for (int hf = 0; in_range && hf < kBoxes; ++hf) {
           tma_load_3d_hint(sm.q[st] + hf * Cfg::kBox, map_q, &sm.q_full[st], 64 * hf, 128 * qb, bh,
                            keep);
           tma_load_3d_hint(sm.dO[st] + hf * Cfg::kBox, map_do, &sm.q_full[st], 64 * hf, 128 * qb,
                            bh, keep);
         }
-        const size_t row0 = (size_t)bh * p.S_pad + 128 * qb;
-        bulk_load(sm.lse2[st], p.lse2 + row0, 512, &sm.q_full[st], keep);
-        bulk_load(sm.dlt[st], p.delta + row0, 512, &sm.q_full[st], keep);
+        if (in_range) {
+          bulk_load(sm.lse2[st], p.lse2 + row0, 512, &sm.q_full[st], keep);
+          bulk_load(sm.dlt[st], p.delta + row0, 512, &sm.q_full[st], keep);
+        }
         loaded |= 1u << st;
         par = (par & ~(1u << st)) | (ph << st);
       }
@@ -626,16 +637,25 @@ __device__ __forceinline__ void bwd_dq_producer(BwdQSmem<DH>& sm, const BwdParam
     if (w >= p.num_items) break;
     const BwdQItem I = bwd_q_item_of(p, w);
     if (items > 0 && !(ok = mbar_wait(&sm.q_empty, (uint32_t)(items - 1) & 1u, abort))) break;
-    mbar_arrive_expect_tx(&sm.q_full, 2 * Cfg::kTile);
-    for (int hf = 0; hf < kBoxes; ++hf) {
+    // (checked builds: a query block of the sequence, of a query head of the batch)
+    const bool q_in_range = attn_check(I.qb >= 0 && 128 * I.qb < p.S && I.bh >= 0 &&
+                                           I.bh < p.B * p.Hq,
+                                       p.error_word);
+    mbar_arrive_expect_tx(&sm.q_full, q_in_range ? 2u * Cfg::kTile : 0u);
+    for (int hf = 0; q_in_range && hf < kBoxes; ++hf) {
       tma_load_3d(sm.q + hf * Cfg::kBox, map_q, &sm.q_full, 64 * hf, 128 * I.qb, I.bh);
       tma_load_3d(sm.dO + hf * Cfg::kBox, map_do, &sm.q_full, 64 * hf, 128 * I.qb, I.bh);
     }
     ++items;
     for (int kb = I.lo; kb <= I.hi; ++kb, ++u) {
+      // (checked builds: a key block of the sequence, of a K/V head of the batch)
+      const bool in_range = attn_check(kb >= 0 && 128 * kb < p.S && I.bkv >= 0 &&
+                                           I.bkv < p.B * p.Hkv,
+                                       p.error_word);
+      const uint32_t bytes = in_range ? (uint32_t)Cfg::kTile : 0u;
       if (!(ok = mbar_wait(&sm.k_empty[ks], kph ^ 1u, abort))) break;
-      mbar_arrive_expect_tx(&sm.k_full[ks], Cfg::kTile);
-      for (int hf = 0; hf < kBoxes; ++hf)
+      mbar_arrive_expect_tx(&sm.k_full[ks], bytes);
+      for (int hf = 0; in_range && hf < kBoxes; ++hf)
         tma_load_3d_hint(sm.k[ks] + hf * Cfg::kBox, map_k, &sm.k_full[ks], 64 * hf, 128 * kb,
                          I.bkv, keep);
       k_loaded |= 1u << ks;
@@ -643,8 +663,8 @@ __device__ __forceinline__ void bwd_dq_producer(BwdQSmem<DH>& sm, const BwdParam
       if (++ks == Smem::kStagesK) { ks = 0; kph ^= 1u; }
       const uint32_t vs = u & 1u, vph = (u >> 1) & 1u;
       if (!(ok = mbar_wait(&sm.v_empty[vs], vph ^ 1u, abort))) break;
-      mbar_arrive_expect_tx(&sm.v_full[vs], Cfg::kTile);
-      for (int hf = 0; hf < kBoxes; ++hf)
+      mbar_arrive_expect_tx(&sm.v_full[vs], bytes);
+      for (int hf = 0; in_range && hf < kBoxes; ++hf)
         tma_load_3d_hint(sm.v[vs] + hf * Cfg::kBox, map_v, &sm.v_full[vs], 64 * hf, 128 * kb,
                          I.bkv, keep);
       v_loaded |= 1u << vs;

@@ -239,16 +239,22 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
         const int n = min(BK, nkeys - blk * BK);
         if (!mbar_wait(&sm.empty[st], ph ^ 1, abort)) break;
         if (p.fault != 2 || blk != 0) {   // (the test hook withholds one block)
-          mbar_arrive_expect_tx(&sm.full[st], 2u * n * ROW);
           // a block that runs past the end of a ring continues at row 0
           const int n1 = min(n, p.Tmax - row);
-          bulk_load(sm.k[st], kg + (size_t)row * ROW, n1 * ROW, &sm.full[st], stream_once);
-          bulk_load(sm.v[st], vg + (size_t)row * ROW, n1 * ROW, &sm.full[st], stream_once);
-          if (n1 < n) {   // (offsets in bytes: the stage arrays hold bf16 elements)
-            bulk_load(reinterpret_cast<uint8_t*>(sm.k[st]) + n1 * ROW, kg, (n - n1) * ROW,
-                      &sm.full[st], stream_once);
-            bulk_load(reinterpret_cast<uint8_t*>(sm.v[st]) + n1 * ROW, vg, (n - n1) * ROW,
-                      &sm.full[st], stream_once);
+          // (checked builds: both copies inside the head's Tmax rows)
+          const bool in_range = attn_check(row >= 0 && n >= 1 && n <= BK && n1 >= 1 &&
+                                               (p.ring || n1 == n) && n - n1 <= row,
+                                           p.error_word);
+          mbar_arrive_expect_tx(&sm.full[st], in_range ? 2u * n * ROW : 0u);
+          if (in_range) {
+            bulk_load(sm.k[st], kg + (size_t)row * ROW, n1 * ROW, &sm.full[st], stream_once);
+            bulk_load(sm.v[st], vg + (size_t)row * ROW, n1 * ROW, &sm.full[st], stream_once);
+            if (n1 < n) {   // (offsets in bytes: the stage arrays hold bf16 elements)
+              bulk_load(reinterpret_cast<uint8_t*>(sm.k[st]) + n1 * ROW, kg, (n - n1) * ROW,
+                        &sm.full[st], stream_once);
+              bulk_load(reinterpret_cast<uint8_t*>(sm.v[st]) + n1 * ROW, vg, (n - n1) * ROW,
+                        &sm.full[st], stream_once);
+            }
           }
           loaded |= 1u << st;
           par = (par & ~(1u << st)) | (ph << st);

@@ -165,18 +165,22 @@ __device__ __forceinline__ void decode_tc_producer(DecodeTcSmem<DH>& sm, const D
     const uint32_t ph = (uint32_t)(j / Cfg::kStages) & 1u;
     // may be negative for a run's first tile: zeros
     const int row = j < sp.n1 ? sp.origin1 + Cfg::kKeys * j : sp.origin2 + Cfg::kKeys * (j - sp.n1);
+    // (checked builds: a tile ends inside the cache and starts less than a
+    // tile below row 0)
+    const bool in_range = attn_check(row > -Cfg::kKeys && row + Cfg::kKeys <= p.Tmax, p.error_word);
+    const uint32_t bytes = in_range ? (uint32_t)Cfg::kTileBytes : 0u;
     if (!mbar_wait(&sm.k_empty[st], ph ^ 1u, abort)) break;
     if (p.fault != 3 || j != 0) {   // (the test hook withholds one tile)
-      mbar_arrive_expect_tx(&sm.k_full[st], Cfg::kTileBytes);
-      for (int hf = 0; hf < Cfg::kHalves; ++hf)
+      mbar_arrive_expect_tx(&sm.k_full[st], bytes);
+      for (int hf = 0; in_range && hf < Cfg::kHalves; ++hf)
         tma_load_3d_hint(sm.k[st] + hf * Cfg::kBoxBytes, map_k, &sm.k_full[st], hf * 64, row, bg,
                          once);
       k_loaded |= 1u << st;
       k_par = (k_par & ~(1u << st)) | (ph << st);
     }
     if (!mbar_wait(&sm.v_empty[st], ph ^ 1u, abort)) break;
-    mbar_arrive_expect_tx(&sm.v_full[st], Cfg::kTileBytes);
-    for (int hf = 0; hf < Cfg::kHalves; ++hf)
+    mbar_arrive_expect_tx(&sm.v_full[st], bytes);
+    for (int hf = 0; in_range && hf < Cfg::kHalves; ++hf)
       tma_load_3d_hint(sm.v[st] + hf * Cfg::kBoxBytes, map_v, &sm.v_full[st], hf * 64, row, bg,
                        once);
     v_loaded |= 1u << st;

@@ -138,17 +138,26 @@ __device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Pr
     if (w >= p.num_items) break;
     const Prefill256Tile tile = prefill256_tile_of(p, w);
     if (nq > 0 && !(ok = mbar_wait(&sm.q_empty, (uint32_t)(nq - 1) & 1u, abort))) break;
-    mbar_arrive_expect_tx(&sm.q_full, Cfg::kQBytes);
-    for (int hf = 0; hf < 4; ++hf)
+    // (checked builds: a query row of the chunk and a query head of the batch)
+    const bool q_in_range = attn_check(tile.q0 >= 0 && tile.q0 < p.Sq && tile.bh >= 0 &&
+                                           tile.bh < p.B * p.Hq,
+                                       p.error_word);
+    mbar_arrive_expect_tx(&sm.q_full, q_in_range ? (uint32_t)Cfg::kQBytes : 0u);
+    for (int hf = 0; q_in_range && hf < 4; ++hf)
       tma_load_3d(sm.q + hf * Cfg::kQBox, map_q, &sm.q_full, hf * 64, tile.q0, tile.bh);
     ++nq;
     for (int j = tile.lo; j <= tile.hi; ++j, ++t) {
       const int st = (int)(t % Cfg::kStagesK);
       const uint32_t ph = (t / Cfg::kStagesK) & 1u;
+      // (checked builds: a key tile that starts inside the keys, of a K/V head of the batch)
+      const bool in_range = attn_check(j >= 0 && 64 * j < p.Skv && tile.bh_kv >= 0 &&
+                                           tile.bh_kv < p.B * p.Hkv,
+                                       p.error_word);
+      const uint32_t bytes = in_range ? (uint32_t)Cfg::kTileBytes : 0u;
       if (!(ok = mbar_wait(&sm.k_empty[st], ph ^ 1u, abort))) break;
-      mbar_arrive_expect_tx(&sm.k_full[st], Cfg::kTileBytes);
+      mbar_arrive_expect_tx(&sm.k_full[st], bytes);
       if (p.fault != 1 || it != 0 || j != tile.lo) {   // (the test hook withholds one tile)
-        for (int hf = 0; hf < 4; ++hf)
+        for (int hf = 0; in_range && hf < 4; ++hf)
           tma_load_3d_hint(sm.k[st] + hf * Cfg::kKBox, map_k, &sm.k_full[st], hf * 64, 64 * j,
                            tile.bh_kv, keep);
       }
@@ -157,8 +166,8 @@ __device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Pr
       const int sv = (int)(t % Cfg::kStagesV);
       const uint32_t pv = (t / Cfg::kStagesV) & 1u;
       if (!(ok = mbar_wait(&sm.v_empty[sv], pv ^ 1u, abort))) break;
-      mbar_arrive_expect_tx(&sm.v_full[sv], Cfg::kTileBytes);
-      for (int hf = 0; hf < 4; ++hf)
+      mbar_arrive_expect_tx(&sm.v_full[sv], bytes);
+      for (int hf = 0; in_range && hf < 4; ++hf)
         tma_load_3d_hint(sm.v[sv] + hf * Cfg::kKBox, map_v, &sm.v_full[sv], hf * 64, 64 * j,
                          tile.bh_kv, keep);
       v_loaded |= 1u << sv;

@@ -371,8 +371,12 @@ __device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const Pref
     const PrefillTile& tile = item.tile;
     auto load_q = [&](int s, uint32_t& n) {
       if (n > 0 && !mbar_wait(&sm.q_empty[s], (n - 1) & 1u, abort)) return false;
-      mbar_arrive_expect_tx(&sm.q_full[s], Cfg::kTileBytes);
-      for (int hf = 0; hf < Cfg::kHalves; ++hf)
+      // (checked builds: a query row of the chunk and a query head of the batch)
+      const bool in_range = attn_check(tile.row_first(s) >= 0 && tile.row_first(s) < p.Sq &&
+                                           item.bh >= 0 && item.bh < p.B * p.Hq,
+                                       p.error_word);
+      mbar_arrive_expect_tx(&sm.q_full[s], in_range ? (uint32_t)Cfg::kTileBytes : 0u);
+      for (int hf = 0; in_range && hf < Cfg::kHalves; ++hf)
         tma_load_3d(sm.q[s] + hf * Cfg::kBoxBytes, map_q, &sm.q_full[s], hf * 64,
                     tile.row_first(s), item.bh);
       ++n;
@@ -380,10 +384,15 @@ __device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const Pref
     };
     if (!(ok = load_q(0, nq0))) break;
     for (int j = tile.lo; j <= tile.hi; ++j) {
+      // (checked builds: a key tile that starts inside the keys, of a K/V head of the batch)
+      const bool in_range = attn_check(j >= 0 && 128 * j < tile.Skv && item.bh_kv >= 0 &&
+                                           item.bh_kv < p.B * p.Hkv,
+                                       p.error_word);
+      const uint32_t bytes = in_range ? (uint32_t)Cfg::kTileBytes : 0u;
       if (!(ok = mbar_wait(&sm.k_empty[kst], kph ^ 1, abort))) break;
       if (p.fault != 1 || it != 0 || j != tile.lo) {   // (the test hook withholds one tile)
-        mbar_arrive_expect_tx(&sm.k_full[kst], Cfg::kTileBytes);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+        mbar_arrive_expect_tx(&sm.k_full[kst], bytes);
+        for (int hf = 0; in_range && hf < Cfg::kHalves; ++hf)
           tma_load_3d_hint(sm.k[kst] + hf * Cfg::kBoxBytes, map_k, &sm.k_full[kst], hf * 64,
                            128 * j, item.bh_kv, keep);
         k_loaded |= 1u << kst;
@@ -394,8 +403,8 @@ __device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const Pref
       if (j == tile.lo && tile.valid(1) && !(ok = load_q(1, nq1))) break;
 
       if (!(ok = mbar_wait(&sm.v_empty[vst], vph ^ 1, abort))) break;
-      mbar_arrive_expect_tx(&sm.v_full[vst], Cfg::kTileBytes);
-      for (int hf = 0; hf < Cfg::kHalves; ++hf)
+      mbar_arrive_expect_tx(&sm.v_full[vst], bytes);
+      for (int hf = 0; in_range && hf < Cfg::kHalves; ++hf)
         tma_load_3d_hint(sm.v[vst] + hf * Cfg::kBoxBytes, map_v, &sm.v_full[vst], hf * 64,
                          128 * j, item.bh_kv, keep);
       v_loaded |= 1u << vst;

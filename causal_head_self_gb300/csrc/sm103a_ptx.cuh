@@ -386,6 +386,20 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 // ---------------------------------------------------------------- math helpers
 
+// Range checks of checked builds (compiled with -DATTN_CHECK): a failed
+// check latches ATTN_ERR_CHECK (7) in the device error word and returns
+// false, and the caller skips the copy it was about to issue (arriving on
+// its barrier without bytes, so nothing waits for it).  In normal builds
+// every check is the constant true and costs nothing.
+#ifdef ATTN_CHECK
+__device__ __forceinline__ bool attn_check(bool ok, int* error_word) {
+  if (!ok) atomicCAS(error_word, 0, 7);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool attn_check(bool, int*) { return true; }
+#endif
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

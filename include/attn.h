@@ -64,7 +64,9 @@ typedef enum {
   ATTN_ERR_CUDA = 3,         /* a CUDA runtime or launch error */
   ATTN_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (reported by attn_status) */
   ATTN_ERR_NO_MEMORY = 5,    /* a library workspace could not be allocated */
-  ATTN_ERR_SCRATCH_LIMIT = 6 /* attn_decode_noalloc: the call needs more than its fixed scratch */
+  ATTN_ERR_SCRATCH_LIMIT = 6, /* attn_decode_noalloc: the call needs more than its fixed scratch */
+  ATTN_ERR_CHECK = 7          /* checked builds only (ATTN_CHECK): a kernel's own range check of a
+                                 copy it was about to issue failed; the copy was skipped */
 } attn_status_t;
 
 /*
