@@ -37,9 +37,21 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def test_checked_build_builds_and_exports_every_symbol():
+    # the range-checked variant (-DATTN_CHECK) is a separate library with the same ABI
+    path = _build.build(check=True)
+    assert path.endswith("libattn_sm103a_check.so")
+    checked = ctypes.CDLL(path)
+    for name in _declared_symbols():
+        assert hasattr(checked, name), name
+    checked.attn_error_string.restype = ctypes.c_char_p
+    assert checked.attn_error_string(7) == b"ATTN_ERR_CHECK"
+
+
 def test_error_strings(lib):
     assert _binding.error_string(0) == "ATTN_OK"
     assert _binding.error_string(4) == "ATTN_ERR_TIMEOUT"
+    assert _binding.error_string(_binding.ATTN_ERR_CHECK) == "ATTN_ERR_CHECK"
     assert _binding.error_string(99) == "ATTN_ERR_UNKNOWN"
     assert _binding.version() >> 16 == 1
 
