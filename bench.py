@@ -192,49 +192,108 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def time_oracle(prefill_host, decode_host, w_p, w_d, prefill_heads=None, decode_seqs=None,
-                prefill_rows=None, min_prefill_s=0.0):
-    """Time the float64 oracle on a sample; returns (sample description,
-    prefill TFLOP/s, decode GB/s, seconds, threads).  The prefill sample is
-    repeated until it has run for at least min_prefill_s seconds."""
+def sample_rows(S, n):
+    """n query rows spread evenly over 0..S-1 (first and last included).  The
+    oracle materialises every full score row, so its cost per row does not
+    depend on the row; an even spread also keeps the sample's share of the
+    visible (unmasked) pairs close to its share of the rows."""
+    n = max(1, min(S, n))
+    return np.unique(np.linspace(0, S - 1, n).round().astype(np.int64))
+
+
+def oracle_prefill_rate(w, host, rows=None, heads=None, min_s=0.0):
+    """Time the float64 oracle on a prefill workload `w` (host bf16 q, k, v).
+    rows: query rows evaluated per (b, h) (None: all); heads: query heads
+    evaluated (None: all; the K/V heads they read are kept).  The call is
+    repeated until it has run for min_s seconds.  The whole configuration's
+    time is extrapolated linearly in the evaluated rows (the oracle's cost per
+    row is constant); returns (TFLOP/s over the configuration's visible
+    pairs, seconds spent, sample description)."""
     import oracle
-    q, k, v = prefill_host
-    B, Hq = w_p["B"], w_p["Hq"]
-    heads = prefill_heads or B * Hq
-    bsel = [i // Hq for i in range(heads)]
-    hsel = [i % Hq for i in range(heads)]
-    qs = torch.stack([q[b, h] for b, h in zip(bsel, hsel)])[None]
-    ks = torch.stack([k[b, h] for b, h in zip(bsel, hsel)])[None]
-    vs = torch.stack([v[b, h] for b, h in zip(bsel, hsel)])[None]
-    rows = None if prefill_rows is None else np.arange(w_p["S"] - prefill_rows, w_p["S"])
-    q64, k64, v64 = (x.double().numpy() for x in (qs, ks, vs))
-    reps, tp = 0, 0.0
-    while reps == 0 or tp < min_prefill_s:
-        t0 = time.perf_counter()
-        oracle.attention(q64, k64, v64, causal=w_p["causal"], window=w_p["window"], rows=rows)
-        tp += time.perf_counter() - t0
-        reps += 1
+    q, k, v = host
+    B, Hq, Hkv, S, Dh = w["B"], w["Hq"], w["Hkv"], w["S"], w["Dh"]
+    hsel = list(range(Hq)) if heads is None else list(heads)
+    group = Hq // Hkv
+    if heads is not None:
+        # each chosen query head with its own K/V head: an MHA-shaped sample
+        q = q[:, hsel]
+        k = k[:, [h // group for h in hsel]]
+        v = v[:, [h // group for h in hsel]]
     if rows is None:
-        pflops = 4 * w_p["Dh"] * heads * visible_pairs(w_p["S"], w_p["causal"], w_p["window"])
+        q64 = q.double().numpy()
+        rsel = None
+        nrows = S
     else:
-        pflops = 4 * w_p["Dh"] * heads * int(sum(r + 1 for r in rows))
-    pflops *= reps
-    qd, kc, vc, sl = decode_host
-    nseq = decode_seqs or w_d["B"]
-    Lmax = int(sl[:nseq].max())
-    kc64 = kc[:nseq, :, :Lmax].double().numpy()
-    vc64 = vc[:nseq, :, :Lmax].double().numpy()
-    q64d = qd[:nseq].double().numpy()
-    t0 = time.perf_counter()
-    oracle.decode(q64d, kc64, vc64, sl[:nseq].numpy(), window=w_d["window"])
-    td = time.perf_counter() - t0
-    wd = dict(w_d, B=nseq)
-    dbytes = decode_bytes(wd, sl[:nseq].numpy())
-    sample = (f"prefill {heads} of {B * Hq} (batch, head) pairs"
-              + (f", last {prefill_rows} rows" if rows is not None else ", all rows")
+        rsel = np.asarray(rows, np.int64)
+        nrows = rsel.size
+        # only the sampled rows are filled (and read); the zero pages of the
+        # rest are never touched
+        q64 = np.zeros(tuple(q.shape), np.float64)
+        q64[:, :, rsel] = q[:, :, torch.from_numpy(rsel)].double().numpy()
+    k64, v64 = k.double().numpy(), v.double().numpy()
+    reps, t = 0, 0.0
+    while reps == 0 or t < min_s:
+        t0 = time.perf_counter()
+        oracle.attention(q64, k64, v64, causal=w["causal"], window=w["window"], rows=rsel)
+        t += time.perf_counter() - t0
+        reps += 1
+    frac = (len(hsel) / Hq) * (nrows / S)          # share of the (b, h, row) triples run
+    t_full = t / reps / frac
+    sample = (f"{'all' if heads is None else len(hsel)} of {Hq} query heads x "
+              f"{'all' if rows is None else nrows} of {S} rows"
               + (f", {reps} repetitions" if reps > 1 else "")
-              + f"; decode {nseq} of {w_d['B']} sequences, all heads")
-    return sample, pflops / tp / 1e12, dbytes / td / 1e9, tp + td, oracle.num_threads()
+              + ("" if frac == 1.0 else ", extrapolated linearly in rows"))
+    return prefill_flops(w) / t_full / 1e12, t, sample
+
+
+def oracle_decode_rate(w, host, nseq=None):
+    """Time the float64 oracle on a decode step (all heads of the first nseq
+    sequences); returns (KV-cache GB/s, seconds, sample description)."""
+    import oracle
+    qd, kc, vc, sl = host
+    n = nseq or w["B"]
+    Lmax = int(sl[:n].max())
+    kc64 = kc[:n, :, :Lmax].double().numpy()
+    vc64 = vc[:n, :, :Lmax].double().numpy()
+    q64 = qd[:n].double().numpy()
+    t0 = time.perf_counter()
+    oracle.decode(q64, kc64, vc64, sl[:n].numpy(), window=w["window"])
+    t = time.perf_counter() - t0
+    by = decode_bytes(dict(w, B=n), sl[:n].numpy())
+    return by / t / 1e9, t, f"{n} of {w['B']} sequences, all heads"
+
+
+# The oracle beside every configuration of the target: which rows it runs.
+CPU_PREFILL_SAMPLES = {
+    "prefill_mha_b1_h2_s128_d64": dict(rows=None, heads=None, min_s=0.5),
+    "prefill_mha_b2_h32_s1024_d128": dict(rows=None, heads=None, min_s=3.0),
+    "prefill_mha_b1_h32_s4096_d128": dict(rows=256, heads=None, min_s=0.0),
+    "prefill_mha_b1_h32_s4096_d128_noncausal": dict(rows=256, heads=None, min_s=0.0),
+    "prefill_gqa_b1_h32kv8_s32768_d128_w4096": dict(rows=64, heads=None, min_s=0.0),
+}
+
+
+def cpu_baseline_all(prefill_host=None, decode_host=None):
+    """The float64 oracle on this machine's host cores for every configuration:
+    the two small prefills whole (repeated), the S=4096 prefills on 256 rows
+    per head and the S=32768 windowed prefill on 64 rows per head (each
+    extrapolated linearly in rows), the decode step whole."""
+    import oracle
+    out = {}
+    for name, smp in CPU_PREFILL_SAMPLES.items():
+        w = inputs.WORKLOADS[name]
+        host = prefill_host if (prefill_host is not None and name == PREFILL) \
+            else inputs.workload_inputs(name)
+        rows = None if smp["rows"] is None else sample_rows(w["S"], smp["rows"])
+        tf, sec, sample = oracle_prefill_rate(w, host, rows=rows, heads=smp["heads"],
+                                              min_s=smp["min_s"])
+        out[name] = {"value": tf, "unit": "TFLOP/s", "seconds": sec, "sample": sample}
+        del host
+    wd = inputs.WORKLOADS[DECODE]
+    host = decode_host if decode_host is not None else inputs.workload_inputs(DECODE)
+    gbs, sec, sample = oracle_decode_rate(wd, host)
+    out[DECODE] = {"value": gbs, "unit": "GB/s", "seconds": sec, "sample": sample}
+    return out, oracle.num_threads()
 
 
 # ------------------------------------------------------------------ arms
@@ -261,31 +320,38 @@ def job_rate(work_per_rank, seconds_slowest, world):
 
 
 def run_reference(args, rank, world):
-    """The oracle on the host cores, as the reference arm."""
+    """The oracle on the host cores, as the reference arm: each step runs the
+    headline prefill on query rows spread evenly over the sequence (all
+    heads) and the decode step on one sequence; the row count is sized so the
+    whole run stays within a few minutes."""
     if rank != 0:
         return None
     w_p, w_d = inputs.WORKLOADS[PREFILL], inputs.WORKLOADS[DECODE]
     ph = inputs.workload_inputs(PREFILL)
     dh = inputs.workload_inputs(DECODE)
-    # each step: the last `rows` query rows of one head (the costliest rows of
-    # a causal pass) and one decode sequence; sized so the run stays short
-    budget = max(0.01, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
-    rows = 64
-    _, _, _, sec, _ = time_oracle(ph, dh, w_p, w_d, prefill_heads=1, decode_seqs=1,
-                                  prefill_rows=rows)
-    while sec < 0.5 * budget and rows < w_p["S"]:
-        rows = min(w_p["S"], rows * 2)
-        _, _, _, sec, _ = time_oracle(ph, dh, w_p, w_d, prefill_heads=1, decode_seqs=1,
-                                      prefill_rows=rows)
+    budget = max(0.02, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = 16
+    _, sec, _ = oracle_prefill_rate(w_p, ph, rows=sample_rows(w_p["S"], n))
+    while sec < 0.5 * budget and n < w_p["S"]:
+        n = min(w_p["S"], n * 2)
+        _, sec, _ = oracle_prefill_rate(w_p, ph, rows=sample_rows(w_p["S"], n))
+    rows = None if n >= w_p["S"] else sample_rows(w_p["S"], n)
+
+    def one_step():
+        tf, tp, sample = oracle_prefill_rate(w_p, ph, rows=rows)
+        gbs, td, dsample = oracle_decode_rate(w_d, dh, nseq=1)
+        return tf, gbs, tp + td, f"prefill {sample}; decode {dsample}"
+
     for _ in range(args.warmup):
-        time_oracle(ph, dh, w_p, w_d, prefill_heads=1, decode_seqs=1, prefill_rows=rows)
-    pv, dv, secs = [], [], 0.0
+        one_step()
+    pv, dv, secs, sample = [], [], 0.0, ""
     for _ in range(args.steps):
-        sample, p, d, sec, thr = time_oracle(ph, dh, w_p, w_d, prefill_heads=1, decode_seqs=1,
-                                             prefill_rows=rows)
-        pv.append(p)
-        dv.append(d)
+        tf, gbs, sec, sample = one_step()
+        pv.append(tf)
+        dv.append(gbs)
         secs += sec
+    import oracle
+    thr = oracle.num_threads()
     value = statistics.median(pv)
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
@@ -302,7 +368,9 @@ def run_reference(args, rank, world):
 
 
 def _time_launches(fn, flush, stream, iters=20, warmup=3):
-    """Median CUDA-event time (s) of fn() on `stream`, L2 flushed before each."""
+    """Latency of one isolated launch: fn() between two CUDA events on
+    `stream`, L2 flushed (a 256 MiB write) before each, synchronised after
+    each.  Returns {median, min, max, mean} in seconds over `iters` launches."""
     for _ in range(warmup):
         fn()
     ts = []
@@ -314,7 +382,51 @@ def _time_launches(fn, flush, stream, iters=20, warmup=3):
         e1.record(stream)
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1) / 1e3)
-    return statistics.median(ts)
+    return {"median": statistics.median(ts), "min": min(ts), "max": max(ts),
+            "mean": statistics.mean(ts)}
+
+
+def _time_throughput(fns, stream, iters=20, warmup=3):
+    """Mean time (s) per launch of `iters` launches issued back to back on
+    `stream`, launch i running fns[i % len(fns)] (each on its own copy of the
+    inputs), bracketed by one pair of CUDA events."""
+    for i in range(warmup):
+        fns[i % len(fns)]()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(iters):
+        fns[i % len(fns)]()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / iters
+
+
+def input_sets(set_bytes, l2_bytes, cap=16):
+    """Copies of a launch's inputs to cycle through so that a copy is read
+    again only after at least four L2 capacities of other data have passed:
+    every launch then reads its inputs from DRAM, without a flush."""
+    return max(1, min(cap, math.ceil(4 * l2_bytes / max(1, set_bytes))))
+
+
+def _nbytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts)
+
+
+def _copies(n, *ts):
+    """n sets of device tensors: the given ones, then n - 1 clones."""
+    return [tuple(ts)] + [tuple(t.clone() for t in ts) for _ in range(n - 1)]
+
+
+def _row(work, unit, per_launch, lat, peak=None, **extra):
+    """One timed row: throughput from back-to-back launches, latency beside it."""
+    val = work / per_launch / (1e12 if unit == "TFLOP/s" else 1e9)
+    r = {"value": val, "unit": unit, "ms_per_launch": per_launch * 1e3,
+         "latency_isolated_ms": {k: v * 1e3 for k, v in lat.items()}}
+    if peak is not None:
+        r["frac_bf16" if unit == "TFLOP/s" else "frac_hbm"] = val / peak
+    r.update(extra)
+    return r
 
 
 def chunk_flops(w):
@@ -327,126 +439,123 @@ PREFILL_CONFIGS = ("prefill_mha_b1_h32_s4096_d128", "prefill_mha_b1_h32_s4096_d1
                    "prefill_gqa_b1_h32kv8_s32768_d128_w4096")
 
 
-def time_prefill_configs(chs, dev, flush, stream, peaks):
-    """The larger prefill shapes beside the headline one (median of 20
-    launches after 3 warm-ups, L2 flushed before each): causal MHA at S=4096,
-    its non-causal variant, and windowed GQA at S=32768 (window 4096).
-    TFLOP/s count only the visible (unmasked) pairs."""
+def time_prefill_configs(chs, dev, flush, stream, peaks, l2):
+    """The larger prefill shapes beside the headline one: causal MHA at
+    S=4096, its non-causal variant, and windowed GQA at S=32768 (window
+    4096).  Throughput of 20 back-to-back launches over copies of the inputs
+    that together exceed L2 (3 warm-ups), and the isolated latency (L2
+    flushed before each launch).  TFLOP/s count only the visible pairs."""
     out = {}
     for name in PREFILL_CONFIGS:
         w = inputs.WORKLOADS[name]
         q, k, v = (x.to(dev) for x in inputs.workload_inputs(name))
         o = torch.empty_like(q)
-        t = _time_launches(lambda: chs.attn_fwd(q, k, v, o, causal=bool(w["causal"]),
-                                                window=w["window"]), flush, stream)
-        tf = prefill_flops(w) / t / 1e12
-        out[name] = {"value": tf, "unit": "TFLOP/s", "frac_bf16": tf / peaks["bf16_tflops"],
-                     "ms_per_launch": t * 1e3}
-        del q, k, v, o
+        sets = _copies(input_sets(_nbytes(q, k, v, o), l2), q, k, v, o)
+        fns = [lambda s=s: chs.attn_fwd(*s, causal=bool(w["causal"]), window=w["window"])
+               for s in sets]
+        t = _time_throughput(fns, stream)
+        lat = _time_launches(fns[0], flush, stream)
+        out[name] = _row(prefill_flops(w), "TFLOP/s", t, lat, peaks["bf16_tflops"],
+                         input_copies=len(sets))
+        del q, k, v, o, sets, fns
     if chs.attn_status() != chs.ATTN_OK:
         raise RuntimeError("device error while timing the prefill shapes")
     return out
 
 
-def time_next_rows(chs, dev, flush, stream, peaks):
-    """The rows beyond the headline step, each on its own workload (median of
-    20 launches after 3 warm-ups, L2 flushed before each): chunked prefill,
-    rolling-buffer decode, head size 256 prefill, MQA decode on the tensor
-    cores at head sizes 128 and 256, and the backward pass (2.5x the
-    forward's FLOPs)."""
+def _decode_row(chs, name, dev, flush, stream, peaks, l2, ring):
+    w = inputs.WORKLOADS[name]
+    q, kc, vc, sl = inputs.workload_inputs(name)
+    by = decode_bytes(w, sl.numpy())
+    qd, kcd, vcd, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
+    od = torch.empty_like(qd)
+    sets = _copies(input_sets(_nbytes(qd, kcd, vcd), l2), qd, kcd, vcd, sld, od)
+    call = chs.attn_decode_ring if ring else chs.attn_decode
+    fns = [lambda s=s: call(*s, window=w["window"]) for s in sets]
+    t = _time_throughput(fns, stream)
+    lat = _time_launches(fns[0], flush, stream)
+    return _row(by, "GB/s", t, lat, peaks["hbm_gbs"], workload=name, input_copies=len(sets),
+                tokens_per_s=w["B"] / t, tflops=decode_flops(w, sl.numpy()) / t / 1e12)
+
+
+def time_next_rows(chs, dev, flush, stream, peaks, l2):
+    """The rows beyond the headline step, each on its own workload, timed as
+    the prefill shapes are: chunked prefill, rolling-buffer decode, head size
+    256 prefill, MQA decode on the tensor cores at head sizes 128 and 256,
+    decode at head size 64, and the backward pass (2.5x the forward's FLOPs)."""
     out = {}
-    bf16, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    bf16 = peaks["bf16_tflops"]
 
     name = "chunk_gqa_b2_h32kv8_c1024_at3072_d128"
     w = inputs.WORKLOADS[name]
     q, kc, vc = (x.to(dev) for x in inputs.workload_inputs(name))
-    t = _time_launches(lambda: chs.attn_fwd_chunk(q, kc, vc, w["start"]), flush, stream)
-    tf = chunk_flops(w) / t / 1e12
-    out["F1_chunked_prefill"] = {"workload": name, "value": tf, "unit": "TFLOP/s",
-                                 "frac_bf16": tf / bf16, "ms_per_launch": t * 1e3}
-    del q, kc, vc
+    o = torch.empty_like(q)
+    sets = _copies(input_sets(_nbytes(q, kc, vc, o), l2), q, kc, vc, o)
+    fns = [lambda s=s: chs.attn_fwd_chunk(s[0], s[1], s[2], w["start"], o=s[3]) for s in sets]
+    t = _time_throughput(fns, stream)
+    lat = _time_launches(fns[0], flush, stream)
+    out["F1_chunked_prefill"] = _row(chunk_flops(w), "TFLOP/s", t, lat, bf16, workload=name,
+                                     input_copies=len(sets))
+    del q, kc, vc, o, sets, fns
 
-    name = "ring_decode_gqa_b16_h32kv8_c4096_d128"
-    w = inputs.WORKLOADS[name]
-    q, kc, vc, sl = inputs.decode_inputs(w["B"], w["Hq"], w["Hkv"], w["Tmax"], w["Dh"], w["lmin"],
-                                         w["lmax"], w["seed"])
-    q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
-    t = _time_launches(lambda: chs.attn_decode_ring(q, kc, vc, sld, window=w["window"]),
-                       flush, stream)
-    keys = np.minimum(sl.numpy().astype(np.int64), w["window"]).sum()
-    by = keys * w["Hkv"] * w["Dh"] * 2 * 2 + 2 * q.numel() * 2 + sl.numel() * 4
-    out["F2_ring_decode"] = {"workload": name, "value": by / t / 1e9, "unit": "GB/s",
-                             "frac_hbm": by / t / 1e9 / hbm, "tokens_per_s": w["B"] / t,
-                             "ms_per_launch": t * 1e3}
-    del q, kc, vc, sld
-
-    name = "ring_decode_mqa_b16_h32kv1_c4096_d128"
-    w = inputs.WORKLOADS[name]
-    q, kc, vc, sl = inputs.decode_inputs(w["B"], w["Hq"], w["Hkv"], w["Tmax"], w["Dh"], w["lmin"],
-                                         w["lmax"], w["seed"])
-    q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
-    t = _time_launches(lambda: chs.attn_decode_ring(q, kc, vc, sld, window=w["window"]),
-                       flush, stream)
-    keys = np.minimum(sl.numpy().astype(np.int64), w["window"]).sum()
-    by = keys * w["Hkv"] * w["Dh"] * 2 * 2 + 2 * q.numel() * 2 + sl.numel() * 4
-    out["F2_ring_decode_mqa"] = {"workload": name, "value": by / t / 1e9, "unit": "GB/s",
-                                 "frac_hbm": by / t / 1e9 / hbm, "tokens_per_s": w["B"] / t,
-                                 "ms_per_launch": t * 1e3}
-    del q, kc, vc, sld
+    for key, name, ring in (("F2_ring_decode", "ring_decode_gqa_b16_h32kv8_c4096_d128", True),
+                            ("F2_ring_decode_mqa", "ring_decode_mqa_b16_h32kv1_c4096_d128", True),
+                            ("F3_mqa_decode", "decode_mqa_b16_h32kv1_t32768_d128", False),
+                            ("F3_mqa_decode_d256", "decode_mqa_b16_h8kv1_t32768_d256", False),
+                            ("decode_d64", "decode_gqa_b16_h32kv8_t32768_d64", False)):
+        out[key] = _decode_row(chs, name, dev, flush, stream, peaks, l2, ring)
 
     name = "prefill_gqa_b1_h16kv8_s8192_d256"
     w = inputs.WORKLOADS[name]
     q, k, v = (x.to(dev) for x in inputs.workload_inputs(name))
-    t = _time_launches(lambda: chs.attn_fwd(q, k, v), flush, stream)
-    tf = prefill_flops(w) / t / 1e12
-    out["F3_prefill_d256"] = {"workload": name, "value": tf, "unit": "TFLOP/s",
-                              "frac_bf16": tf / bf16, "ms_per_launch": t * 1e3}
-    del q, k, v
-
-    name = "decode_mqa_b16_h32kv1_t32768_d128"
-    w = inputs.WORKLOADS[name]
-    q, kc, vc, sl = inputs.workload_inputs(name)
-    by = decode_bytes(w, sl.numpy())
-    q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
-    t = _time_launches(lambda: chs.attn_decode(q, kc, vc, sld), flush, stream)
-    out["F3_mqa_decode"] = {"workload": name, "value": by / t / 1e9, "unit": "GB/s",
-                            "frac_hbm": by / t / 1e9 / hbm,
-                            "tflops": decode_flops(w, sl.numpy()) / t / 1e12,
-                            "tokens_per_s": w["B"] / t, "ms_per_launch": t * 1e3}
-    del q, kc, vc, sld
-
-    name = "decode_mqa_b16_h8kv1_t32768_d256"
-    w = inputs.WORKLOADS[name]
-    q, kc, vc, sl = inputs.workload_inputs(name)
-    by = decode_bytes(w, sl.numpy())
-    q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
-    t = _time_launches(lambda: chs.attn_decode(q, kc, vc, sld), flush, stream)
-    out["F3_mqa_decode_d256"] = {"workload": name, "value": by / t / 1e9, "unit": "GB/s",
-                                 "frac_hbm": by / t / 1e9 / hbm, "tokens_per_s": w["B"] / t,
-                                 "ms_per_launch": t * 1e3}
-    del q, kc, vc, sld
+    o = torch.empty_like(q)
+    sets = _copies(input_sets(_nbytes(q, k, v, o), l2), q, k, v, o)
+    fns = [lambda s=s: chs.attn_fwd(*s) for s in sets]
+    t = _time_throughput(fns, stream)
+    lat = _time_launches(fns[0], flush, stream)
+    out["F3_prefill_d256"] = _row(prefill_flops(w), "TFLOP/s", t, lat, bf16, workload=name,
+                                  input_copies=len(sets))
+    del q, k, v, o, sets, fns
 
     name = "backward_mha_b1_h32_s4096_d128"
     w = inputs.WORKLOADS[name]
     q, k, v, do = (x.to(dev) for x in inputs.workload_inputs(name))
     o, lse = chs.attn_fwd_lse(q, k, v)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    t = _time_launches(lambda: chs.attn_bwd(q, k, v, o, do, lse, dq, dk, dv), flush, stream)
+    sets = _copies(input_sets(_nbytes(q, k, v, o, do, dq, dk, dv, lse), l2),
+                   q, k, v, o, do, lse, dq, dk, dv)
+    fns = [lambda s=s: chs.attn_bwd(*s) for s in sets]
+    t = _time_throughput(fns, stream)
+    lat = _time_launches(fns[0], flush, stream)
     fl = 2.5 * 4 * w["Dh"] * w["B"] * w["Hq"] * visible_pairs(w["S"], w["causal"], w["window"])
-    out["F4_backward"] = {"workload": name, "value": fl / t / 1e12, "unit": "TFLOP/s",
-                          "frac_bf16": fl / t / 1e12 / bf16, "ms_per_launch": t * 1e3,
-                          "flops": "2.5 x the forward's (10*Dh per visible pair per head); "
-                                   "the kernels execute 14*Dh (S and dP in both passes)"}
-    del q, k, v, do, o, lse, dq, dk, dv
+    out["F4_backward"] = _row(fl, "TFLOP/s", t, lat, bf16, workload=name,
+                              input_copies=len(sets),
+                              flops="2.5 x the forward's (10*Dh per visible pair per head); "
+                                    "the kernels execute 14*Dh (S and dP in both passes)")
+    del q, k, v, do, o, lse, dq, dk, dv, sets, fns
     if chs.attn_status() != chs.ATTN_OK:
         raise RuntimeError("device error while timing the next rows")
     return out
+
+
+def _host_us_per_call(fn, n=50):
+    """Host time of one library call (argument checks, tensor maps, launch),
+    with the GPU held busy by a sleep kernel so no call waits on the queue."""
+    torch.cuda.synchronize()
+    torch.cuda._sleep(100_000_000)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        fn()
+    t = (time.perf_counter() - t0) / n
+    torch.cuda.synchronize()
+    return t * 1e6
 
 
 def run_gpu(args, rank, world, local_rank):
     import causal_head_self_gb300 as chs
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
     w_p, w_d = inputs.WORKLOADS[PREFILL], inputs.WORKLOADS[DECODE]
     # weak scaling: every rank runs its own batch (seeds differ per rank)
     qh, kh, vh = inputs.prefill_inputs(w_p["B"], w_p["Hq"], w_p["Hkv"], w_p["S"], w_p["Dh"],
@@ -456,6 +565,10 @@ def run_gpu(args, rank, world, local_rank):
                                               rank_seed(w_d["seed"], rank))
     q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
     o = torch.empty_like(q)
+    # the prefill leg cycles through copies of its inputs (64 MiB each) so
+    # that every launch reads them from DRAM; the decode cache (2 GiB) is
+    # larger than L2 by itself
+    psets = _copies(input_sets(_nbytes(q, k, v, o), l2), q, k, v, o)
     qd, kc, vc, sl = qdh.to(dev), kch.to(dev), vch.to(dev), slh.to(dev)
     od = torch.empty_like(qd)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -464,41 +577,56 @@ def run_gpu(args, rank, world, local_rank):
     pf, pb = prefill_flops(w_p), prefill_bytes(w_p)
     db, dfl = decode_bytes(w_d, slh.numpy()), decode_flops(w_d, slh.numpy())
 
-    def step(ev=None):
-        flush.zero_()
-        if ev is not None:
-            ev[0].record(stream)
-        chs.attn_fwd(q, k, v, o, causal=bool(w_p["causal"]), window=w_p["window"])
-        if ev is not None:
-            ev[1].record(stream)
+    def prefill(i):
+        chs.attn_fwd(*psets[i % len(psets)], causal=bool(w_p["causal"]), window=w_p["window"])
+
+    def decode(i):
         chs.attn_decode(qd, kc, vc, sl, od, window=w_d["window"])
-        if ev is not None:
-            ev[2].record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    if chs.attn_status() != chs.ATTN_OK:
-        raise RuntimeError("device error during warm-up")
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
     with ClockSampler(local_rank) as clocks:
+        # warm-up steps right before the timed region (no idle gap between
+        # them); more of them if W steps are too short to bring the clocks up
+        t0 = time.perf_counter()
+        warm = 0
+        while warm < args.warmup or time.perf_counter() - t0 < 0.3:
+            prefill(warm)
+            decode(warm)
+            warm += 1
+            if warm % 8 == 0:
+                torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
+        if chs.attn_status() != chs.ATTN_OK:
+            raise RuntimeError("device error during warm-up")
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        # the K steps: their prefills back to back, then their decodes back
+        # to back; CUDA events at the start, between the legs and at the end
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         t_wall = time.perf_counter()
+        ev[0].record(stream)
         for i in range(args.steps):
-            step(evs[i])
+            prefill(i)
+        ev[1].record(stream)
+        for i in range(args.steps):
+            decode(i)
+        ev[2].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
-    if world > 1:
-        torch.distributed.barrier()
-    status = chs.attn_status()
-    if status != chs.ATTN_OK:
-        raise RuntimeError(f"device error in the timed region: {status}")
-    t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3   # seconds
-    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
-    t_pre, t_dec, t_wall = max_over_ranks([t_pre, t_dec, t_wall], world, dev)
+        if world > 1:
+            torch.distributed.barrier()
+        status = chs.attn_status()
+        if status != chs.ATTN_OK:
+            raise RuntimeError(f"device error in the timed region: {status}")
+        t_pre = ev[0].elapsed_time(ev[1]) / 1e3   # seconds
+        t_dec = ev[1].elapsed_time(ev[2]) / 1e3
+        t_pre, t_dec, t_wall = max_over_ranks([t_pre, t_dec, t_wall], world, dev)
+        # one isolated launch at a time (L2 flushed before each, an event
+        # pair around each): the latency a lone call sees
+        lat_p = _time_launches(lambda: prefill(0), flush, stream)
+        lat_d = _time_launches(lambda: decode(0), flush, stream)
+    host_us = {"attn_fwd": _host_us_per_call(lambda: prefill(0)),
+               "attn_decode": _host_us_per_call(lambda: decode(0))}
 
     # ---------------------------------------------------------- end to end (host buffers)
     e2e_steps = max(3, min(20, args.steps))
@@ -535,12 +663,12 @@ def run_gpu(args, rank, world, local_rank):
     if rank != 0:
         return None
     del qp, kp, vp, op, qdp, kcp, vcp, slp, odp
-    shapes = time_prefill_configs(chs, dev, flush, stream, read_peaks()[0])
-    extras = time_next_rows(chs, dev, flush, stream, read_peaks()[0])
+    peaks, peak_src = read_peaks()
+    shapes = time_prefill_configs(chs, dev, flush, stream, peaks, l2)
+    extras = time_next_rows(chs, dev, flush, stream, peaks, l2)
 
     # ---------------------------------------------------------- report
     K = args.steps
-    peaks, peak_src = read_peaks()
     traffic = read_traffic()
     pre_launch = t_pre / K
     dec_launch = t_dec / K
@@ -564,21 +692,29 @@ def run_gpu(args, rank, world, local_rank):
     # CPU baseline: the oracle on this machine's host cores, N=1 only
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        sample, p_tf, d_gbs, sec, thr = time_oracle((qh, kh, vh), (qdh, kch, vch, slh), w_p, w_d,
-                                                    min_prefill_s=10.0)
-        cpu = {"value": p_tf, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": sample,
-               "seconds": sec, "decode_value": d_gbs, "decode_unit": "GB/s"}
+        per, thr = cpu_baseline_all((qh, kh, vh), (qdh, kch, vch, slh))
+        head = per[PREFILL]
+        cpu = {"value": head["value"], "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"{PREFILL}: {head['sample']}; every configuration in per_config",
+               "decode_value": per[DECODE]["value"], "decode_unit": "GB/s",
+               "seconds": sum(x["seconds"] for x in per.values()), "per_config": per}
 
+    ms = lambda x: {k: v * 1e3 for k, v in x.items()}   # noqa: E731
     return {
-        "impl": "gb300", "metric": METRIC, "value": job_rate(pf, pre_launch, world) / 1e12, "unit": "TFLOP/s",
-        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "impl": "gb300", "metric": METRIC, "value": job_rate(pf, pre_launch, world) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "warmup_steps_run": warm,
         "ms_per_step": (t_pre + t_dec) / K * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {
             "workload": f"{PREFILL} + {DECODE}",
             "prefill": {k: w_p[k] for k in ("B", "Hq", "Hkv", "S", "Dh", "causal", "window")},
             "decode": {k: w_d[k] for k in ("B", "Hq", "Hkv", "Tmax", "Dh", "lmin", "lmax", "window")},
-            "l2": "flushed by a 256 MiB write before every step (outside the timed kernels)",
+            "l2": (f"inputs larger than L2: the prefill leg cycles through {len(psets)} copies "
+                   f"of its inputs ({len(psets) * _nbytes(q, k, v, o) >> 20} MiB); the decode "
+                   f"cache is {_nbytes(kc, vc) >> 20} MiB; no flush inside the timed region"),
+            "timing": ("the K steps' prefills back to back, then their decodes back to back, "
+                       "CUDA events at the start, between the legs and at the end"),
             "parallelism": f"dp{world} (independent batches per GPU)",
         },
         "frac_of_peak": {"prefill_bf16_burst": pre_tflops / peaks["bf16_tflops"],
@@ -588,6 +724,10 @@ def run_gpu(args, rank, world, local_rank):
         "decode": {"value": job_rate(db, dec_launch, world) / 1e9, "unit": "GB/s",
                    "tokens_per_s": w_d["B"] * world / dec_launch,
                    "tflops": dfl / dec_launch / 1e12 * world, "ms_per_launch": dec_launch * 1e3},
+        "latency_isolated_ms": {"note": "one launch at a time, L2 flushed before each, "
+                                        "an event pair around each (20 launches)",
+                                "prefill": ms(lat_p), "decode": ms(lat_d)},
+        "host_us_per_call": host_us,
         "roofline": dominant,
         "rooflines": {"prefill": roof_p, "decode": roof_d},
         "cpu_baseline": cpu,

@@ -117,18 +117,54 @@ bool resolve_scale(float scale, int Dh, float* scale_log2) {
 
 namespace chs {
 
+// A tensor map is a pure function of these arguments, so a call that repeats
+// an earlier one (the usual case: the same buffers every step) takes the map
+// from a small per-thread cache instead of encoding it again.
+namespace {
+struct MapKey {
+  const void* base;
+  long long outer;
+  int Dh, rows, box_rows, stride_rows;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && outer == o.outer && Dh == o.Dh && rows == o.rows &&
+           box_rows == o.box_rows && stride_rows == o.stride_rows;
+  }
+};
+struct MapCache {
+  static constexpr int kEntries = 16;
+  MapKey key[kEntries];
+  alignas(64) CUtensorMap map[kEntries];
+  int used = 0, next = 0;
+};
+thread_local MapCache t_maps;
+}  // namespace
+
 bool encode_bf16_map(CUtensorMap* map, const void* base, int Dh, int rows, long long outer,
                      int box_rows, int stride_rows) {
   if (stride_rows == 0) stride_rows = rows;
   if (rows < 1 || stride_rows < rows) return false;
+  const MapKey key{base, outer, Dh, rows, box_rows, stride_rows};
+  MapCache& c = t_maps;
+  for (int i = 0; i < c.used; ++i) {
+    if (c.key[i] == key) {
+      *map = c.map[i];
+      return true;
+    }
+  }
   cuuint64_t dims[3] = {(cuuint64_t)Dh, (cuuint64_t)rows, (cuuint64_t)outer};
   cuuint64_t strides[2] = {(cuuint64_t)Dh * 2, (cuuint64_t)Dh * 2 * (cuuint64_t)stride_rows};
   cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t elem[3] = {1, 1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                  strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+               box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const int slot = c.next;
+  c.key[slot] = key;
+  c.map[slot] = *map;
+  c.next = (slot + 1) % MapCache::kEntries;
+  if (c.used < MapCache::kEntries) ++c.used;
+  return true;
 }
 
 }  // namespace chs
@@ -224,17 +260,25 @@ int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* 
                     window, scale, stream);
 }
 
-// Shared by attn_decode (ring = 0) and attn_decode_ring (ring = 1).
-static int decode_common(const void* q, const void* kcache, const void* vcache, const int* seqlens,
-                         void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window, int ring,
-                         float scale, cudaStream_t stream) {
+// Argument and aliasing checks of every decode entry point (attn_decode,
+// attn_decode_ring, attn_decode_noalloc), so that all three return the same
+// errors for the same arguments.  On ATTN_OK, *window and *scale_log2 hold
+// the resolved window (0: none) and softmax scale times log2(e); *empty is
+// set when B == 0 (nothing to launch).
+static int decode_check_args(const void* q, const void* kcache, const void* vcache,
+                             const int* seqlens, const void* o, int B, int Hq, int Hkv, int Tmax,
+                             int Dh, int* window, int ring, float scale, float* scale_log2,
+                             bool* empty) {
+  *empty = false;
   if (B < 0 || Tmax < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (Dh != 64 && Dh != 128 && Dh != 256) return ATTN_ERR_UNSUPPORTED;
-  if (window < 0) window = 0;
-  if (ring && window > Tmax) return ATTN_ERR_INVALID_ARG;   // the ring holds Tmax positions
-  float scale_log2 = 0.f;
-  if (!resolve_scale(scale, Dh, &scale_log2)) return ATTN_ERR_INVALID_ARG;
-  if (B == 0) return ATTN_OK;
+  if (*window < 0) *window = 0;
+  if (ring && *window > Tmax) return ATTN_ERR_INVALID_ARG;   // the ring holds Tmax positions
+  if (!resolve_scale(scale, Dh, scale_log2)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
   if (!q || !kcache || !vcache || !seqlens || !o) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(seqlens) & 3u))
@@ -246,8 +290,20 @@ static int decode_common(const void* q, const void* kcache, const void* vcache, 
     return ATTN_ERR_INVALID_ARG;
   if ((long long)B * Hkv * (Hq / Hkv) > 65535LL * 65535LL) return ATTN_ERR_INVALID_ARG;
   if (B > 65535) return ATTN_ERR_INVALID_ARG;   // grid.z
+  return ATTN_OK;
+}
+
+// Shared by attn_decode (ring = 0) and attn_decode_ring (ring = 1).
+static int decode_common(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                         void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window, int ring,
+                         float scale, cudaStream_t stream) {
+  float scale_log2 = 0.f;
+  bool empty = false;
+  int rc = decode_check_args(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, &window, ring,
+                             scale, &scale_log2, &empty);
+  if (rc != ATTN_OK || empty) return rc;
   DeviceState* st = nullptr;
-  int rc = device_state(&st);
+  rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
   if (Hq / Hkv >= chs::kDecodeTcMinGroup) {
     // many query heads per cached byte: the tensor-core path (a contraction)
@@ -386,24 +442,13 @@ unsigned char* g_noalloc_ptr[kMaxDevices] = {};
 extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
                                    const int* seqlens, void* o, int B, int Hq, int Hkv, int Tmax,
                                    int Dh, int window, float scale, cudaStream_t stream) {
-  if (B < 0 || Tmax < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (Dh != 64 && Dh != 128 && Dh != 256) return ATTN_ERR_UNSUPPORTED;
-  if (window < 0) window = 0;
   float scale_log2 = 0.f;
-  if (!resolve_scale(scale, Dh, &scale_log2)) return ATTN_ERR_INVALID_ARG;
-  if (B == 0) return ATTN_OK;
-  if (!q || !kcache || !vcache || !seqlens || !o) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
-      (reinterpret_cast<uintptr_t>(seqlens) & 3u))
-    return ATTN_ERR_INVALID_ARG;
-  const size_t qo_bytes = (size_t)B * Hq * Dh * 2;
-  const size_t kv_bytes = (size_t)B * Hkv * Tmax * Dh * 2;
-  if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, kcache, kv_bytes) ||
-      overlaps(o, qo_bytes, vcache, kv_bytes) || overlaps(o, qo_bytes, seqlens, (size_t)B * 4))
-    return ATTN_ERR_INVALID_ARG;
-  if (B > 65535) return ATTN_ERR_INVALID_ARG;   // grid.z
+  bool empty = false;
+  int rc = decode_check_args(q, kcache, vcache, seqlens, o, B, Hq, Hkv, Tmax, Dh, &window, 0,
+                             scale, &scale_log2, &empty);
+  if (rc != ATTN_OK || empty) return rc;
   DeviceState* st = nullptr;
-  int rc = device_state(&st);
+  rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
   // the fixed array's address, looked up once per device with that device current
   auto scratch_ptr = [&](unsigned char** out) -> int {

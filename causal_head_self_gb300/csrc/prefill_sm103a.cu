@@ -11,23 +11,21 @@ static cudaError_t launch_prefill_dh(const CUtensorMap& mq, const CUtensorMap& m
                                      int num_sms, int device, cudaStream_t stream) {
   constexpr size_t smem = prefill_smem_bytes<DH>();
   static_assert(smem <= 232448, "shared memory budget of one sm_103a CTA");
+  // The warpgroups' register rebalance assumes the kernel was compiled to the
+  // full kRegsLaunch registers per thread; with fewer, the increase could
+  // wait forever, so the launch is refused.  Checked once per device, with
+  // the shared-memory attribute: a device is marked configured only when
+  // both succeed.
   static std::atomic<int> configured[kMaxDevices];
   cudaError_t e = configure_once(configured, device, [] {
+    cudaFuncAttributes fa;
+    cudaError_t r = cudaFuncGetAttributes(&fa, attn_prefill_sm103a<DH>);
+    if (r != cudaSuccess) return r;
+    if (fa.numRegs < PrefillCfg<DH>::kRegsLaunch) return cudaErrorInvalidConfiguration;
     return cudaFuncSetAttribute(attn_prefill_sm103a<DH>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (e != cudaSuccess) return e;
-  // The warpgroups' register rebalance assumes the kernel was compiled to the
-  // full kRegsLaunch registers per thread; with fewer, the increase could
-  // wait forever, so refuse to launch.
-  static int regs = -1;
-  if (regs < 0) {
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_prefill_sm103a<DH>);
-    if (e != cudaSuccess) return e;
-    regs = fa.numRegs;
-  }
-  if (regs < PrefillCfg<DH>::kRegsLaunch) return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM (the shared memory allows no second), each
   // walking its share of the work items
   const int grid = prm.num_items < num_sms ? prm.num_items : num_sms;

@@ -63,6 +63,9 @@ WORKLOADS = {
     # one decode step for 16 sequences against caches of 16384..32768 keys
     "decode_gqa_b16_h32kv8_t32768_d128": dict(kind="decode", B=16, Hq=32, Hkv=8, Tmax=32768,
                                               Dh=128, lmin=16384, lmax=32768, window=0, seed=4),
+    # the same decode step at head size 64
+    "decode_gqa_b16_h32kv8_t32768_d64": dict(kind="decode", B=16, Hq=32, Hkv=8, Tmax=32768,
+                                             Dh=64, lmin=16384, lmax=32768, window=0, seed=14),
     # the same decode step for 4 sequences (0.5 GB of cache: a profiler-sized case)
     "decode_gqa_b4_h32kv8_t32768_d128": dict(kind="decode", B=4, Hq=32, Hkv=8, Tmax=32768,
                                              Dh=128, lmin=16384, lmax=32768, window=0, seed=5),

@@ -49,14 +49,23 @@ def test_noalloc_matches_decode_on_two_calls(B, Hq, Hkv, Tmax, Dh, lmin, lmax, w
         assert (o.float().cpu().numpy() == ref).all()
 
 
+SCRATCH_BYTES = 16 << 20   # the fixed array's size, as the header states
+
+
 def test_noalloc_rejects_a_call_beyond_its_scratch():
-    """B=256 sequences of a 32768-key cache need more than the 16 MiB scratch;
-    the call is refused before anything is launched (the pointers are never
-    dereferenced)."""
+    """A call whose split partials cannot fit the 16 MiB scratch is refused
+    before anything is launched, so its pointers are never dereferenced.
+    The shape is chosen so that even a single split per sequence needs more
+    than the scratch (the header's formula: B*Hq*nsplit*(Dh+2)*4 bytes of
+    partials, nsplit >= 1), whatever split plan the library picks; the
+    assertion below checks that on the host before the call is made."""
+    B, Hq, Hkv, Tmax, Dh = 2048, 32, 8, 64, 128
+    min_partials = B * Hq * 1 * (Dh + 2) * 4
+    assert min_partials > SCRATCH_BYTES, "the refusal must not depend on the split plan"
     lib = _binding.load()
     torch.cuda.init()
     big = 1 << 40
-    rc = lib.attn_decode_noalloc(0x10000, big, 2 * big, 3 * big, 4 * big, 256, 32, 8, 32768, 128,
+    rc = lib.attn_decode_noalloc(0x10000, big, 2 * big, 3 * big, 4 * big, B, Hq, Hkv, Tmax, Dh,
                                  0, 0.0, None)
     assert rc == chs.ATTN_ERR_SCRATCH_LIMIT
     assert chs.error_string(rc) == "ATTN_ERR_SCRATCH_LIMIT"
