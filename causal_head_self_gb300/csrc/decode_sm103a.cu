@@ -73,8 +73,9 @@ static cudaError_t launch_dh(const DecodeParams& prm, int device, cudaStream_t s
   if (e != cudaSuccess) return e;
   const int groups = (prm.Hq / prm.Hkv) / HPB;
   dim3 grid(prm.Hkv * groups, prm.nsplit, prm.B);
-  kernel<<<grid, kDecodeThreads, smem, stream>>>(prm);
-  return cudaGetLastError();
+  // a programmatic dependent launch: its launch overlaps the previous
+  // kernel's tail (each CTA waits for that kernel before reading memory)
+  return launch_pdl(kernel, grid, dim3(kDecodeThreads), smem, stream, prm);
 }
 
 template <int DH>
@@ -152,8 +153,8 @@ static cudaError_t launch_tc_dh(const CUtensorMap& mq, const CUtensorMap& mk, co
   });
   if (e != cudaSuccess) return e;
   dim3 grid(prm.nsplit, prm.B * prm.Hkv * prm.row_blocks);
-  attn_decode_tc_sm103a<DH><<<grid, DecodeTcCfg<DH>::kThreads, smem, stream>>>(mq, mk, mv, prm);
-  e = cudaGetLastError();
+  e = launch_pdl(attn_decode_tc_sm103a<DH>, grid, dim3(DecodeTcCfg<DH>::kThreads), smem, stream,
+                 mq, mk, mv, prm);
   if (e != cudaSuccess) return e;
   // the combine kernel is a programmatic dependent launch: it is scheduled as
   // the decode CTAs finish and waits on the grid dependency, so its launch

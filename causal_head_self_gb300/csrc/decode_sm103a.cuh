@@ -187,6 +187,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                       ~uintptr_t(127));
   volatile int* abort = &sm.abort_flag;
+  // the lengths and the cache may come from the previous kernel in the
+  // stream: wait for it before the first global read (a no-op unless this
+  // launch is a programmatic dependent)
+  griddep_wait();
 
   // grid (head groups, splits, B): the CTAs of one split -- the query-head
   // groups that read the same K/V rows when Hq / Hkv exceeds 4 (MQA) -- are

@@ -399,6 +399,10 @@ __global__ void __launch_bounds__(192, 1)
                                       ~uintptr_t(1023));
   volatile int* abort = &sm.abort_flag;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // the lengths and the cache may come from the previous kernel in the
+  // stream: wait for it before the first global read (a no-op unless this
+  // launch is a programmatic dependent)
+  griddep_wait();
 
   const int split = blockIdx.x;
   const int rb = blockIdx.y % p.row_blocks;
@@ -465,7 +469,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0 && sm.abort_flag) atomicExch(p.error_word, 4);   // ATTN_ERR_TIMEOUT
   // this CTA's partials are written: the combine grid may be scheduled (it
   // still waits for this whole grid to finish before reading them)
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) griddep_launch_dependents();
 }
 
 // Merge the splits of one (b, query head): o = sum_s 2^(m_s - M) o_s /
@@ -475,7 +479,7 @@ template <int DH>
 __global__ void __launch_bounds__(DH) attn_decode_tc_combine(const DecodeTcParams p) {
   // launched as a programmatic dependent of attn_decode_tc_sm103a: wait until
   // that grid has completed and its writes are visible
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  griddep_wait();
   const int bh = blockIdx.x;
   const int b = bh / p.Hq;
   const int d = threadIdx.x;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <atomic>
+#include <utility>
 
 #include <cstdint>
 #include <cuda.h>
@@ -20,6 +21,25 @@ inline cudaError_t configure_once(std::atomic<int>* flags, int device, F&& set) 
   const cudaError_t e = set();
   if (e == cudaSuccess && tracked) flags[device].store(1, std::memory_order_release);
   return e;
+}
+
+// Launch `kernel` on `stream` as a programmatic dependent of the kernel
+// before it: its CTAs may be scheduled while that kernel finishes, and each
+// waits (griddep_wait) for it to complete before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 struct DeviceInfo {

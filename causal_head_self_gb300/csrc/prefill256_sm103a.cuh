@@ -458,6 +458,11 @@ __global__ void __launch_bounds__(Prefill256Cfg::kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // global memory only after the previous kernel in the stream is complete;
+  // this grid (one CTA per SM, all of its shared memory) leaves the next
+  // kernel nothing to take, so it may be launched now
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const uint32_t tbase = sm.tmem_base;
   // the issuer's tensor-memory addresses are compile-time: all 512 columns
   // are this CTA's, so the allocation must start at column 0

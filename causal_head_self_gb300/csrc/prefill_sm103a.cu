@@ -29,8 +29,9 @@ static cudaError_t launch_prefill_dh(const CUtensorMap& mq, const CUtensorMap& m
   // persistent: one CTA per SM (the shared memory allows no second), each
   // walking its share of the work items
   const int grid = prm.num_items < num_sms ? prm.num_items : num_sms;
-  attn_prefill_sm103a<DH><<<grid, PrefillCfg<DH>::kThreads, smem, stream>>>(mq, mk, mv, prm);
-  return cudaGetLastError();
+  // a programmatic dependent launch: set-up overlaps the previous kernel's tail
+  return launch_pdl(attn_prefill_sm103a<DH>, dim3(grid), dim3(PrefillCfg<DH>::kThreads), smem,
+                    stream, mq, mk, mv, prm);
 }
 
 // Multiplier and shift for FastDiv (exact for dividends below 2^31).
@@ -84,8 +85,8 @@ static cudaError_t launch_prefill256(const void* q, const void* k, const void* v
   });
   if (e != cudaSuccess) return e;
   const int grid = prm.num_items < dev.num_sms ? prm.num_items : dev.num_sms;
-  attn_prefill256_sm103a<<<grid, Cfg::kThreads, smem, stream>>>(mq, mk, mv, prm);
-  return cudaGetLastError();
+  return launch_pdl(attn_prefill256_sm103a, dim3(grid), dim3(Cfg::kThreads), smem, stream, mq,
+                    mk, mv, prm);
 }
 
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,

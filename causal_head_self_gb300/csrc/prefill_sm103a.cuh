@@ -662,6 +662,13 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // Set-up touched only shared memory, tensor memory and the parameters:
+  // global memory waits for the previous kernel in the stream (a no-op
+  // unless this launch is a programmatic dependent).  One CTA per SM holds
+  // all of its registers and shared memory, so the next kernel, which may
+  // now be launched, cannot take resources from this grid.
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const uint32_t tbase = sm.tmem_base;
   // all 512 columns are this CTA's, so the allocation starts at column 0;
   // the MMA issuers rely on that (compile-time tensor-memory addresses)

@@ -27,6 +27,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialization attribute may start (set up its barriers and tensor
+// memory) while the previous kernel in the stream is still finishing;
+// griddep_wait() then blocks until that kernel has completed and its memory
+// writes are visible, so it must precede every global-memory access of the
+// launch.  Launched without the attribute, it returns at once.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel in the stream be launched (it still waits in its own
+// griddep_wait for this whole grid to complete before touching memory).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t elect_one_sync() {
   uint32_t pred = 0;
   asm volatile(
