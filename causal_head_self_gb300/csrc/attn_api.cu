@@ -306,7 +306,7 @@ static int decode_common(const void* q, const void* kcache, const void* vcache, 
   rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
   if (Hq / Hkv >= chs::kDecodeTcMinGroup) {
-    // many query heads per cached byte: the tensor-core path (a contraction)
+    // two or more query heads per cached byte: the tensor-core path (a contraction)
     const chs::DecodePlan plan = chs::plan_decode_tc(B, Hq, Hkv, Tmax, st->info.num_sms);
     if ((long long)B * Hkv * ((Hq / Hkv + 127) / 128) > 65535) return ATTN_ERR_INVALID_ARG;
     void* partials = nullptr;
@@ -465,7 +465,7 @@ extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void
   };
   unsigned char* scratch = nullptr;
   if (Hq / Hkv >= chs::kDecodeTcMinGroup) {
-    // large query-head groups: the tensor-core path, as in attn_decode; its
+    // query-head groups: the tensor-core path, as in attn_decode; its
     // split partials are the scratch's only content (it keeps no counters)
     const chs::DecodePlan plan = chs::plan_decode_tc(B, Hq, Hkv, Tmax, st->info.num_sms);
     if ((long long)B * Hkv * ((Hq / Hkv + 127) / 128) > 65535) return ATTN_ERR_INVALID_ARG;

@@ -11,7 +11,9 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int Tmax, int Dh, int num_sms) {
                        : Dh == 256 ? decode_block_keys<256>()
                                    : decode_block_keys<128>();
   const int group = Hq / Hkv;
-  plan.heads_per_cta = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
+  // groups of two or more query heads take the tensor-core path, so this
+  // kernel runs one query head per K/V head: one head per CTA
+  plan.heads_per_cta = 1;
   const long long ctas_per_split = (long long)B * Hkv * (group / plan.heads_per_cta);
   // aim for about eight waves of resident CTAs over the whole cache, in
   // whole blocks, between 2048 and 4096 keys per split (a CTA's start-up and
@@ -78,10 +80,12 @@ static cudaError_t launch_dh(const DecodeParams& prm, int device, cudaStream_t s
   return launch_pdl(kernel, grid, dim3(kDecodeThreads), smem, stream, prm);
 }
 
+// one query head per CTA (plan_decode); the kernel's HPB > 1 forms, which
+// share a CTA's cached rows among several heads of a group, are not launched
+// since groups of two or more heads run on the tensor cores
 template <int DH>
 static cudaError_t launch_hpb(const DecodeParams& prm, int hpb, int device, cudaStream_t stream) {
-  if (hpb == 4) return launch_dh<DH, 4>(prm, device, stream);
-  if (hpb == 2) return launch_dh<DH, 2>(prm, device, stream);
+  if (hpb != 1) return cudaErrorInvalidConfiguration;
   return launch_dh<DH, 1>(prm, device, stream);
 }
 

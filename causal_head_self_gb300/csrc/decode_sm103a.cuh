@@ -8,8 +8,11 @@
 // the whole cache for little arithmetic, so it is bound by HBM bandwidth.
 //
 // One kernel, grid (Hkv * groups, nsplit, B).  A CTA takes `chunk` keys of one
-// (b, K/V head) and the HPB query heads of that head's GQA group it holds, so
-// each cached byte is read from HBM once per group.  One producer thread
+// (b, K/V head) and HPB query heads of that head's group.  The library runs
+// it with HPB = 1 for one query head per K/V head (MHA); groups of two or
+// more heads take the tensor-core decode (decode_tc_sm103a.cuh), which reads
+// each cached byte once per group and does the group's per-key softmax work
+// on 128-row tiles.  One producer thread
 // streams 32-key blocks of K and V into a four-stage shared-memory ring with
 // cp.async.bulk; four consumer warps take 8 keys of each block.  In a warp,
 // LPK = DH/8 lanes share a key, one 16-byte chunk (8 elements) each; every

@@ -1,10 +1,11 @@
-// decode_tc_sm103a.cuh -- the decode step for large query-head groups on the
-// 5th-generation tensor cores (sm_103a).
+// decode_tc_sm103a.cuh -- the decode step for query-head groups (GQA, MQA)
+// on the 5th-generation tensor cores (sm_103a).
 //
-// When many query heads share one K/V head (MQA, or GQA with 8 or more heads
-// per group), a decode step is no longer a pure stream: every cached byte
-// meets Hq / Hkv query rows, 64 FLOP per byte for a group of 32, and the
-// CUDA-core decode kernel becomes bound by its arithmetic.  Packed together,
+// When several query heads share one K/V head, every cached byte meets
+// Hq / Hkv query rows (64 FLOP per byte for a group of 32), and the
+// CUDA-core decode kernel's per-key softmax work, done for every head of the
+// group, becomes its bound (at Dh 64 it held a group of 4 to 55 % of the HBM
+// bandwidth; this path runs it at 82 %).  Packed together,
 // the group's query rows form a real contraction: S = Q K^T with the group's
 // heads as the M dimension (up to 128 per CTA; fewer rows leave the rest of
 // the tile unused), 128 keys (64 at Dh = 256) as N, Dh as K, and O = P V.  So this path is the

@@ -89,11 +89,16 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
                           int ring, float scale_log2, const DecodePlan& plan, int* counters,
                           void* partials, const DeviceInfo& dev, cudaStream_t stream);
 
-// Tensor-core decode for large query-head groups (Hq / Hkv >= kDecodeTcMinGroup):
+// Tensor-core decode for query-head groups (Hq / Hkv >= kDecodeTcMinGroup):
 // splits of whole 128-key tiles, one CTA per (split, b, K/V head, 128 heads),
 // then a combine kernel.  Linear caches, and rings (ring = 1: position t at
-// row t % Tmax, window <= Tmax, window <= 0 meaning Tmax).
-constexpr int kDecodeTcMinGroup = 8;
+// row t % Tmax, window <= Tmax, window <= 0 meaning Tmax).  Measured against
+// the CUDA-core kernel on the same inputs (back-to-back launches): groups of
+// 4 run at 6.8 TB/s instead of 6.3 (Dh 128), 5.6 instead of 3.8 (Dh 64) and
+// 6.0 instead of 5.7 (Dh 256), groups of 2 at 6.7 instead of 6.6; with one
+// query head per K/V head the CUDA-core kernel is as fast (Dh 128) or faster
+// (Dh 64: 6.3 against 5.1 TB/s), so it keeps that case.
+constexpr int kDecodeTcMinGroup = 2;
 DecodePlan plan_decode_tc(int B, int Hq, int Hkv, int Tmax, int num_sms);
 cudaError_t launch_decode_tc(const void* q, const void* kc, const void* vc, const int* seqlens,
                              void* o, int B, int Hq, int Hkv, int Tmax, int Dh, int window,

@@ -169,10 +169,11 @@ int attn_fwd_chunk(const void* q, const void* kcache, const void* vcache, void* 
  * [max(0, seqlens[b] - window), seqlens[b]) (all of them when window <= 0).
  * A seqlens entry outside [1, Tmax] zeroes that sequence's output and latches
  * ATTN_ERR_INVALID_ARG for attn_status().
- * With Hq / Hkv >= 8 (MQA-like groups) the step runs on the tensor cores
- * (the group's query heads packed as the rows of one contraction with each
- * key tile) followed by a small combine kernel (a programmatic dependent
- * launch on the same stream); otherwise on the CUDA cores.
+ * With Hq / Hkv >= 2 (GQA and MQA) the step runs on the tensor cores (the
+ * group's query heads packed as the rows of one contraction with each key
+ * tile) followed by a small combine kernel (a programmatic dependent launch
+ * on the same stream); with one query head per K/V head (MHA) on the CUDA
+ * cores, whose last CTA per head merges the splits.
  * The split-KV partials live in a library-owned device workspace, allocated
  * on first use per device and grown on demand (cudaMalloc): make the first
  * call with the largest shape outside any CUDA graph capture.  Calls on one
@@ -218,11 +219,11 @@ int attn_decode_ring(const void* q, const void* kcache, const void* vcache, cons
  *     16 MiB device array inside this library.  Every GPU that loads the
  *     library holds it until the process exits.
  *   - It runs the kernels attn_decode runs for the same arguments (the
- *     tensor-core path for Hq / Hkv >= 8 at every head size, the CUDA-core
+ *     tensor-core path for Hq / Hkv >= 2 at every head size, the CUDA-core
  *     path otherwise), with the same split plan, so the results are the
  *     same bits.
- *   - On the CUDA-core path a call needs 4*B*Hkv*(Hq/Hkv)/h bytes of counters
- *     (h = 4, 2 or 1 query heads per CTA, rounded up to 256 bytes) plus
+ *   - On the CUDA-core path a call needs 4*B*Hq bytes of counters (one per
+ *     query head, rounded up to 256 bytes) plus
  *     B*Hq*nsplit*(Dh+2)*4 bytes of partials (each part rounded up to 256),
  *     where nsplit is the split count attn_decode would use; on the
  *     tensor-core path only the partials.  A call that needs more than
@@ -254,9 +255,9 @@ int attn_status(cudaStream_t stream);
  *   0  none (the default)
  *   1  attn_fwd: the producer never loads the first K tile of each CTA's
  *      first work item, so the MMA issuers' bounded waits run out
- *   2  attn_decode (CUDA-core path): the producer never loads the first key
- *      block of each CTA
- *   3  attn_decode (tensor-core path, Hq / Hkv >= 8): the producer never loads
+ *   2  attn_decode (CUDA-core path, Hq == Hkv): the producer never loads the
+ *      first key block of each CTA
+ *   3  attn_decode (tensor-core path, Hq / Hkv >= 2): the producer never loads
  *      the first K tile of each CTA
  *   4  attn_bwd: the dK/dV pass's producer never loads the K/V block of each
  *      CTA's first work item

@@ -47,7 +47,10 @@ def chunk_cases(d):
 def decode_cases(d):
     for B, Hq, Hkv, Tmax, Dh, window in [(3, 8, 2, 3000, 128, 0), (2, 32, 1, 5000, 128, 700),
                                          (2, 8, 2, 1200, 256, 0), (2, 16, 2, 900, 256, 300),
-                                         (2, 8, 2, 2000, 64, 0)]:
+                                         (2, 8, 2, 2000, 64, 0),
+                                         # one query head per K/V head: the CUDA-core kernel
+                                         (3, 4, 4, 9000, 128, 0), (2, 4, 4, 1200, 256, 300),
+                                         (2, 4, 4, 5000, 64, 700)]:
         q, kc, vc, sl = inputs.decode_inputs(B, Hq, Hkv, Tmax, Dh, 1, Tmax, seed=Tmax + Dh)
         o = chs.attn_decode(q.to(d), kc.to(d), vc.to(d), sl.to(d), window=window)
         status_ok("decode")
@@ -57,7 +60,8 @@ def decode_cases(d):
 
 def ring_cases(d):
     for B, Hq, Hkv, C, Dh, lens in [(2, 8, 2, 777, 128, [10000, 1554]), (2, 32, 1, 700, 128, [5000, 699]),
-                                    (2, 16, 2, 500, 256, [2345, 499])]:
+                                    (2, 16, 2, 500, 256, [2345, 499]),
+                                    (2, 4, 4, 777, 128, [10000, 1554]), (2, 4, 4, 500, 256, [2345, 499])]:
         gen = torch.Generator().manual_seed(C + Hq)
         Lmax = max(lens)
         q = torch.randn((B, Hq, 1, Dh), generator=gen).to(torch.bfloat16)

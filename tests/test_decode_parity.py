@@ -40,6 +40,12 @@ CASES = [
     (1, 32, 8, 20000, 128, 20000, 20000, 0),
     (3, 8, 2, 12000, 128, 9000, 12000, 0),  # several 2048-key splits per sequence
     (2, 8, 4, 12000, 64, 9000, 12000, 3000),
+    # one query head per K/V head (the CUDA-core kernel): several splits,
+    # windows, every head size
+    (3, 4, 4, 12000, 128, 9000, 12000, 0),
+    (2, 4, 4, 12000, 64, 1, 12000, 3000),
+    (2, 4, 4, 9000, 256, 5000, 9000, 700),
+    (5, 2, 2, 300, 128, 1, 300, 0),
 ]
 
 

@@ -1,6 +1,6 @@
-"""The tensor-core decode path (taken by attn_decode when Hq / Hkv >= 8:
-many query heads share each cached K/V row) against the float64 oracle, and
-against the CUDA-core path on the same step with the K/V heads repeated."""
+"""The tensor-core decode path (taken by attn_decode when Hq / Hkv >= 2:
+several query heads share each cached K/V row) against the float64 oracle,
+and against the CUDA-core path on the same step with the K/V heads repeated."""
 import pytest
 import torch
 
@@ -42,6 +42,11 @@ CASES = [
     (1, 200, 1, 1000, 256, 1000, 1000, 0),    # two row blocks
     (2, 32, 1, 20000, 256, 12000, 20000, 0),  # many splits per sequence
     (2, 40, 5, 777, 256, 65, 777, 64),        # window of exactly one 64-key tile
+    # small groups: 2, 3 and 4 query heads per K/V head
+    (3, 8, 4, 5000, 64, 1, 5000, 0),
+    (2, 12, 4, 3000, 256, 1, 3000, 500),
+    (4, 32, 8, 9000, 128, 2000, 9000, 0),
+    (3, 6, 3, 4100, 128, 1, 4100, 1000),
 ]
 
 

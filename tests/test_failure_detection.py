@@ -45,7 +45,8 @@ def test_prefill_withheld_tile_times_out_then_recovers():
 
 def test_decode_withheld_block_times_out_then_recovers():
     d = torch.device("cuda")
-    q, kc, vc, sl = inputs.decode_inputs(3, 8, 2, 3000, 128, 1000, 3000, seed=22)
+    # one query head per K/V head: the CUDA-core decode, whose hook is kind 2
+    q, kc, vc, sl = inputs.decode_inputs(3, 8, 8, 3000, 128, 1000, 3000, seed=22)
     qd, kcd, vcd, sld = q.to(d), kc.to(d), vc.to(d), sl.to(d)
     assert chs.attn_status() == chs.ATTN_OK
     chs.attn_debug_inject_fault(2)

@@ -1,8 +1,8 @@
 """The entry points inside CUDA graphs: captured once (after eager calls that
 size the library's workspaces and set its kernels' attributes), replayed on
 new inputs copied into the captured buffers, and compared with eager calls
-bit for bit (every kernel is deterministic).  Captured together: a prefill, a
-GQA decode step (CUDA-core kernel with its in-kernel merge), an MQA decode
+bit for bit (every kernel is deterministic).  Captured together: a prefill, an
+MHA decode step (CUDA-core kernel with its in-kernel merge), an MQA decode
 step (tensor-core kernel and its dependent combine launch) and a forward +
 backward pass.  A workspace that would have to grow inside a capture is
 reported as ATTN_ERR_NO_MEMORY instead of calling cudaMalloc there."""
@@ -23,7 +23,7 @@ def _built():
 
 def _inputs(seed, d):
     pre = [x.to(d) for x in inputs.prefill_inputs(1, 8, 2, 700, 128, seed=seed)]
-    dec = [x.to(d) for x in inputs.decode_inputs(4, 32, 8, 4096, 128, 1000, 4096, seed=seed)]
+    dec = [x.to(d) for x in inputs.decode_inputs(4, 8, 8, 4096, 128, 1000, 4096, seed=seed)]
     mqa = [x.to(d) for x in inputs.decode_inputs(2, 32, 1, 6000, 128, 3000, 6000, seed=seed + 1)]
     dout = inputs.grad_inputs(pre[0].shape, seed=seed).to(d)
     return pre, dec, mqa, dout

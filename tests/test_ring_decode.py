@@ -55,7 +55,9 @@ CASES = [
     (1, 2, 2, 33, 128, [1000], 0),                     # a ring barely larger than a block
     (2, 8, 2, 500, 256, [1234, 499], 0),               # Dh 256: 16-key stages
     (2, 8, 2, 8192, 128, [8192 * 2 + 5, 9000], 0),     # wrapped, four 2048-key splits to merge
-    # groups of 8 or more query heads: the tensor-core decode on the ring
+    (2, 4, 4, 8192, 128, [8192 * 2 + 5, 9000], 0),     # MHA (CUDA-core kernel), several splits
+    (2, 4, 4, 500, 256, [1234, 499], 300),             # MHA at Dh 256 with a window
+    # larger query-head groups: the tensor-core decode on the ring
     (2, 32, 1, 4096, 128, [4096 * 3 + 17, 5000], 2048), # MQA, window shorter than the ring
     (3, 16, 2, 1000, 128, [100, 1000, 3333], 0),       # not wrapped, full, wrapped
     (2, 8, 1, 777, 128, [10000, 777 * 2], 500),        # ring not a multiple of a tile
@@ -75,7 +77,7 @@ def test_ring_decode_against_oracle(B, Hq, Hkv, C, Dh, lens, window):
     assert_close(got, ref, what=f"ring {(B, Hq, Hkv, C, Dh, lens, window)}")
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (32, 1)])   # CUDA-core and tensor-core kernels
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (32, 1)])   # CUDA-core, tensor-core, tensor-core
 def test_unwrapped_ring_is_plain_decode_bitwise(Hq, Hkv):
     q, k, v, kr, vr, sl = _ring_case(3, Hq, Hkv, 2048, 128, [1, 700, 2048], seed=41)
     d = torch.device("cuda")

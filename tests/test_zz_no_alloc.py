@@ -30,6 +30,8 @@ CASES = [
     (3, 8, 2, 5000, 64, 1, 5000, 3000),
     (4, 32, 1, 9000, 128, 3000, 9000, 0),    # MQA: the tensor-core path and its combine
     (3, 16, 2, 6000, 256, 2000, 6000, 0),    # group of 8 at Dh 256: tensor cores, 64-key tiles
+    (4, 8, 8, 9000, 128, 3000, 9000, 0),     # MHA: the CUDA-core kernel, its counters in the array
+    (3, 4, 4, 5000, 64, 1, 5000, 2000),      # MHA at Dh 64 with a window
 ]
 
 
