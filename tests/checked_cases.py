@@ -92,9 +92,8 @@ def backward_cases(d):
         rq, rk, rv = oracle.attention_bwd(q, k, v, dout, causal=True, window=window)
         for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
             g = got.float().cpu().numpy()
-            s = max(1.0, float(np.sqrt(np.mean(ref ** 2))))
             err = np.abs(g - ref)
-            assert np.all(err <= 2e-2 * s + 2.0 ** -7 * np.abs(ref)), f"backward {name}"
+            assert np.all(err <= 2e-2 + 2.0 ** -8 * np.abs(ref)), f"backward {name}"
 
 
 def main():

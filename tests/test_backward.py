@@ -8,11 +8,17 @@ Tolerance of the gradients: the kernels round P and dS to bf16 before their
 MMAs and the outputs to bf16 (a relative error of at most 2^-8 each), and D_i
 comes from the bf16-rounded forward output; every sum is fp32.  Unlike the
 forward output (a convex combination of value rows, so bounded by them), a
-gradient entry can be large, and the output rounding alone reaches 2^-8 of
-it.  The bar is therefore element-wise |err| <= 2e-2 * s + 2^-7 * |ref| (the
-forward's absolute bar plus twice the bf16 rounding bound) with mean |err| <=
-2e-3 * s, s = max(1, RMS of the reference).
+gradient entry can be large, and the rounding of the result alone reaches
+2^-8 of it.  The bar is therefore the forward's bar plus one bf16 rounding of
+the result: element-wise |err| <= 2e-2 + 2^-8 |ref|, and mean |err| <=
+2e-3 + 2^-8 mean |ref|.  Measured on every case below (GB300): the largest
+|err| - 2^-8 |ref| is 1.34e-2 (two thirds of the absolute term) and the
+largest mean |err| 1.47e-3 (with CHS_ERROR_TABLE set, every comparison
+appends its errors to that file).
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -38,13 +44,24 @@ def _close_scaled(got, ref, what):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     if not ref.size:
         return
-    s = max(1.0, float(np.sqrt(np.mean(ref ** 2))))
     err = np.abs(got - ref)
-    bound = 2e-2 * s + 2.0 ** -7 * np.abs(ref)
+    if os.environ.get("CHS_ERROR_TABLE"):
+        # the measured errors behind the bar: max and mean |err|, the
+        # reference's RMS, and the largest |err| - 2^-8 |ref| (the error left
+        # once one bf16 rounding of the result is taken out)
+        with open(os.environ["CHS_ERROR_TABLE"], "a") as f:
+            f.write(json.dumps({"case": what, "max_err": float(err.max()),
+                                "mean_err": float(err.mean()),
+                                "rms_ref": float(np.sqrt(np.mean(ref ** 2))),
+                                "max_ref": float(np.abs(ref).max()),
+                                "max_err_less_rounding": float(np.max(err - 2.0 ** -8 * np.abs(ref)))})
+                    + "\n")
+    bound = 2e-2 + 2.0 ** -8 * np.abs(ref)
     worst = int(np.argmax(err - bound))
     assert np.all(err <= bound), (f"{what}: |err| {err.flat[worst]:.3e} > {bound.flat[worst]:.3e} "
                                   f"at ref {ref.flat[worst]:.4e}")
-    assert err.mean() <= 2e-3 * s, f"{what}: mean|err| {err.mean():.3e}"
+    mean_bound = 2e-3 + 2.0 ** -8 * float(np.abs(ref).mean())
+    assert err.mean() <= mean_bound, f"{what}: mean|err| {err.mean():.3e} > {mean_bound:.3e}"
 
 
 def gpu_fwd_bwd(q, k, v, dout, causal, window):
