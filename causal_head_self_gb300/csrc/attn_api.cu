@@ -131,7 +131,7 @@ struct MapKey {
   }
 };
 struct MapCache {
-  static constexpr int kEntries = 16;
+  static constexpr int kEntries = 64;
   MapKey key[kEntries];
   alignas(64) CUtensorMap map[kEntries];
   int used = 0, next = 0;

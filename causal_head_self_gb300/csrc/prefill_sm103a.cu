@@ -7,7 +7,8 @@ namespace chs {
 
 template <int DH>
 static cudaError_t launch_prefill_dh(const CUtensorMap& mq, const CUtensorMap& mk,
-                                     const CUtensorMap& mv, const PrefillParams& prm,
+                                     const CUtensorMap& mv, const CUtensorMap& mo,
+                                     const PrefillParams& prm,
                                      int num_sms, int device, cudaStream_t stream) {
   constexpr size_t smem = prefill_smem_bytes<DH>();
   static_assert(smem <= 232448, "shared memory budget of one sm_103a CTA");
@@ -31,7 +32,7 @@ static cudaError_t launch_prefill_dh(const CUtensorMap& mq, const CUtensorMap& m
   const int grid = prm.num_items < num_sms ? prm.num_items : num_sms;
   // a programmatic dependent launch: set-up overlaps the previous kernel's tail
   return launch_pdl(attn_prefill_sm103a<DH>, dim3(grid), dim3(PrefillCfg<DH>::kThreads), smem,
-                    stream, mq, mk, mv, prm);
+                    stream, mq, mk, mv, mo, prm);
 }
 
 // Multiplier and shift for FastDiv (exact for dividends below 2^31).
@@ -100,10 +101,12 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o,
   // start_pos + Sq of them, and the maps cover only those (the last key
   // tile's rows past them are zero-filled, never read from the cache)
   const int Skv = start_pos + Sq;
-  CUtensorMap mq, mk, mv;
+  // the output is written 32 rows (one softmax warp) x 64 columns per box
+  CUtensorMap mq, mk, mv, mo;
   if (!encode_bf16_map(&mq, q, Dh, Sq, (long long)B * Hq, 128) ||
       !encode_bf16_map(&mk, k, Dh, Skv, (long long)B * Hkv, 128, Tkv) ||
-      !encode_bf16_map(&mv, v, Dh, Skv, (long long)B * Hkv, 128, Tkv))
+      !encode_bf16_map(&mv, v, Dh, Skv, (long long)B * Hkv, 128, Tkv) ||
+      !encode_bf16_map(&mo, o, Dh, Sq, (long long)B * Hq, 32))
     return cudaErrorInvalidValue;
   PrefillParams prm;
   prm.B = B;
@@ -119,16 +122,14 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o,
   const long long items = (long long)prm.num_qblocks * B * Hq;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   prm.num_items = (int)items;
-  prm.o = static_cast<__nv_bfloat16*>(o);
-  prm.o_wide = (reinterpret_cast<uintptr_t>(o) & 31) == 0;
   prm.lse = lse;
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
   prm.div_bh = make_fast_div((uint32_t)(B * Hq));
   prm.div_hq = make_fast_div((uint32_t)Hq);
   prm.div_group = make_fast_div((uint32_t)(Hq / Hkv));
-  return Dh == 128 ? launch_prefill_dh<128>(mq, mk, mv, prm, dev.num_sms, dev.device, stream)
-                   : launch_prefill_dh<64>(mq, mk, mv, prm, dev.num_sms, dev.device, stream);
+  return Dh == 128 ? launch_prefill_dh<128>(mq, mk, mv, mo, prm, dev.num_sms, dev.device, stream)
+                   : launch_prefill_dh<64>(mq, mk, mv, mo, prm, dev.num_sms, dev.device, stream);
 }
 
 }  // namespace chs

@@ -15,10 +15,12 @@
 // 256 query rows of one (b, h): two 128-row sub-tiles that take turns on the
 // tensor core, so that the softmax of one overlaps the MMAs of the other.
 // Items are handed out heaviest first (causal work grows with the query
-// block) in "snake" order over the CTAs, and the TMA producer runs ahead
-// into the next item (its Q and K/V tiles) while the current one finishes.
+// block) in "snake" order over the CTAs (a CTA with only two items takes the
+// lighter one first), and the TMA producer runs ahead into the next item
+// (its Q and K/V tiles) while the current one finishes.
 // Roles (384 threads):
-//   warps 0-3  softmax + epilogue of sub-tile 0 (thread t owns row t, TMEM lane t)
+//   warps 0-3  softmax + epilogue of sub-tile 0 (thread t owns row t, TMEM lane t;
+//              each warp writes its 32 output rows with bulk tensor stores)
 //   warps 4-7  softmax + epilogue of sub-tile 1
 //   warp  8    TMEM allocation; issues the MMAs of sub-tile 0
 //   warp  9    one thread issues every TMA load (Q per item, then K/V tiles)
@@ -63,8 +65,6 @@ struct PrefillParams {
   float scale_log2;   // softmax scale * log2(e)
   int num_qblocks;    // ceil(Sq / 256)
   int num_items;      // work items: num_qblocks * B * Hq
-  __nv_bfloat16* o;   // output [B, Hq, Sq, DH]
-  int o_wide;         // o is 32-byte aligned: 32-byte stores
   float* lse;         // optional [B, Hq, Sq]: log sum_j exp(s_ij) per row (natural log)
   int* error_word;    // set to a nonzero status when a wait gives up
   int fault;          // test hook: 1 = the first K tile is never loaded
@@ -102,6 +102,9 @@ struct __align__(1024) PrefillSmem {
   uint8_t q[2][Cfg::kTileBytes];          // Q sub-tiles of the current item
   uint8_t k[Cfg::kStagesK][Cfg::kTileBytes];
   uint8_t v[Cfg::kStagesV][Cfg::kTileBytes];
+  // per softmax warp: its 32 output rows x 64 columns of bf16, 128-byte
+  // swizzled (the layout of one box of the output's tensor map)
+  uint8_t ostage[8][32 * 128];
   uint64_t q_full[2], q_empty[2];       // Q sub-tile s loaded / its last S MMA done
   uint64_t k_full[Cfg::kStagesK], k_empty[Cfg::kStagesK];
   uint64_t v_full[Cfg::kStagesV], v_empty[Cfg::kStagesV];
@@ -184,6 +187,19 @@ __device__ __forceinline__ int prefill_item(int k, int c, int G) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
+// The k-th work item of this CTA (num_items or more: none left).  When the
+// CTAs have at most two items each (short sequences), a CTA takes its items
+// lightest first: the short item's latency-bound chain (its loads, masked
+// diagonal tiles and epilogue) then overlaps the start of the long one,
+// instead of running alone at the end of the launch.  With more items per
+// CTA the heaviest-first order is kept (its tail is the lightest items).
+__device__ __forceinline__ int prefill_cta_item(int k, int num_items) {
+  const int G = gridDim.x, c = blockIdx.x;
+  if (num_items > 2 * G) return prefill_item(k, c, G);
+  const int n = num_items > G ? 1 + (prefill_item(1, c, G) < num_items ? 1 : 0) : 1;
+  return k < n ? prefill_item(n - 1 - k, c, G) : num_items;
+}
+
 struct PrefillItem {
   int b, h, bh, bh_kv;
   PrefillTile tile;
@@ -255,7 +271,7 @@ __device__ __forceinline__ void prefill_issuer(PrefillSmem<DH>& sm, const Prefil
   uint32_t pph = 0, qph = 0;
   bool ok = true;
   for (int it = 0; ok; ++it) {
-    const int w = prefill_item(it, blockIdx.x, gridDim.x);
+    const int w = prefill_cta_item(it, p.num_items);
     if (w >= p.num_items) break;
     const PrefillTile tile = prefill_item_of(p, w).tile;
     const int n_tiles = tile.hi - tile.lo + 1;
@@ -412,7 +428,7 @@ __device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const Pref
       if (++vst == Cfg::kStagesV) { vst = 0; vph ^= 1; }
     }
     // decode the next item while this one's copies are in flight
-    const int w = prefill_item(it + 1, blockIdx.x, gridDim.x);
+    const int w = prefill_cta_item(it + 1, p.num_items);
     if (w >= p.num_items) break;
     item = prefill_item_of(p, w);
   }
@@ -431,8 +447,8 @@ __device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const Pref
 // maximum; per item: O / l written straight from registers to global memory.
 template <int DH>
 __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const PrefillParams& p,
-                                                uint32_t tbase, volatile int* abort, int warp,
-                                                int lane) {
+                                                const CUtensorMap* map_o, uint32_t tbase,
+                                                volatile int* abort, int warp, int lane) {
   using Cfg = PrefillCfg<DH>;
   const int s = warp / 4;                 // sub-tile
   const int wl = warp % 4;                // warp within the warpgroup = TMEM lane quarter
@@ -444,7 +460,7 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
   uint32_t ph = 0;   // bit 0: s_full phase, bit 1: o_final phase
   bool ok = true;
   for (int it = 0; ok; ++it) {
-    const int w = prefill_item(it, blockIdx.x, gridDim.x);
+    const int w = prefill_cta_item(it, p.num_items);
     if (w >= p.num_items) break;
     const PrefillTile tile = prefill_item_of(p, w).tile;
     if (!tile.valid(s)) continue;           // a ragged last block: no rows here
@@ -569,54 +585,65 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
     }
     if (!ok) break;
 
-    // ---- epilogue: O / l -> bf16 -> row `row` of the output, 32 bytes per
-    // store (16 when the output is only 16-byte aligned)
+    // ---- epilogue: O / l -> bf16 -> the output.  Each warp stages its 32
+    // rows, 64 columns at a time, in shared memory in the 128-byte swizzled
+    // layout of one box of the output's tensor map (16-byte stores, no bank
+    // conflicts), and one lane writes the box with a bulk tensor store.  The
+    // global write is then one asynchronous copy per warp and 64 columns
+    // instead of 32-byte stores to 32 rows per instruction, which kept the
+    // load/store pipeline (and the barrier waits of the other roles, which
+    // go through it) busy for about a microsecond per item.
     if (!(ok = mbar_wait(&sm.o_final[s], (ph >> 1) & 1u, abort))) break;
     ph ^= 2u;
     tc_fence_after_sync();
     const float inv_l = 1.0f / l_run;
     const int bh = p.div_bh.mod(w);
     const int orow = tile.row_first(s) + t;  // output row within the chunk
-    uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.Sq + orow) * DH);
-    const bool store = orow < p.Sq;
     // sum_j exp(s_ij) = 2^m_run * l_run (m_run in units of log2)
-    if (p.lse != nullptr && store)
+    if (p.lse != nullptr && orow < p.Sq)
       p.lse[(size_t)bh * p.Sq + orow] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+    const uint32_t stage = smem_u32(sm.ostage[warp]);
 #pragma unroll
-    for (int c = 0; c < DH / 32; c += 2) {
+    for (int h = 0; h < Cfg::kHalves; ++h) {
       uint32_t o0[32], o1[32];
-      tmem_ld_32x32b_x32(colO + 32 * c, o0);
-      tmem_ld_32x32b_x32(colO + 32 * c + 32, o1);
+      tmem_ld_32x32b_x32(colO + 64 * h, o0);
+      tmem_ld_32x32b_x32(colO + 64 * h + 32, o1);
+      // the previous bulk store from this stage has read it
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
       tmem_ld_wait(o0);
       tmem_ld_wait(o1);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {   // 16 columns each
-        const uint32_t* o = q < 2 ? o0 + 16 * q : o1 + 16 * (q - 2);
-        uint32_t v[8];
+      for (int c = 0; c < 8; ++c) {   // 16-byte chunk c: columns 8c .. 8c+7 of these 64
+        const uint32_t* x8 = c < 4 ? o0 + 8 * c : o1 + 8 * (c - 4);
+        uint32_t v[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          v[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-        if (store) {
-          uint4* d = dst + 2 * (2 * c + q);
-          if (p.o_wide) {
-            st_global_v8(d, v);
-          } else {
-            d[0] = make_uint4(v[0], v[1], v[2], v[3]);
-            d[1] = make_uint4(v[4], v[5], v[6], v[7]);
-          }
-        }
+        for (int e = 0; e < 4; ++e)
+          v[e] = pack_bf16x2(__uint_as_float(x8[2 * e]) * inv_l,
+                             __uint_as_float(x8[2 * e + 1]) * inv_l);
+        st_shared_v4(stage + lane * 128 + ((c ^ (lane & 7)) << 4), v[0], v[1], v[2], v[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      // rows past the end of the chunk are clipped by the tensor map
+      if (lane == 0) {
+        tma_store_3d(map_o, sm.ostage[warp], 64 * h, tile.row_first(s) + 32 * wl, bh);
+        bulk_commit_group();
       }
     }
     // the next item's first P.V may overwrite O_s once these reads are done:
     // the arrive on p_full that allows it follows tcgen05.wait::ld above
   }
+  // the staged rows must be written out before the CTA's shared memory goes
+  if (lane == 0) bulk_wait_group0();
 }
 
 template <int DH>
 __global__ void __launch_bounds__(384, 1)
     attn_prefill_sm103a(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
-                        const __grid_constant__ CUtensorMap map_v, const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap map_v,
+                        const __grid_constant__ CUtensorMap map_o, const PrefillParams p) {
   using Cfg = PrefillCfg<DH>;
   using Smem = PrefillSmem<DH>;
   extern __shared__ uint8_t smem_raw[];
@@ -636,7 +663,8 @@ __global__ void __launch_bounds__(384, 1)
     prefetch_tensormap(&map_q);
     prefetch_tensormap(&map_k);
     prefetch_tensormap(&map_v);
-    first = prefill_item_of(p, prefill_item(0, blockIdx.x, gridDim.x));
+    prefetch_tensormap(&map_o);
+    first = prefill_item_of(p, prefill_cta_item(0, p.num_items));
   }
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
@@ -689,7 +717,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     setmaxnreg_inc<Cfg::kRegsSoftmax>();
-    if (tbase == 0) prefill_softmax<DH>(sm, p, tbase, abort, warp, lane);
+    if (tbase == 0) prefill_softmax<DH>(sm, p, &map_o, tbase, abort, warp, lane);
   }
 
   // ---- teardown (every thread gets here; all waits above are bounded)
