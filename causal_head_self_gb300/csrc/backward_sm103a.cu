@@ -23,21 +23,26 @@ static cudaError_t launch_bwd_dh(const CUtensorMap& mq, const CUtensorMap& mk,
   if (e != cudaSuccess) return e;
   const long long rows = (long long)prm.B * prm.Hq * prm.S_pad;
   constexpr int rpb = bwd_prep_rows_per_block<DH>();
-  attn_bwd_prep<DH><<<(unsigned)((rows + rpb - 1) / rpb), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2,
-      delta, rows, prm.S, prm.S_pad);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // three programmatic dependent launches: each kernel's launch and set-up
+  // overlap the previous one's tail (the prep and the dK/dV pass wait for
+  // their predecessor before reading; the dQ pass, which needs only the
+  // prep's output, runs beside the dK/dV pass's last CTAs)
+  e = launch_pdl(attn_bwd_prep<DH>, dim3((unsigned)((rows + rpb - 1) / rpb)), dim3(256), 0, stream,
+                 static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
+                 lse, lse2, delta, rows, prm.S, prm.S_pad);
+  if (e != cudaSuccess) return e;
   // persistent passes: one CTA per SM (their shared memory allows no second)
   BwdParams pk = prm;
   pk.num_items = prm.nblk * prm.B * prm.Hkv;
   const int grid_kv = pk.num_items < dev.num_sms ? pk.num_items : dev.num_sms;
-  attn_bwd_dkdv<DH><<<grid_kv, BwdCfg<DH>::kThreads, smem_kv, stream>>>(mq, mk, mv, mdo, pk);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_pdl(attn_bwd_dkdv<DH>, dim3(grid_kv), dim3(BwdCfg<DH>::kThreads), smem_kv, stream,
+                 mq, mk, mv, mdo, pk);
+  if (e != cudaSuccess) return e;
   BwdParams pq = prm;
   pq.num_items = prm.nblk * prm.B * prm.Hq;
   const int grid_q = pq.num_items < dev.num_sms ? pq.num_items : dev.num_sms;
-  attn_bwd_dq<DH><<<grid_q, BwdCfg<DH>::kThreads, smem_q, stream>>>(mq, mk, mv, mdo, pq);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_dq<DH>, dim3(grid_q), dim3(BwdCfg<DH>::kThreads), smem_q, stream, mq,
+                    mk, mv, mdo, pq);
 }
 
 size_t bwd_workspace_bytes(int B, int Hq, int S) {

@@ -97,38 +97,59 @@ __host__ __device__ constexpr uint32_t bwd_packed_col(int kk) {
 // D_i = sum_d dO[i, d] o[i, d] (fp32 products of the bf16 values) and
 // lse2_i = lse_i * log2(e) for every row of [B * Hq, S_pad]; rows past S get
 // D = 0 and lse2 = +inf (their weights exp2(x - lse2) are then 0).  DH / 8
-// lanes per row, 16 bytes of o and of dO each.
+// lanes per row, 16 bytes of o and of dO each; a block covers kPrepRowSets
+// row sets, all of whose loads are issued before the first is used.
+constexpr int kPrepRowSets = 4;
 template <int DH>
-constexpr int bwd_prep_rows_per_block() { return 256 / (DH / 8); }
+constexpr int bwd_prep_rows_per_block() { return kPrepRowSets * 256 / (DH / 8); }
 
 template <int DH>
 __global__ void __launch_bounds__(256)
     attn_bwd_prep(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                   const float* __restrict__ lse, float* __restrict__ lse2,
                   float* __restrict__ delta, long long rows, int S, int S_pad) {
-  constexpr int kLanes = DH / 8;   // 16 or 8 lanes per row
-  const long long r = (long long)blockIdx.x * bwd_prep_rows_per_block<DH>() + threadIdx.x / kLanes;
+  constexpr int kLanes = DH / 8;                // 16 or 8 lanes per row
+  constexpr int kRowsPerSet = 256 / kLanes;
+  // o, dO and lse may come from the previous kernel in the stream
+  griddep_wait();
+  griddep_launch_dependents();
   const int sub = threadIdx.x % kLanes;
-  const long long bh = r / S_pad;
-  const int i = (int)(r - bh * S_pad);
-  const bool valid = r < rows && i < S;
-  float acc = 0.f;
-  if (valid) {
-    const size_t base = ((size_t)bh * S + i) * DH + 8 * sub;
-    const uint4 a = *reinterpret_cast<const uint4*>(o + base);
-    const uint4 b = *reinterpret_cast<const uint4*>(dout + base);
-    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+  long long r[kPrepRowSets];
+  bool valid[kPrepRowSets];
+  uint4 a[kPrepRowSets], b[kPrepRowSets];
+#pragma unroll
+  for (int k = 0; k < kPrepRowSets; ++k) {
+    r[k] = (long long)blockIdx.x * bwd_prep_rows_per_block<DH>() + k * kRowsPerSet +
+           threadIdx.x / kLanes;
+    const long long bh = r[k] / S_pad;
+    const int i = (int)(r[k] - bh * S_pad);
+    valid[k] = r[k] < rows && i < S;
+    a[k] = b[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (valid[k]) {
+      const size_t base = ((size_t)bh * S + i) * DH + 8 * sub;
+      a[k] = *reinterpret_cast<const uint4*>(o + base);
+      b[k] = *reinterpret_cast<const uint4*>(dout + base);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPrepRowSets; ++k) {
+    const uint32_t wa[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+    const uint32_t wb[4] = {b[k].x, b[k].y, b[k].z, b[k].w};
+    float acc = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       acc = fmaf(__uint_as_float(wa[e] << 16), __uint_as_float(wb[e] << 16), acc);
       acc = fmaf(__uint_as_float(wa[e] & 0xffff0000u), __uint_as_float(wb[e] & 0xffff0000u), acc);
     }
-  }
 #pragma unroll
-  for (int m = kLanes / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (sub == 0 && r < rows) {
-    delta[r] = valid ? acc : 0.f;
-    lse2[r] = valid ? lse[(size_t)bh * S + i] * 1.4426950408889634f : __int_as_float(0x7f800000);
+    for (int m = kLanes / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (sub == 0 && r[k] < rows) {
+      const long long bh = r[k] / S_pad;
+      const int i = (int)(r[k] - bh * S_pad);
+      delta[r[k]] = valid[k] ? acc : 0.f;
+      lse2[r[k]] = valid[k] ? lse[(size_t)bh * S + i] * 1.4426950408889634f
+                            : __int_as_float(0x7f800000);
+    }
   }
 }
 
@@ -560,6 +581,11 @@ __global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // launched as a programmatic dependent of the prep kernel: its D and lse2
+  // (and the inputs) are read only after it has completed; then the dQ pass,
+  // which needs no output of this one, may be scheduled on SMs this grid frees
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const uint32_t tbase = sm.tmem_base;
   // compile-time tensor-memory columns: the allocation must start at column 0
   if (tbase != 0 && threadIdx.x == 0) sm.abort_flag = 1;
@@ -941,6 +967,12 @@ __global__ void __launch_bounds__(BwdCfg<DH>::kThreads, 1)
     tmem_dealloc(tbase, 512);
   }
   if (threadIdx.x == 0 && sm.abort_flag) atomicExch(p.error_word, 4);   // ATTN_ERR_TIMEOUT
+  // Launched as a programmatic dependent of the dK/dV pass, this grid may run
+  // beside that pass's last CTAs (it reads nothing the pass writes: only the
+  // inputs and the prep kernel's D and lse2, complete before any dK/dV CTA
+  // let this grid be scheduled).  It does not finish before the dK/dV pass
+  // has, so that the next kernel in the stream sees dK and dV as well.
+  if (threadIdx.x == 0) griddep_wait();
 }
 
 template <int DH>
