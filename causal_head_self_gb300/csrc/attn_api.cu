@@ -351,7 +351,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dh,
              int causal, int window, float scale, cudaStream_t stream) {
   if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (Dh != 64 && Dh != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Dh != 64 && Dh != 128 && Dh != 256) return ATTN_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (window < 0) window = 0;
   if (window > 0 && !causal) return ATTN_ERR_INVALID_ARG;

@@ -38,6 +38,9 @@ WORKLOADS = {
                                            causal=True, window=0, seed=2),
     "backward_gqa_b2_h32kv8_s2048_d128": dict(kind="backward", B=2, Hq=32, Hkv=8, S=2048,
                                               Dh=128, causal=True, window=0, seed=7),
+    # the backward pass at head size 256 (the causal GQA prefill at Dh=256)
+    "backward_gqa_b1_h16kv8_s8192_d256": dict(kind="backward", B=1, Hq=16, Hkv=8, S=8192, Dh=256,
+                                              causal=True, window=0, seed=6),
     # the S=4096 backward on 8 heads (a profiler-sized case)
     "backward_mha_b1_h8_s4096_d128": dict(kind="backward", B=1, Hq=8, Hkv=8, S=4096, Dh=128,
                                           causal=True, window=0, seed=2),

@@ -20,7 +20,7 @@
  *     heads moved ahead of the sequence axis).  All tensor pointers are
  *     DEVICE pointers, 16-byte aligned.  The caller owns every tensor.
  *   - Dh must be 64, 128 or 256 (the Gemma head size) for every entry
- *     point but attn_bwd (64 or 128) (ATTN_ERR_UNSUPPORTED otherwise).
+ *     point (ATTN_ERR_UNSUPPORTED otherwise).
  *   - Hq % Hkv == 0 is required (ATTN_ERR_INVALID_ARG otherwise).
  *   - scale == 0 selects 1/sqrt(Dh), the textbook's choice (divide by the
  *     square root of the HEAD size, not the model width); a positive scale is
@@ -116,16 +116,19 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* ls
  *   dq    [B, Hq,  S, Dh]  dL/dq                       (device, bf16, written)
  *   dk    [B, Hkv, S, Dh]  dL/dk, summed over the query heads of each group
  *   dv    [B, Hkv, S, Dh]  dL/dv, likewise             (device, bf16, written)
- * dq, dk and dv must not overlap each other or any input.  Dh must be 64 or
- * 128 (ATTN_ERR_UNSUPPORTED otherwise).  The result is deterministic (no
- * atomics): one pass computes dK and dV per key block, a second dQ per query
- * block.  Per-row intermediates live in a library-owned device workspace
+ * dq, dk and dv must not overlap each other or any input.  Dh must be 64,
+ * 128 or 256 (ATTN_ERR_UNSUPPORTED otherwise).  The result is deterministic
+ * (no atomics): at Dh 64 and 128 one pass computes dK and dV per key block, a
+ * second dQ per query block; at Dh 256, where a 256-column accumulator fills
+ * half of tensor memory, dV, dK and dQ each take a pass of their own.
+ * Per-row intermediates live in a library-owned device workspace
  * (8 bytes per query row, allocated on first use and grown on demand,
  * ATTN_ERR_NO_MEMORY if that fails); backward calls that overlap on the GPU
  * race on it.  B == 0 or S == 0 is a no-op.
  * Work: 10*Dh FLOPs per visible (query, key) pair per query head (S
  * recomputed, dP, dV, dQ, dK: 2*Dh each), 2.5 x attn_fwd's; the kernels
- * execute 14*Dh (S and dP are computed in both passes).
+ * execute 14*Dh (S and dP are computed in both passes; at Dh 256, 16*Dh:
+ * S in all three passes, dP in two).
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
              const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dh,

@@ -82,7 +82,8 @@ def ring_cases(d):
 
 
 def backward_cases(d):
-    for B, Hq, Hkv, S, Dh, window in [(1, 4, 2, 300, 128, 0), (1, 2, 1, 257, 64, 100)]:
+    for B, Hq, Hkv, S, Dh, window in [(1, 4, 2, 300, 128, 0), (1, 2, 1, 257, 64, 100),
+                                      (1, 4, 2, 300, 256, 0), (1, 2, 1, 257, 256, 100)]:
         q, k, v = inputs.prefill_inputs(B, Hq, Hkv, S, Dh, seed=S)
         dout = inputs.grad_inputs(q.shape, seed=S)
         qd, kd, vd, dd = q.to(d), k.to(d), v.to(d), dout.to(d)

@@ -131,7 +131,7 @@ def bwd(lib, *args, ptrs=PB, scale=0.0):
 
 @pytest.mark.parametrize("args,code", [
     ((1, 6, 4, 16, 128, 1, 0), _binding.ATTN_ERR_INVALID_ARG),   # Hq % Hkv != 0
-    ((1, 4, 4, 16, 256, 1, 0), _binding.ATTN_ERR_UNSUPPORTED),   # backward takes Dh 64 / 128
+    ((1, 4, 4, 16, 96, 1, 0), _binding.ATTN_ERR_UNSUPPORTED),    # backward takes Dh 64 / 128 / 256
     ((1, 4, 4, 16, 128, 0, 8), _binding.ATTN_ERR_INVALID_ARG),   # window without causal
     ((1, 4, 4, 16, 128, 2, 0), _binding.ATTN_ERR_INVALID_ARG),   # causal flag not 0/1
     ((0, 4, 4, 16, 128, 1, 0), _binding.ATTN_OK),                # empty batch: no-op

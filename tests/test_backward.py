@@ -181,7 +181,7 @@ def test_deterministic_and_every_output_written():
 
 def test_rejects_unsupported_head_size_and_aliasing():
     d = torch.device("cuda")
-    q = torch.zeros((1, 2, 64, 256), dtype=torch.bfloat16, device=d)
+    q = torch.zeros((1, 2, 64, 96), dtype=torch.bfloat16, device=d)
     lse = torch.zeros((1, 2, 64), dtype=torch.float32, device=d)
     with pytest.raises(chs.AttnError) as e:
         chs.attn_bwd(q, q, q, q, q, lse)
