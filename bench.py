@@ -482,7 +482,8 @@ def time_next_rows(chs, dev, flush, stream, peaks, l2):
     """The rows beyond the headline step, each on its own workload, timed as
     the prefill shapes are: chunked prefill, rolling-buffer decode, head size
     256 prefill, MQA decode on the tensor cores at head sizes 128 and 256,
-    decode at head size 64, and the backward pass (2.5x the forward's FLOPs)."""
+    decode at head size 64, and the backward pass at head sizes 128 and 256
+    (2.5x the forward's FLOPs)."""
     out = {}
     bf16 = peaks["bf16_tflops"]
 
@@ -517,7 +518,16 @@ def time_next_rows(chs, dev, flush, stream, peaks, l2):
                                   input_copies=len(sets))
     del q, k, v, o, sets, fns
 
-    name = "backward_mha_b1_h32_s4096_d128"
+    for key, name in (("F4_backward", "backward_mha_b1_h32_s4096_d128"),
+                      ("F4_backward_d256", "backward_gqa_b1_h16kv8_s8192_d256")):
+        out[key] = _backward_row(chs, name, dev, flush, stream, bf16, l2)
+    if chs.attn_status() != chs.ATTN_OK:
+        raise RuntimeError("device error while timing the next rows")
+    return out
+
+
+def _backward_row(chs, name, dev, flush, stream, bf16, l2):
+    """The backward pass (attn_bwd after attn_fwd_lse) of a named workload."""
     w = inputs.WORKLOADS[name]
     q, k, v, do = (x.to(dev) for x in inputs.workload_inputs(name))
     o, lse = chs.attn_fwd_lse(q, k, v)
@@ -528,14 +538,13 @@ def time_next_rows(chs, dev, flush, stream, peaks, l2):
     t = _time_throughput(fns, stream)
     lat = _time_launches(fns[0], flush, stream)
     fl = 2.5 * 4 * w["Dh"] * w["B"] * w["Hq"] * visible_pairs(w["S"], w["causal"], w["window"])
-    out["F4_backward"] = _row(fl, "TFLOP/s", t, lat, bf16, workload=name,
-                              input_copies=len(sets),
-                              flops="2.5 x the forward's (10*Dh per visible pair per head); "
-                                    "the kernels execute 14*Dh (S and dP in both passes)")
+    executed = "16*Dh (S in three passes, dP in two)" if w["Dh"] == 256 else \
+        "14*Dh (S and dP in both passes)"
+    row = _row(fl, "TFLOP/s", t, lat, bf16, workload=name, input_copies=len(sets),
+               flops="2.5 x the forward's (10*Dh per visible pair per head); "
+                     f"the kernels execute {executed}")
     del q, k, v, do, o, lse, dq, dk, dv, sets, fns
-    if chs.attn_status() != chs.ATTN_OK:
-        raise RuntimeError("device error while timing the next rows")
-    return out
+    return row
 
 
 def _host_us_per_call(fn, n=50):
