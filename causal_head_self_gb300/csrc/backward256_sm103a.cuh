@@ -82,17 +82,23 @@ __device__ __forceinline__ void bwd256_kblocks_of(const BwdParams& p, int qb, in
 
 // ============================================================ dV and dK passes
 
+// Stages: in the dV pass Q is read by S^T(n) alone and released after it, so
+// three Q stages keep S^T two steps ahead of its loads, and the per-row
+// statistics (read by the element-wise warps until P^T(n) is written) travel
+// with dO, released after dV(n).  In the dK pass Q is read by S^T(n) and
+// dK(n), dO by dP^T(n) alone; the statistics travel with Q.
 template <bool DK>
 struct __align__(1024) Bwd256KvSmem {
   using Cfg = Bwd256Cfg;
-  static constexpr int kStagesQ = 2;            // Q is read by S^T(n) and (dK pass) dK(n)
-  static constexpr int kStagesDO = DK ? 1 : 2;  // dO by dP^T(n) (dK pass) or dV(n)
+  static constexpr int kStagesQ = DK ? 2 : 3;
+  static constexpr int kStagesDO = DK ? 1 : 2;
+  static constexpr int kStagesStat = DK ? kStagesQ : kStagesDO;
   uint8_t k[Cfg::kBigTile];                     // this item's key block (stays)
-  uint8_t v[DK ? Cfg::kBigTile : 1024];         // its value block (dK pass; stays)
   uint8_t q[kStagesQ][Cfg::kSmallTile];         // query blocks
   uint8_t dO[kStagesDO][Cfg::kSmallTile];       // their output gradients
-  float lse2[kStagesQ][64];                     // their log-sum-exps (log2 units), with Q
-  float dlt[kStagesQ][64];                      // their D_i, with Q
+  uint8_t v[DK ? Cfg::kBigTile : 16];           // the value block (dK pass; stays)
+  float lse2[kStagesStat][64];                  // the blocks' log-sum-exps (log2 units)
+  float dlt[kStagesStat][64];                   // their D_i
   uint64_t kv_full, kv_empty;
   uint64_t q_full[kStagesQ], q_empty[kStagesQ];
   uint64_t do_full[kStagesDO], do_empty[kStagesDO];
@@ -156,22 +162,30 @@ __device__ __forceinline__ void bwd256_kv_producer(Bwd256KvSmem<DK>& sm, const B
         const bool in_range = attn_check(qb >= 0 && 64 * qb < p.S && bh >= 0 && bh < p.B * p.Hq &&
                                              row0 + 64 <= (size_t)p.B * p.Hq * p.S_pad,
                                          p.error_word);
+        // the per-row statistics ride with Q (dK pass) or dO (dV pass)
+        constexpr uint32_t kStatBytes = 2u * 256u;
         if (!(ok = mbar_wait(&sm.q_empty[st], ph ^ 1u, abort))) break;
-        mbar_arrive_expect_tx(&sm.q_full[st], in_range ? Cfg::kSmallTile + 2u * 256u : 0u);
+        mbar_arrive_expect_tx(&sm.q_full[st],
+                              in_range ? Cfg::kSmallTile + (DK ? kStatBytes : 0u) : 0u);
         for (int hf = 0; in_range && hf < 4; ++hf)
           tma_load_3d_hint(sm.q[st] + hf * Cfg::kSmallBox, map_q, &sm.q_full[st], 64 * hf,
                            64 * qb, bh, keep);
-        if (in_range) {
+        if (DK && in_range) {
           bulk_load(sm.lse2[st], p.lse2 + row0, 256, &sm.q_full[st], keep);
           bulk_load(sm.dlt[st], p.delta + row0, 256, &sm.q_full[st], keep);
         }
         q_loaded |= 1u << st;
         q_par = (q_par & ~(1u << st)) | (ph << st);
         if (!(ok = mbar_wait(&sm.do_empty[ds], dph ^ 1u, abort))) break;
-        mbar_arrive_expect_tx(&sm.do_full[ds], in_range ? (uint32_t)Cfg::kSmallTile : 0u);
+        mbar_arrive_expect_tx(&sm.do_full[ds],
+                              in_range ? Cfg::kSmallTile + (DK ? 0u : kStatBytes) : 0u);
         for (int hf = 0; in_range && hf < 4; ++hf)
           tma_load_3d_hint(sm.dO[ds] + hf * Cfg::kSmallBox, map_do, &sm.do_full[ds], 64 * hf,
                            64 * qb, bh, keep);
+        if (!DK && in_range) {
+          bulk_load(sm.lse2[ds], p.lse2 + row0, 256, &sm.do_full[ds], keep);
+          bulk_load(sm.dlt[ds], p.delta + row0, 256, &sm.do_full[ds], keep);
+        }
         d_loaded |= 1u << ds;
         d_par = (d_par & ~(1u << ds)) | (dph << ds);
       }
@@ -238,6 +252,7 @@ __device__ __forceinline__ void bwd256_kv_issuer(Bwd256KvSmem<DK>& sm, const Bwd
     tc_fence_after_sync();
     mma_s(Cfg::kColS + 64 * (x & 1u), dk_, dq_k + qst(x) * kStage);
     mma_commit_warp(&sm.s_full[x & 1u]);
+    if (!DK) mma_commit_warp(&sm.q_empty[qst(x)]);   // (dV pass: S^T is Q's only reader)
     if (DK) {
       if (!wait_all(&sm.do_full[dst(x)], dph(x))) return false;
       tc_fence_after_sync();
@@ -274,7 +289,6 @@ __device__ __forceinline__ void bwd256_kv_issuer(Bwd256KvSmem<DK>& sm, const Bwd
         if (!(ok = wait_all(&sm.do_full[dst(u)], dph(u)))) break;
         tc_fence_after_sync();
         mma_acc(Cfg::kColS + 64 * (u & 1u), ddo_mn + dst(u) * kStage, n == 0);   // dV += P^T dO
-        mma_commit_warp(&sm.q_empty[qst(u)]);
         mma_commit_warp(&sm.do_empty[dst(u)]);
       }
     }
@@ -311,10 +325,11 @@ __device__ __forceinline__ void bwd256_kv_softmax(Bwd256KvSmem<DK>& sm, const Bw
     const int j = 128 * I.kb + t;   // this thread's key
     for (int hh = 0; ok && hh < p.group; ++hh) {
       for (int qb = I.lo; qb <= I.hi; ++qb, ++u) {
-        const uint32_t st = u % Smem::kStagesQ;
+        const uint32_t st = u % Smem::kStagesStat;
         const uint32_t b = u & 1u;   // this step's score (and dP) buffer
-        // the stage's lse2 / D (bulk copies counted on q_full)
-        if (!(ok = mbar_wait(&sm.q_full[st], (u / Smem::kStagesQ) & 1u, abort))) break;
+        // the step's lse2 / D (bulk copies counted on the Q or the dO stage)
+        uint64_t* stat_full = DK ? &sm.q_full[st] : &sm.do_full[st];
+        if (!(ok = mbar_wait(stat_full, (u / Smem::kStagesStat) & 1u, abort))) break;
         if (!(ok = mbar_wait(&sm.s_full[b], (u >> 1) & 1u, abort))) break;
         tc_fence_after_sync();
         // visible query columns of key j: c in [clo, chi] (query i = 64 qb + 32 wg + c)
