@@ -144,7 +144,9 @@ __device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Pr
                                        p.error_word);
     mbar_arrive_expect_tx(&sm.q_full, q_in_range ? (uint32_t)Cfg::kQBytes : 0u);
     for (int hf = 0; q_in_range && hf < 4; ++hf)
-      tma_load_3d(sm.q + hf * Cfg::kQBox, map_q, &sm.q_full, hf * 64, tile.q0, tile.bh);
+      // (read once: evict-first, leaving L2 to the K/V tiles that are re-read)
+      tma_load_3d_hint(sm.q + hf * Cfg::kQBox, map_q, &sm.q_full, hf * 64, tile.q0, tile.bh,
+                       policy_evict_first());
     ++nq;
     for (int j = tile.lo; j <= tile.hi; ++j, ++t) {
       const int st = (int)(t % Cfg::kStagesK);
@@ -383,6 +385,9 @@ __device__ __forceinline__ void prefill256_softmax(Prefill256Smem& sm, const Pre
     // sum_j exp(s_ij) = 2^m_run * l_run (m_run in units of log2)
     if (p.lse != nullptr && store)
       p.lse[(size_t)tile.bh * p.Sq + orow] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+    // (the output is not read again by this kernel: evict-first, leaving L2
+    // to the K/V tiles the other query blocks re-read)
+    const uint64_t out_policy = policy_evict_first();
 #pragma unroll 1
     for (int c = 0; c < Cfg::DH / 32; c += 2) {
       uint32_t o0[32], o1[32];
@@ -400,7 +405,7 @@ __device__ __forceinline__ void prefill256_softmax(Prefill256Smem& sm, const Pre
         if (store) {
           uint4* d = dst + 2 * (2 * c + q);
           if (p.o_wide) {
-            st_global_v8(d, v);
+            st_global_v8_hint(d, v, out_policy);
           } else {
             d[0] = make_uint4(v[0], v[1], v[2], v[3]);
             d[1] = make_uint4(v[4], v[5], v[6], v[7]);

@@ -393,8 +393,10 @@ __device__ __forceinline__ void prefill_producer(PrefillSmem<DH>& sm, const Pref
                                        p.error_word);
       mbar_arrive_expect_tx(&sm.q_full[s], in_range ? (uint32_t)Cfg::kTileBytes : 0u);
       for (int hf = 0; in_range && hf < Cfg::kHalves; ++hf)
-        tma_load_3d(sm.q[s] + hf * Cfg::kBoxBytes, map_q, &sm.q_full[s], hf * 64,
-                    tile.row_first(s), item.bh);
+        // Q is read once: evict-first, so that it leaves the K/V tiles the
+        // other query blocks of the head re-read in L2
+        tma_load_3d_hint(sm.q[s] + hf * Cfg::kBoxBytes, map_q, &sm.q_full[s], hf * 64,
+                         tile.row_first(s), item.bh, policy_evict_first());
       ++n;
       return true;
     };
@@ -627,7 +629,9 @@ __device__ __forceinline__ void prefill_softmax(PrefillSmem<DH>& sm, const Prefi
       __syncwarp();
       // rows past the end of the chunk are clipped by the tensor map
       if (lane == 0) {
-        tma_store_3d(map_o, sm.ostage[warp], 64 * h, tile.row_first(s) + 32 * wl, bh);
+        // (evict-first: the output is not read again by this kernel)
+        tma_store_3d_hint(map_o, sm.ostage[warp], 64 * h, tile.row_first(s) + 32 * wl, bh,
+                          policy_evict_first());
         bulk_commit_group();
       }
     }

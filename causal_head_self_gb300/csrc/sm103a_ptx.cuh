@@ -155,6 +155,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 }
 
 // 1-D bulk copy global -> shared; `bytes` and both addresses are multiples of 16.
+// Same as tma_store_3d, with an L2 eviction-priority hint (createpolicy value).
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, const void* src, int c0,
+                                                  int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                           uint64_t policy) {
   asm volatile(
@@ -440,6 +450,13 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
                   "r"(w[6]), "r"(w[7]) : "memory");
+}
+
+// The same with an L2 eviction-priority hint (createpolicy value).
+__device__ __forceinline__ void st_global_v8_hint(void* p, const uint32_t (&w)[8], uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+               :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                  "r"(w[6]), "r"(w[7]), "l"(policy) : "memory");
 }
 
 // x if off <= span (unsigned), else -inf: a predicated select, so that a
