@@ -418,6 +418,24 @@ def _copies(n, *ts):
     return [tuple(ts)] + [tuple(t.clone() for t in ts) for _ in range(n - 1)]
 
 
+def _packed(ts, dev):
+    """((pinned host buffer, device buffer), device views): the tensors ts back
+    to back (each at a 256-byte boundary) in one pinned host buffer, and views
+    of the same layout into one device buffer of that size."""
+    offs, n = [], 0
+    for t in ts:
+        offs.append(n)
+        n += (t.numel() * t.element_size() + 255) // 256 * 256
+    host = torch.empty(n, dtype=torch.uint8).pin_memory()
+    devbuf = torch.empty(n, dtype=torch.uint8, device=dev)
+    views = []
+    for t, off in zip(ts, offs):
+        nb = t.numel() * t.element_size()
+        host[off:off + nb].view(t.dtype).view(t.shape).copy_(t)
+        views.append(devbuf[off:off + nb].view(t.dtype).view(t.shape))
+    return (host, devbuf), views
+
+
 def _row(work, unit, per_launch, lat, peak=None, **extra):
     """One timed row: throughput from back-to-back launches, latency beside it."""
     val = work / per_launch / (1e12 if unit == "TFLOP/s" else 1e9)
@@ -638,27 +656,26 @@ def run_gpu(args, rank, world, local_rank):
                "attn_decode": _host_us_per_call(lambda: decode(0))}
 
     # ---------------------------------------------------------- end to end (host buffers)
+    # A step's inputs sit back to back in one pinned host buffer and cross to
+    # the device in one copy, into one device buffer that q, k and v (and for
+    # the decode the cache and the lengths) are views of: one large transfer
+    # runs at the host link's rate, several small ones below it.
     e2e_steps = max(3, min(20, args.steps))
-    qp, kp, vp = (x.pin_memory() for x in (qh, kh, vh))
+    hp, (qe, ke, ve) = _packed((qh, kh, vh), dev)
     op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    qdp, kcp, vcp, slp = (x.pin_memory() for x in (qdh, kch, vch, slh))
+    hd, (qde, kce, vce, sle) = _packed((qdh, kch, vch, slh), dev)
     odp = torch.empty(od.shape, dtype=od.dtype).pin_memory()
     e2e_p, e2e_d = [], []
     for i in range(e2e_steps + 2):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         flush.zero_()
         e[0].record(stream)
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
-        chs.attn_fwd(q, k, v, o, causal=bool(w_p["causal"]), window=w_p["window"])
+        hp[1].copy_(hp[0], non_blocking=True)
+        chs.attn_fwd(qe, ke, ve, o, causal=bool(w_p["causal"]), window=w_p["window"])
         op.copy_(o, non_blocking=True)
         e[1].record(stream)
-        qd.copy_(qdp, non_blocking=True)
-        kc.copy_(kcp, non_blocking=True)
-        vc.copy_(vcp, non_blocking=True)
-        sl.copy_(slp, non_blocking=True)
-        chs.attn_decode(qd, kc, vc, sl, od, window=w_d["window"])
+        hd[1].copy_(hd[0], non_blocking=True)
+        chs.attn_decode(qde, kce, vce, sle, od, window=w_d["window"])
         odp.copy_(od, non_blocking=True)
         e[2].record(stream)
         torch.cuda.synchronize(dev)
@@ -671,7 +688,8 @@ def run_gpu(args, rank, world, local_rank):
     tp_e2e, td_e2e = max_over_ranks([tp_e2e, td_e2e], world, dev)
     if rank != 0:
         return None
-    del qp, kp, vp, op, qdp, kcp, vcp, slp, odp
+    h2d_p, h2d_d = hp[0].numel(), hd[0].numel()   # bytes per step, padding included
+    del hp, hd, qe, ke, ve, qde, kce, vce, sle, op, odp
     peaks, peak_src = read_peaks()
     shapes = time_prefill_configs(chs, dev, flush, stream, peaks, l2)
     extras = time_next_rows(chs, dev, flush, stream, peaks, l2)
@@ -742,11 +760,10 @@ def run_gpu(args, rank, world, local_rank):
         "rooflines": {"prefill": roof_p, "decode": roof_d},
         "cpu_baseline": cpu,
         "e2e": {"value": job_rate(pf, tp_e2e, world) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (qh, kh, vh)),
+                "h2d_bytes_per_step": h2d_p,
                 "d2h_bytes_per_step": o.numel() * o.element_size(),
                 "decode": {"value": job_rate(db, td_e2e, world) / 1e9, "unit": "GB/s",
-                           "h2d_bytes_per_step": sum(x.numel() * x.element_size()
-                                                     for x in (qdh, kch, vch, slh)),
+                           "h2d_bytes_per_step": h2d_d,
                            "d2h_bytes_per_step": od.numel() * od.element_size()}},
         "prefill_shapes": shapes,
         "next_rows": extras,
