@@ -41,6 +41,9 @@ WORKLOADS = {
     # the backward pass at head size 256 (the causal GQA prefill at Dh=256)
     "backward_gqa_b1_h16kv8_s8192_d256": dict(kind="backward", B=1, Hq=16, Hkv=8, S=8192, Dh=256,
                                               causal=True, window=0, seed=6),
+    # the Dh=256 backward on 4 query heads over 2 K/V heads at S=4096 (a profiler-sized case)
+    "backward_gqa_b1_h4kv2_s4096_d256": dict(kind="backward", B=1, Hq=4, Hkv=2, S=4096, Dh=256,
+                                             causal=True, window=0, seed=6),
     # the S=4096 backward on 8 heads (a profiler-sized case)
     "backward_mha_b1_h8_s4096_d128": dict(kind="backward", B=1, Hq=8, Hkv=8, S=4096, Dh=128,
                                           causal=True, window=0, seed=2),
