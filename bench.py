@@ -701,7 +701,8 @@ def run_gpu(args, rank, world, local_rank):
     dec_launch = t_dec / K
     pre_tflops = pf / pre_launch / 1e12
     dec_gbs = db / dec_launch / 1e9
-    kp_name = "attn_prefill_sm103a<128>"
+    # (head size 128 at 1024 keys per head runs on the 64-key-tile kernel)
+    kp_name = "attn_prefill_k64_sm103a<128>"
     kd_name = "attn_decode_tc_sm103a<128>"
     roof_p = {"kernel": kp_name, "bound": "tensor", "achieved": pre_tflops,
               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",

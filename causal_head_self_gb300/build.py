@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libattn_sm103a.so")
 BUILD_CHECK = os.path.join(PKG, "_build_check")
 LIB_CHECK = os.path.join(PKG, "libattn_sm103a_check.so")
 SOURCES = ["attn_api.cu", "prefill_sm103a.cu", "decode_sm103a.cu", "backward_sm103a.cu"]
-HEADERS = ["sm103a_ptx.cuh", "prefill_sm103a.cuh", "prefill256_sm103a.cuh", "decode_sm103a.cuh",
+HEADERS = ["sm103a_ptx.cuh", "prefill_sm103a.cuh", "prefill_k64_sm103a.cuh", "decode_sm103a.cuh",
            "decode_tc_sm103a.cuh", "backward_sm103a.cuh", "backward256_sm103a.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

@@ -1,23 +1,31 @@
-// prefill256_sm103a.cuh -- causal prefill at head size 256 (the Gemma head
-// size) on the 5th-generation tensor cores (sm_103a).
+// prefill_k64_sm103a.cuh -- causal prefill with one 128-row sub-tile per
+// work item and 64-key tiles, on the 5th-generation tensor cores (sm_103a).
+// Two instances:
 //
-// At Dh = 256 the accumulator O of one 128-row sub-tile takes 256 of the 512
-// tensor-memory columns, so the two-sub-tile ping-pong of the Dh <= 128
-// kernel does not fit.  This kernel runs one 128-row sub-tile per work item
-// and keeps the tensor core busy differently: S is double-buffered, so the
-// S MMA of the next key tile runs while the softmax works on the current one.
-// Key tiles are 64 keys wide, so that Q (64 KiB), a two-stage K ring and a
-// three-stage V ring of 32 KiB tiles fit in shared memory (224 KiB; the third
-// V stage lets a V tile load while the two P.V before it run); tensor memory
-// holds S0 [0,64),
-// S1 [64,128) and O [256,512).  P (bf16) is written over the first 32 columns
-// of its S buffer and read from there by the P.V MMA.
+//   Dh = 256 (the Gemma head size).  The accumulator O of one 128-row
+//   sub-tile takes 256 of the 512 tensor-memory columns, so the two-sub-tile
+//   ping-pong of the Dh <= 128 kernel does not fit.  One CTA per SM: Q
+//   (64 KiB), a two-stage K ring and a three-stage V ring of 32 KiB tiles
+//   (224 KiB; the third V stage lets a V tile load while the two P.V before
+//   it run); tensor memory S0 [0,64), S1 [64,128), O [256,512).
 //
-// The kernel is persistent (one CTA per SM walking 128-row items, heaviest
-// first) with the roles of the Dh <= 128 kernel: one thread issues every TMA
-// load, one warp issues every MMA, four warps run the softmax and the
-// epilogue (thread t owns row t).  Masks, the lazy maximum and the
-// chunked-prefill offset follow that kernel.  Every wait is bounded.
+//   Dh = 128, short sequences.  Two CTAs per SM, each with half of the
+//   shared memory (Q 32 KiB, two-stage K and V rings of 16 KiB tiles) and
+//   half of the tensor memory (S0 [0,64), S1 [64,128), O [128,256) from its
+//   allocation's base).  When every CTA has only one or two short items, the
+//   fixed cost of an item (its first loads, the masked diagonal tiles, the
+//   epilogue) dominates the ping-pong kernel's time; here the other CTA on
+//   the SM keeps the tensor core busy through it.
+//
+// S is double-buffered, so the S MMA of the next key tile runs while the
+// softmax works on the current one.  P (bf16) is written over the first 32
+// columns of its S buffer and read from there by the P.V MMA.
+//
+// The kernel is persistent (CTAs walk 128-row items, heaviest first) with the
+// roles of the Dh <= 128 kernel: one thread issues every TMA load, one warp
+// issues every MMA, four warps run the softmax and the epilogue (thread t owns
+// row t).  Masks, the lazy maximum and the chunked-prefill offset follow that
+// kernel.  Every wait is bounded.
 #pragma once
 
 #include <cstdint>
@@ -28,7 +36,7 @@
 
 namespace chs {
 
-struct Prefill256Params {
+struct PrefillK64Params {
   int B, Hq, Hkv;
   int Sq, Skv, q_off;   // as in the Dh <= 128 kernel
   int causal, window;
@@ -37,29 +45,37 @@ struct Prefill256Params {
   int num_items;        // num_qblocks * B * Hq
   int per_qb;           // B * Hq
   int group;            // Hq / Hkv
-  __nv_bfloat16* o;     // [B, Hq, Sq, 256]
+  __nv_bfloat16* o;     // [B, Hq, Sq, Dh]
   int o_wide;           // o is 32-byte aligned: 32-byte stores
   float* lse;           // optional [B, Hq, Sq]: log sum_j exp(s_ij) per row (natural log)
   int* error_word;
   int fault;            // test hook: 1 = the first K tile is never loaded
 };
 
-struct Prefill256Cfg {
-  static constexpr int DH = 256;
+template <int DH_>
+struct PrefillK64Cfg {
+  static_assert(DH_ == 128 || DH_ == 256, "head size 128 or 256");
+  static constexpr int DH = DH_;
+  static constexpr int kBoxes = DH / 64;               // 64-column boxes per row
   static constexpr int kKeys = 64;                     // keys per tile
   static constexpr int kQBox = 128 * 64 * 2;           // Q box: 128 rows x 64 columns
   static constexpr int kKBox = kKeys * 64 * 2;         // K/V box: 64 rows x 64 columns
-  static constexpr int kQBytes = 4 * kQBox;            // 64 KiB
-  static constexpr int kTileBytes = 4 * kKBox;         // 32 KiB
+  static constexpr int kQBytes = kBoxes * kQBox;       // 32 / 64 KiB
+  static constexpr int kTileBytes = kBoxes * kKBox;    // 16 / 32 KiB
   static constexpr int kStagesK = 2;   // K tiles: S(t) is issued two tiles ahead
-  static constexpr int kStagesV = 3;   // V tiles: a third stage hides the load behind two P.V
+  // V tiles: at Dh 256 a third stage hides the load behind two P.V
+  static constexpr int kStagesV = DH == 256 ? 3 : 2;
+  static constexpr int kCtasPerSm = DH == 256 ? 1 : 2;
+  static constexpr uint32_t kTmemCols = DH == 256 ? 512 : 256;   // this CTA's allocation
   static constexpr int kThreads = 192;   // warps 0-3 softmax, 4 producer, 5 MMA issuer
   static constexpr int kWarpProducer = 4, kWarpIssuer = 5;
-  static constexpr uint32_t kColS = 0, kColO = 256;    // S buffer b at kColS + 64 b
+  // S buffer b at kColS + 64 b, O in the allocation's last DH columns
+  static constexpr uint32_t kColS = 0, kColO = kTmemCols - DH;
 };
 
-struct __align__(1024) Prefill256Smem {
-  using Cfg = Prefill256Cfg;
+template <int DH>
+struct __align__(1024) PrefillK64Smem {
+  using Cfg = PrefillK64Cfg<DH>;
   uint8_t q[Cfg::kQBytes];
   uint8_t k[Cfg::kStagesK][Cfg::kTileBytes];
   uint8_t v[Cfg::kStagesV][Cfg::kTileBytes];
@@ -73,15 +89,15 @@ struct __align__(1024) Prefill256Smem {
 
 // Geometry of one 128-row work item: query rows [q0, q0 + 128) of the chunk,
 // at positions q_off + row; key tiles lo..hi of 64 keys.
-struct Prefill256Tile {
+struct PrefillK64Tile {
   int q0, lo, hi;
   int bh, bh_kv;
-  __device__ __forceinline__ int pos_first(const Prefill256Params& p) const { return p.q_off + q0; }
-  __device__ __forceinline__ int pos_last(const Prefill256Params& p) const {
+  __device__ __forceinline__ int pos_first(const PrefillK64Params& p) const { return p.q_off + q0; }
+  __device__ __forceinline__ int pos_last(const PrefillK64Params& p) const {
     return p.q_off + min(q0 + 127, p.Sq - 1);
   }
   // is any (row, key) pair of tile j masked?
-  __device__ __forceinline__ bool needs_mask(const Prefill256Params& p, int j) const {
+  __device__ __forceinline__ bool needs_mask(const PrefillK64Params& p, int j) const {
     const int c0 = 64 * j, c1 = 64 * j + 63;
     if (c1 >= p.Skv) return true;
     if (p.causal && c1 > pos_first(p)) return true;
@@ -92,12 +108,22 @@ struct Prefill256Tile {
 
 // Item w: heaviest query blocks first (causal work grows with the block),
 // dealt to the CTAs in snake order (see the Dh <= 128 kernel).
-__device__ __forceinline__ int prefill256_item(int k, int c, int G) {
+__device__ __forceinline__ int prefill_k64_item(int k, int c, int G) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
-__device__ __forceinline__ Prefill256Tile prefill256_tile_of(const Prefill256Params& p, int w) {
-  Prefill256Tile t;
+// The k-th work item of this CTA (num_items or more: none left).  With at
+// most two items per CTA the lighter one goes first, as in the Dh <= 128
+// kernel: its latency-bound chain then overlaps the start of the long item.
+__device__ __forceinline__ int prefill_k64_cta_item(int k, int num_items) {
+  const int G = gridDim.x, c = blockIdx.x;
+  if (num_items > 2 * G) return prefill_k64_item(k, c, G);
+  const int n = num_items > G ? 1 + (prefill_k64_item(1, c, G) < num_items ? 1 : 0) : 1;
+  return k < n ? prefill_k64_item(n - 1 - k, c, G) : num_items;
+}
+
+__device__ __forceinline__ PrefillK64Tile prefill_k64_tile_of(const PrefillK64Params& p, int w) {
+  PrefillK64Tile t;
   const int blk = w / p.per_qb;
   const int qb = p.num_qblocks - 1 - blk;
   t.bh = w - blk * p.per_qb;
@@ -111,7 +137,7 @@ __device__ __forceinline__ Prefill256Tile prefill256_tile_of(const Prefill256Par
   return t;
 }
 
-__device__ __forceinline__ void mbar_wait_drain_256(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_wait_drain_k64(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(a, parity)) {
@@ -119,31 +145,32 @@ __device__ __forceinline__ void mbar_wait_drain_256(uint64_t* bar, uint32_t pari
   }
 }
 
-// TMA producer (one thread): per item, Q (four 128 x 64 boxes) once its
-// previous item's last S is done, then the item's K and V tiles (four
-// 64 x 64 boxes each) through two-stage rings.
-__device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Prefill256Params& p,
+// TMA producer (one thread): per item, Q (Dh/64 boxes of 128 x 64) once its
+// previous item's last S is done, then the item's K and V tiles (Dh/64 boxes
+// of 64 x 64 each) through the K and V rings.
+template <int DH>
+__device__ __forceinline__ void prefill_k64_producer(PrefillK64Smem<DH>& sm, const PrefillK64Params& p,
                                                     const CUtensorMap* map_q,
                                                     const CUtensorMap* map_k,
                                                     const CUtensorMap* map_v,
                                                     volatile int* abort) {
-  using Cfg = Prefill256Cfg;
+  using Cfg = PrefillK64Cfg<DH>;
   const uint64_t keep = policy_evict_last();   // K/V tiles are re-read by other items
   uint32_t t = 0;                              // K/V tiles loaded so far
   uint32_t k_loaded = 0, k_par = 0, v_loaded = 0, v_par = 0;
   int nq = 0;
   bool ok = true;
   for (int it = 0; ok; ++it) {
-    const int w = prefill256_item(it, blockIdx.x, gridDim.x);
+    const int w = prefill_k64_cta_item(it, p.num_items);
     if (w >= p.num_items) break;
-    const Prefill256Tile tile = prefill256_tile_of(p, w);
+    const PrefillK64Tile tile = prefill_k64_tile_of(p, w);
     if (nq > 0 && !(ok = mbar_wait(&sm.q_empty, (uint32_t)(nq - 1) & 1u, abort))) break;
     // (checked builds: a query row of the chunk and a query head of the batch)
     const bool q_in_range = attn_check(tile.q0 >= 0 && tile.q0 < p.Sq && tile.bh >= 0 &&
                                            tile.bh < p.B * p.Hq,
                                        p.error_word);
     mbar_arrive_expect_tx(&sm.q_full, q_in_range ? (uint32_t)Cfg::kQBytes : 0u);
-    for (int hf = 0; q_in_range && hf < 4; ++hf)
+    for (int hf = 0; q_in_range && hf < Cfg::kBoxes; ++hf)
       // (read once: evict-first, leaving L2 to the K/V tiles that are re-read)
       tma_load_3d_hint(sm.q + hf * Cfg::kQBox, map_q, &sm.q_full, hf * 64, tile.q0, tile.bh,
                        policy_evict_first());
@@ -159,7 +186,7 @@ __device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Pr
       if (!(ok = mbar_wait(&sm.k_empty[st], ph ^ 1u, abort))) break;
       mbar_arrive_expect_tx(&sm.k_full[st], bytes);
       if (p.fault != 1 || it != 0 || j != tile.lo) {   // (the test hook withholds one tile)
-        for (int hf = 0; in_range && hf < 4; ++hf)
+        for (int hf = 0; in_range && hf < Cfg::kBoxes; ++hf)
           tma_load_3d_hint(sm.k[st] + hf * Cfg::kKBox, map_k, &sm.k_full[st], hf * 64, 64 * j,
                            tile.bh_kv, keep);
       }
@@ -169,7 +196,7 @@ __device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Pr
       const uint32_t pv = (t / Cfg::kStagesV) & 1u;
       if (!(ok = mbar_wait(&sm.v_empty[sv], pv ^ 1u, abort))) break;
       mbar_arrive_expect_tx(&sm.v_full[sv], bytes);
-      for (int hf = 0; in_range && hf < 4; ++hf)
+      for (int hf = 0; in_range && hf < Cfg::kBoxes; ++hf)
         tma_load_3d_hint(sm.v[sv] + hf * Cfg::kKBox, map_v, &sm.v_full[sv], hf * 64, 64 * j,
                          tile.bh_kv, keep);
       v_loaded |= 1u << sv;
@@ -177,11 +204,11 @@ __device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Pr
     }
   }
   // every copy this thread started has landed before the CTA may exit
-  if (nq > 0) mbar_wait_drain_256(&sm.q_full, (uint32_t)(nq - 1) & 1u);
+  if (nq > 0) mbar_wait_drain_k64(&sm.q_full, (uint32_t)(nq - 1) & 1u);
   for (int i = 0; i < Cfg::kStagesK; ++i)
-    if (k_loaded & (1u << i)) mbar_wait_drain_256(&sm.k_full[i], (k_par >> i) & 1u);
+    if (k_loaded & (1u << i)) mbar_wait_drain_k64(&sm.k_full[i], (k_par >> i) & 1u);
   for (int i = 0; i < Cfg::kStagesV; ++i)
-    if (v_loaded & (1u << i)) mbar_wait_drain_256(&sm.v_full[i], (v_par >> i) & 1u);
+    if (v_loaded & (1u << i)) mbar_wait_drain_k64(&sm.v_full[i], (v_par >> i) & 1u);
 }
 
 // MMA issuer (one converged warp, one elected lane per instruction).  Per
@@ -189,9 +216,10 @@ __device__ __forceinline__ void prefill256_producer(Prefill256Smem& sm, const Pr
 // written, and S(t+2) into the buffer P(t) lived in (the tensor core runs one
 // thread's MMAs in order).  The first P.V of an item overwrites O: the
 // softmax threads publish that P only after their epilogue has read O.
-__device__ __forceinline__ void prefill256_issuer(Prefill256Smem& sm, const Prefill256Params& p,
-                                                  volatile int* abort) {
-  using Cfg = Prefill256Cfg;
+template <int DH>
+__device__ __forceinline__ void prefill_k64_issuer(PrefillK64Smem<DH>& sm, const PrefillK64Params& p,
+                                                   uint32_t tbase, volatile int* abort) {
+  using Cfg = PrefillK64Cfg<DH>;
   constexpr uint32_t idesc_qk = idesc_bf16_f32(128, Cfg::kKeys, false, false);
   constexpr uint32_t idesc_pv = idesc_bf16_f32(128, Cfg::DH, false, true);
   constexpr uint64_t kKmajor = smem_desc_sw128(0, 16, 1024);            // Q, K
@@ -199,14 +227,13 @@ __device__ __forceinline__ void prefill256_issuer(Prefill256Smem& sm, const Pref
   const uint64_t dq = kKmajor | (smem_u32(sm.q) >> 4);
   const uint64_t dk = kKmajor | (smem_u32(sm.k[0]) >> 4);
   const uint64_t dv = kMnMajor | (smem_u32(sm.v[0]) >> 4);
-  // the CTA owns all 512 columns, so its allocation starts at column 0
-  constexpr uint32_t dO = Cfg::kColO;
+  const uint32_t dO = tbase + Cfg::kColO;
   auto issue_s = [&](uint32_t t) -> bool {
     const int st = (int)(t % Cfg::kStagesK);
     const uint32_t ph = (t / Cfg::kStagesK) & 1u;
     if (!__all_sync(0xffffffffu, mbar_wait(&sm.k_full[st], ph, abort))) return false;
     tc_fence_after_sync();
-    const uint32_t dS = Cfg::kColS + 64u * (t & 1u);
+    const uint32_t dS = tbase + Cfg::kColS + 64u * (t & 1u);
     const uint64_t b = dk + (uint64_t)(st * (Cfg::kTileBytes >> 4));
 #pragma unroll
     for (int kk = 0; kk < Cfg::DH / 16; ++kk) {
@@ -223,9 +250,9 @@ __device__ __forceinline__ void prefill256_issuer(Prefill256Smem& sm, const Pref
   int nq = 0;
   bool ok = true;
   for (int it = 0; ok; ++it) {
-    const int w = prefill256_item(it, blockIdx.x, gridDim.x);
+    const int w = prefill_k64_cta_item(it, p.num_items);
     if (w >= p.num_items) break;
-    const Prefill256Tile tile = prefill256_tile_of(p, w);
+    const PrefillK64Tile tile = prefill_k64_tile_of(p, w);
     const int n = tile.hi - tile.lo + 1;
     if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, (uint32_t)nq & 1u, abort)))) break;
     ++nq;
@@ -241,7 +268,7 @@ __device__ __forceinline__ void prefill256_issuer(Prefill256Smem& sm, const Pref
         break;
       tc_fence_after_sync();
       // O (+)= P V: P from TMEM (8 columns = 16 keys per MMA), V MN-major
-      const uint32_t dP = Cfg::kColS + 64u * (t & 1u);
+      const uint32_t dP = tbase + Cfg::kColS + 64u * (t & 1u);
       const uint64_t b = dv + (uint64_t)(st * (Cfg::kTileBytes >> 4));
 #pragma unroll
       for (int kk = 0; kk < Cfg::kKeys / 16; ++kk)
@@ -258,16 +285,17 @@ __device__ __forceinline__ void prefill256_issuer(Prefill256Smem& sm, const Pref
   }
   // nothing of this warp's may still run on the tensor core at teardown
   mma_commit_warp(&sm.mma_done);
-  mbar_wait_drain_256(&sm.mma_done, 0);
+  mbar_wait_drain_k64(&sm.mma_done, 0);
 }
 
 // Softmax and epilogue (warps 0-3; thread t owns row t of the item, TMEM lane
 // t): the online softmax of "Online normalizer calculation for softmax" with
 // the lazy maximum of the Dh <= 128 kernel, 64 scores per tile.
-__device__ __forceinline__ void prefill256_softmax(Prefill256Smem& sm, const Prefill256Params& p,
-                                                   uint32_t tbase, volatile int* abort, int warp,
-                                                   int lane) {
-  using Cfg = Prefill256Cfg;
+template <int DH>
+__device__ __forceinline__ void prefill_k64_softmax(PrefillK64Smem<DH>& sm, const PrefillK64Params& p,
+                                                    uint32_t tbase, volatile int* abort, int warp,
+                                                    int lane) {
+  using Cfg = PrefillK64Cfg<DH>;
   const int t = warp * 32 + lane;
   const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
   const uint32_t colO = lane_addr + Cfg::kColO;
@@ -276,9 +304,9 @@ __device__ __forceinline__ void prefill256_softmax(Prefill256Smem& sm, const Pre
   uint32_t items = 0;   // items finished (o_final phases)
   bool ok = true;
   for (int it = 0; ok; ++it) {
-    const int w = prefill256_item(it, blockIdx.x, gridDim.x);
+    const int w = prefill_k64_cta_item(it, p.num_items);
     if (w >= p.num_items) break;
-    const Prefill256Tile tile = prefill256_tile_of(p, w);
+    const PrefillK64Tile tile = prefill_k64_tile_of(p, w);
     const int row = tile.pos_first(p) + t;   // this thread's query position
 
     float m_run = -INFINITY, l_run = 0.f;
@@ -374,7 +402,7 @@ __device__ __forceinline__ void prefill256_softmax(Prefill256Smem& sm, const Pre
     }
     if (!ok) break;
 
-    // ---- epilogue: O / l -> bf16 -> output row, 512 bytes per row
+    // ---- epilogue: O / l -> bf16 -> output row, 2 Dh bytes per row
     if (!(ok = mbar_wait(&sm.o_final, items & 1u, abort))) break;
     ++items;
     tc_fence_after_sync();
@@ -418,13 +446,14 @@ __device__ __forceinline__ void prefill256_softmax(Prefill256Smem& sm, const Pre
   }
 }
 
-__global__ void __launch_bounds__(Prefill256Cfg::kThreads, 1)
-    attn_prefill256_sm103a(const __grid_constant__ CUtensorMap map_q,
-                           const __grid_constant__ CUtensorMap map_k,
-                           const __grid_constant__ CUtensorMap map_v, const Prefill256Params p) {
-  using Cfg = Prefill256Cfg;
+template <int DH>
+__global__ void __launch_bounds__(PrefillK64Cfg<DH>::kThreads, PrefillK64Cfg<DH>::kCtasPerSm)
+    attn_prefill_k64_sm103a(const __grid_constant__ CUtensorMap map_q,
+                            const __grid_constant__ CUtensorMap map_k,
+                            const __grid_constant__ CUtensorMap map_v, const PrefillK64Params p) {
+  using Cfg = PrefillK64Cfg<DH>;
   extern __shared__ uint8_t smem_raw[];
-  Prefill256Smem& sm = *reinterpret_cast<Prefill256Smem*>(
+  PrefillK64Smem<DH>& sm = *reinterpret_cast<PrefillK64Smem<DH>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   volatile int* abort = &sm.abort_flag;
   const int warp = threadIdx.x / 32;
@@ -457,29 +486,26 @@ __global__ void __launch_bounds__(Prefill256Cfg::kThreads, 1)
     fence_mbarrier_init();
   }
   if (warp == Cfg::kWarpProducer) {
-    tmem_alloc(&sm.tmem_base, 512);
+    tmem_alloc(&sm.tmem_base, Cfg::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   // global memory only after the previous kernel in the stream is complete;
-  // this grid (one CTA per SM, all of its shared memory) leaves the next
-  // kernel nothing to take, so it may be launched now
+  // this grid (its CTAs take nearly all of the shared memory of their SMs)
+  // leaves the next kernel little to take, so it may be launched now
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
+  // every tensor-memory address is relative to this CTA's allocation (at
+  // Dh 128 two CTAs share an SM's 512 columns)
   const uint32_t tbase = sm.tmem_base;
-  // the issuer's tensor-memory addresses are compile-time: all 512 columns
-  // are this CTA's, so the allocation must start at column 0
-  if (tbase != 0 && threadIdx.x == 0) sm.abort_flag = 1;
-  if (tbase == 0) {
-    if (warp == Cfg::kWarpProducer) {
-      if (lane == 0) prefill256_producer(sm, p, &map_q, &map_k, &map_v, abort);
-    } else if (warp == Cfg::kWarpIssuer) {
-      prefill256_issuer(sm, p, abort);
-    } else {
-      prefill256_softmax(sm, p, tbase, abort, warp, lane);
-    }
+  if (warp == Cfg::kWarpProducer) {
+    if (lane == 0) prefill_k64_producer<DH>(sm, p, &map_q, &map_k, &map_v, abort);
+  } else if (warp == Cfg::kWarpIssuer) {
+    prefill_k64_issuer<DH>(sm, p, tbase, abort);
+  } else {
+    prefill_k64_softmax<DH>(sm, p, tbase, abort, warp, lane);
   }
 
   // ---- teardown (every wait above is bounded)
@@ -488,13 +514,19 @@ __global__ void __launch_bounds__(Prefill256Cfg::kThreads, 1)
   __syncthreads();
   if (warp == Cfg::kWarpProducer) {
     tc_fence_after_sync();
-    tmem_dealloc(tbase, 512);
+    tmem_dealloc(tbase, Cfg::kTmemCols);
   }
   if (threadIdx.x == 0 && sm.abort_flag) atomicExch(p.error_word, 4);   // ATTN_ERR_TIMEOUT
 }
 
-constexpr size_t prefill256_smem_bytes() {
-  return sizeof(Prefill256Smem) + 1024;   // + alignment slack
+template <int DH>
+constexpr size_t prefill_k64_smem_bytes() {
+  return sizeof(PrefillK64Smem<DH>) + 1024;   // + alignment slack
 }
+
+// two CTAs per SM at Dh 128: each takes under half of the SM's 228 KiB
+// (1 KiB of it reserved per CTA)
+static_assert(prefill_k64_smem_bytes<128>() <= 113 * 1024, "Dh 128: two CTAs per SM");
+static_assert(prefill_k64_smem_bytes<256>() <= 227 * 1024, "Dh 256: one CTA per SM");
 
 }  // namespace chs

@@ -1,6 +1,6 @@
-// prefill_sm103a.cu -- host launcher of the tcgen05 prefill kernel.
+// prefill_sm103a.cu -- host launchers of the tcgen05 prefill kernels.
 #include "launch.h"
-#include "prefill256_sm103a.cuh"
+#include "prefill_k64_sm103a.cuh"
 #include "prefill_sm103a.cuh"
 
 namespace chs {
@@ -44,19 +44,21 @@ static FastDiv make_fast_div(uint32_t d) {
   return FastDiv{(uint32_t)m, 31 + l, d};
 }
 
-// Head size 256: one 128-row sub-tile per work item, 64-key tiles.
-static cudaError_t launch_prefill256(const void* q, const void* k, const void* v, void* o,
-                                     float* lse, int B, int Hq, int Hkv, int Sq, int Tkv,
-                                     int start_pos, int causal, int window, float scale_log2,
-                                     const DeviceInfo& dev, cudaStream_t stream) {
-  using Cfg = Prefill256Cfg;
+// One 128-row sub-tile per work item, 64-key tiles: head size 256, and head
+// size 128 on short sequences (two CTAs per SM).
+template <int DH>
+static cudaError_t launch_prefill_k64(const void* q, const void* k, const void* v, void* o,
+                                      float* lse, int B, int Hq, int Hkv, int Sq, int Tkv,
+                                      int start_pos, int causal, int window, float scale_log2,
+                                      const DeviceInfo& dev, cudaStream_t stream) {
+  using Cfg = PrefillK64Cfg<DH>;
   const int Skv = start_pos + Sq;
   CUtensorMap mq, mk, mv;
   if (!encode_bf16_map(&mq, q, Cfg::DH, Sq, (long long)B * Hq, 128) ||
       !encode_bf16_map(&mk, k, Cfg::DH, Skv, (long long)B * Hkv, Cfg::kKeys, Tkv) ||
       !encode_bf16_map(&mv, v, Cfg::DH, Skv, (long long)B * Hkv, Cfg::kKeys, Tkv))
     return cudaErrorInvalidValue;
-  Prefill256Params prm;
+  PrefillK64Params prm;
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
@@ -77,26 +79,35 @@ static cudaError_t launch_prefill256(const void* q, const void* k, const void* v
   prm.lse = lse;
   prm.error_word = dev.error_word;
   prm.fault = dev.fault;
-  constexpr size_t smem = prefill256_smem_bytes();
-  static_assert(smem <= 232448, "shared memory budget of one sm_103a CTA");
+  constexpr size_t smem = prefill_k64_smem_bytes<DH>();
   static std::atomic<int> configured[kMaxDevices];
   cudaError_t e = configure_once(configured, dev.device, [] {
-    return cudaFuncSetAttribute(attn_prefill256_sm103a,
+    return cudaFuncSetAttribute(attn_prefill_k64_sm103a<DH>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (e != cudaSuccess) return e;
-  const int grid = prm.num_items < dev.num_sms ? prm.num_items : dev.num_sms;
-  return launch_pdl(attn_prefill256_sm103a, dim3(grid), dim3(Cfg::kThreads), smem, stream, mq,
-                    mk, mv, prm);
+  // persistent: as many CTAs as the SMs hold at once
+  const int cap = Cfg::kCtasPerSm * dev.num_sms;
+  const int grid = prm.num_items < cap ? prm.num_items : cap;
+  return launch_pdl(attn_prefill_k64_sm103a<DH>, dim3(grid), dim3(Cfg::kThreads), smem, stream,
+                    mq, mk, mv, prm);
 }
+
+// Head size 128 takes the two-CTA 64-key kernel up to this many keys per
+// head (measured on GB300: 7 % faster at 1024 keys, even at 2048, 12-15 %
+// slower from 4096 on, where the ping-pong kernel's 128-key MMAs win).
+constexpr int kPrefillK64MaxKeys128 = 1536;
 
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int Hq, int Hkv, int Sq, int Tkv, int start_pos, int Dh,
                            int causal, int window, float scale_log2, const DeviceInfo& dev,
                            cudaStream_t stream) {
   if (Dh == 256)
-    return launch_prefill256(q, k, v, o, lse, B, Hq, Hkv, Sq, Tkv, start_pos, causal, window,
-                             scale_log2, dev, stream);
+    return launch_prefill_k64<256>(q, k, v, o, lse, B, Hq, Hkv, Sq, Tkv, start_pos, causal,
+                                   window, scale_log2, dev, stream);
+  if (Dh == 128 && start_pos + Sq <= kPrefillK64MaxKeys128)
+    return launch_prefill_k64<128>(q, k, v, o, lse, B, Hq, Hkv, Sq, Tkv, start_pos, causal,
+                                   window, scale_log2, dev, stream);
   // K and V hold Tkv rows per head in memory; the chunk sees the first
   // start_pos + Sq of them, and the maps cover only those (the last key
   // tile's rows past them are zero-filled, never read from the cache)

@@ -51,6 +51,10 @@ CASES = [
     (1, 4, 2, 150, 400, 200, 128, 0, 0),      # non-causal: the whole cache plus chunk
     (1, 2, 2, 129, 1200, 1000, 128, 1, 333),  # window shorter than the cached prefix
     (3, 6, 3, 64, 3000, 2900, 64, 1, 0),      # short chunk after a long prefix
+    # head size 128 past 1536 keys (the ping-pong kernel): ragged chunks
+    (1, 4, 2, 129, 2500, 1700, 128, 1, 0),
+    (1, 2, 2, 200, 2400, 2000, 128, 1, 500),
+    (1, 4, 4, 100, 1536, 1436, 128, 1, 0),    # 1536 keys: the 64-key kernel
 ]
 
 

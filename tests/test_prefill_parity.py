@@ -60,6 +60,29 @@ def test_all_rows_small(B, Hq, Hkv, S, Dh, causal, window):
     assert_close(o.float().cpu().numpy(), ref, what=f"{(B, Hq, Hkv, S, Dh, causal, window)}")
 
 
+# Head size 128 runs on two kernels: up to 1536 keys per head the 64-key-tile
+# kernel with two CTAs per SM (every Dh 128 case above), beyond that the
+# ping-pong kernel.  Both sides of the switch, and ragged tails, windows and
+# GQA / MQA groups on the ping-pong side.
+SWITCH_128 = [
+    (1, 2, 2, 1536, 128, 1, 0),    # the longest sequence on the 64-key kernel
+    (1, 2, 2, 1537, 128, 1, 0),    # the shortest on the ping-pong kernel: a one-row tail
+    (1, 3, 3, 1663, 128, 1, 0),
+    (1, 2, 2, 1601, 128, 0, 0),
+    (1, 4, 2, 1700, 128, 1, 17),
+    (1, 4, 1, 1800, 128, 1, 300),
+    (2, 8, 2, 1560, 128, 1, 0),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,Dh,causal,window", SWITCH_128)
+def test_all_rows_both_head128_kernels(B, Hq, Hkv, S, Dh, causal, window):
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, S, Dh, seed=S + window + 3)
+    o = gpu_fwd(q, k, v, causal, window)
+    ref = oracle.attention(q, k, v, causal=bool(causal), window=window)
+    assert_close(o.float().cpu().numpy(), ref, what=f"{(B, Hq, Hkv, S, Dh, causal, window)}")
+
+
 # More work items (256-row query blocks x heads) than SMs, so every CTA of the
 # persistent kernel runs several in a row: the barrier phases, ring positions
 # and tensor-memory accumulators carry from one item into the next.  Mixed
