@@ -10,12 +10,14 @@
 //   it run); tensor memory S0 [0,64), S1 [64,128), O [256,512).
 //
 //   Dh = 128, short sequences.  Two CTAs per SM, each with half of the
-//   shared memory (Q 32 KiB, two-stage K and V rings of 16 KiB tiles) and
-//   half of the tensor memory (S0 [0,64), S1 [64,128), O [128,256) from its
-//   allocation's base).  When every CTA has only one or two short items, the
-//   fixed cost of an item (its first loads, the masked diagonal tiles, the
-//   epilogue) dominates the ping-pong kernel's time; here the other CTA on
-//   the SM keeps the tensor core busy through it.
+//   shared memory (Q 32 KiB, two-stage K and V rings of 16 KiB tiles, a
+//   4 KiB output staging tile per softmax warp) and half of the tensor
+//   memory (S0 [0,64), S1 [64,128), O [128,256) from its allocation's base).
+//   When every CTA has only one or two short items, the fixed cost of an
+//   item (its first loads, the masked diagonal tiles, the epilogue)
+//   dominates the ping-pong kernel's time; here the other CTA on the SM keeps
+//   the tensor core busy through it.  The output leaves through bulk tensor
+//   stores from the staging tiles.
 //
 // S is double-buffered, so the S MMA of the next key tile runs while the
 // softmax works on the current one.  P (bf16) is written over the first 32
@@ -71,14 +73,28 @@ struct PrefillK64Cfg {
   static constexpr int kWarpProducer = 4, kWarpIssuer = 5;
   // S buffer b at kColS + 64 b, O in the allocation's last DH columns
   static constexpr uint32_t kColS = 0, kColO = kTmemCols - DH;
+  // Dh 128: the output goes through shared memory and bulk tensor stores
+  // (32 rows x 64 columns per box and softmax warp).  Dh 256 has no shared
+  // memory left for it and stores from registers.
+  static constexpr bool kTmaStore = DH == 128;
+  static constexpr int kStageBytes = kTmaStore ? 4 * 32 * 128 : 0;
+  // Two CTAs and their shared memory fit an SM only without the 1 KiB
+  // alignment slack: that instance takes the dynamic shared memory as placed
+  // (1024-byte aligned, which the kernel checks).
+  static constexpr int kAlignSlack = kTmaStore ? 0 : 1024;
 };
 
+// Every array is a whole number of KiB, so each starts 1024-byte aligned once
+// the structure does (the 128-byte swizzle repeats every 1024 bytes).
 template <int DH>
-struct __align__(1024) PrefillK64Smem {
+struct PrefillK64Smem {
   using Cfg = PrefillK64Cfg<DH>;
   uint8_t q[Cfg::kQBytes];
   uint8_t k[Cfg::kStagesK][Cfg::kTileBytes];
   uint8_t v[Cfg::kStagesV][Cfg::kTileBytes];
+  // per softmax warp (Dh 128): its 32 output rows x 64 columns of bf16,
+  // 128-byte swizzled (the layout of one box of the output's tensor map)
+  uint8_t ostage[Cfg::kStageBytes > 0 ? Cfg::kStageBytes : 1];
   uint64_t q_full, q_empty;
   uint64_t k_full[Cfg::kStagesK], k_empty[Cfg::kStagesK];
   uint64_t v_full[Cfg::kStagesV], v_empty[Cfg::kStagesV];
@@ -293,8 +309,8 @@ __device__ __forceinline__ void prefill_k64_issuer(PrefillK64Smem<DH>& sm, const
 // the lazy maximum of the Dh <= 128 kernel, 64 scores per tile.
 template <int DH>
 __device__ __forceinline__ void prefill_k64_softmax(PrefillK64Smem<DH>& sm, const PrefillK64Params& p,
-                                                    uint32_t tbase, volatile int* abort, int warp,
-                                                    int lane) {
+                                                    const CUtensorMap* map_o, uint32_t tbase,
+                                                    volatile int* abort, int warp, int lane) {
   using Cfg = PrefillK64Cfg<DH>;
   const int t = warp * 32 + lane;
   const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
@@ -402,7 +418,7 @@ __device__ __forceinline__ void prefill_k64_softmax(PrefillK64Smem<DH>& sm, cons
     }
     if (!ok) break;
 
-    // ---- epilogue: O / l -> bf16 -> output row, 2 Dh bytes per row
+    // ---- epilogue: O / l -> bf16 -> output rows
     if (!(ok = mbar_wait(&sm.o_final, items & 1u, abort))) break;
     ++items;
     tc_fence_after_sync();
@@ -416,27 +432,62 @@ __device__ __forceinline__ void prefill_k64_softmax(PrefillK64Smem<DH>& sm, cons
     // (the output is not read again by this kernel: evict-first, leaving L2
     // to the K/V tiles the other query blocks re-read)
     const uint64_t out_policy = policy_evict_first();
+    if constexpr (Cfg::kTmaStore) {
+      // 64 columns per round: TMEM -> registers -> this warp's staging tile
+      // -> one bulk tensor store (rows past the chunk's end are clipped by
+      // the tensor map)
+      uint8_t* stg = sm.ostage + warp * (32 * 128);
+      const uint32_t stage = smem_u32(stg);
+#pragma unroll
+      for (int h = 0; h < Cfg::kBoxes; ++h) {
+        uint32_t o0[32], o1[32];
+        tmem_ld_32x32b_x32(colO + 64 * h, o0);
+        tmem_ld_32x32b_x32(colO + 64 * h + 32, o1);
+        // the previous bulk store from this tile has read it
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+        tmem_ld_wait(o0);
+        tmem_ld_wait(o1);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {   // 16-byte chunk c: columns 8c .. 8c+7 of these 64
+          const uint32_t* x8 = c < 4 ? o0 + 8 * c : o1 + 8 * (c - 4);
+          uint32_t v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            v[e] = pack_bf16x2(__uint_as_float(x8[2 * e]) * inv_l,
+                               __uint_as_float(x8[2 * e + 1]) * inv_l);
+          st_shared_v4(stage + lane * 128 + ((c ^ (lane & 7)) << 4), v[0], v[1], v[2], v[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d_hint(map_o, stg, 64 * h, tile.q0 + 32 * warp, tile.bh, out_policy);
+          bulk_commit_group();
+        }
+      }
+    } else {
 #pragma unroll 1
-    for (int c = 0; c < Cfg::DH / 32; c += 2) {
-      uint32_t o0[32], o1[32];
-      tmem_ld_32x32b_x32(colO + 32 * c, o0);
-      tmem_ld_32x32b_x32(colO + 32 * c + 32, o1);
-      tmem_ld_wait(o0);
-      tmem_ld_wait(o1);
+      for (int c = 0; c < Cfg::DH / 32; c += 2) {
+        uint32_t o0[32], o1[32];
+        tmem_ld_32x32b_x32(colO + 32 * c, o0);
+        tmem_ld_32x32b_x32(colO + 32 * c + 32, o1);
+        tmem_ld_wait(o0);
+        tmem_ld_wait(o1);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {   // 16 columns each
-        const uint32_t* o = q < 2 ? o0 + 16 * q : o1 + 16 * (q - 2);
-        uint32_t v[8];
+        for (int q = 0; q < 4; ++q) {   // 16 columns each
+          const uint32_t* o = q < 2 ? o0 + 16 * q : o1 + 16 * (q - 2);
+          uint32_t v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          v[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-        if (store) {
-          uint4* d = dst + 2 * (2 * c + q);
-          if (p.o_wide) {
-            st_global_v8_hint(d, v, out_policy);
-          } else {
-            d[0] = make_uint4(v[0], v[1], v[2], v[3]);
-            d[1] = make_uint4(v[4], v[5], v[6], v[7]);
+          for (int e = 0; e < 8; ++e)
+            v[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          if (store) {
+            uint4* d = dst + 2 * (2 * c + q);
+            if (p.o_wide) {
+              st_global_v8_hint(d, v, out_policy);
+            } else {
+              d[0] = make_uint4(v[0], v[1], v[2], v[3]);
+              d[1] = make_uint4(v[4], v[5], v[6], v[7]);
+            }
           }
         }
       }
@@ -444,15 +495,26 @@ __device__ __forceinline__ void prefill_k64_softmax(PrefillK64Smem<DH>& sm, cons
     // the next item's first P.V overwrites O only after the arrive on p_full
     // that follows these loads (tcgen05.wait::ld above)
   }
+  // the staged rows must be written out before the CTA's shared memory goes
+  if constexpr (Cfg::kTmaStore) {
+    if (lane == 0) bulk_wait_group0();
+  }
 }
 
 template <int DH>
 __global__ void __launch_bounds__(PrefillK64Cfg<DH>::kThreads, PrefillK64Cfg<DH>::kCtasPerSm)
     attn_prefill_k64_sm103a(const __grid_constant__ CUtensorMap map_q,
                             const __grid_constant__ CUtensorMap map_k,
-                            const __grid_constant__ CUtensorMap map_v, const PrefillK64Params p) {
+                            const __grid_constant__ CUtensorMap map_v,
+                            const __grid_constant__ CUtensorMap map_o,   // Dh 128 only
+                            const PrefillK64Params p) {
   using Cfg = PrefillK64Cfg<DH>;
   extern __shared__ uint8_t smem_raw[];
+  if (Cfg::kAlignSlack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
+    // no room to align: refuse before any barrier, copy or allocation
+    if (threadIdx.x == 0) atomicExch(p.error_word, 3);   // ATTN_ERR_CUDA
+    return;
+  }
   PrefillK64Smem<DH>& sm = *reinterpret_cast<PrefillK64Smem<DH>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   volatile int* abort = &sm.abort_flag;
@@ -463,6 +525,7 @@ __global__ void __launch_bounds__(PrefillK64Cfg<DH>::kThreads, PrefillK64Cfg<DH>
     prefetch_tensormap(&map_q);
     prefetch_tensormap(&map_k);
     prefetch_tensormap(&map_v);
+    if (Cfg::kTmaStore) prefetch_tensormap(&map_o);
   }
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
@@ -505,7 +568,7 @@ __global__ void __launch_bounds__(PrefillK64Cfg<DH>::kThreads, PrefillK64Cfg<DH>
   } else if (warp == Cfg::kWarpIssuer) {
     prefill_k64_issuer<DH>(sm, p, tbase, abort);
   } else {
-    prefill_k64_softmax<DH>(sm, p, tbase, abort, warp, lane);
+    prefill_k64_softmax<DH>(sm, p, &map_o, tbase, abort, warp, lane);
   }
 
   // ---- teardown (every wait above is bounded)
@@ -521,12 +584,11 @@ __global__ void __launch_bounds__(PrefillK64Cfg<DH>::kThreads, PrefillK64Cfg<DH>
 
 template <int DH>
 constexpr size_t prefill_k64_smem_bytes() {
-  return sizeof(PrefillK64Smem<DH>) + 1024;   // + alignment slack
+  return sizeof(PrefillK64Smem<DH>) + PrefillK64Cfg<DH>::kAlignSlack;
 }
 
-// two CTAs per SM at Dh 128: each takes under half of the SM's 228 KiB
-// (1 KiB of it reserved per CTA)
-static_assert(prefill_k64_smem_bytes<128>() <= 113 * 1024, "Dh 128: two CTAs per SM");
+// two CTAs per SM at Dh 128 in the SM's 228 KiB (1 KiB of it reserved per CTA)
+static_assert(2 * (prefill_k64_smem_bytes<128>() + 1024) <= 228 * 1024, "Dh 128: two CTAs per SM");
 static_assert(prefill_k64_smem_bytes<256>() <= 227 * 1024, "Dh 256: one CTA per SM");
 
 }  // namespace chs

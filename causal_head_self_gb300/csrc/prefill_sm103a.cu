@@ -53,10 +53,15 @@ static cudaError_t launch_prefill_k64(const void* q, const void* k, const void* 
                                       const DeviceInfo& dev, cudaStream_t stream) {
   using Cfg = PrefillK64Cfg<DH>;
   const int Skv = start_pos + Sq;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!encode_bf16_map(&mq, q, Cfg::DH, Sq, (long long)B * Hq, 128) ||
       !encode_bf16_map(&mk, k, Cfg::DH, Skv, (long long)B * Hkv, Cfg::kKeys, Tkv) ||
       !encode_bf16_map(&mv, v, Cfg::DH, Skv, (long long)B * Hkv, Cfg::kKeys, Tkv))
+    return cudaErrorInvalidValue;
+  // the output map (32 rows x 64 columns per box) where the kernel stores
+  // through it; otherwise an unused copy of the Q map
+  mo = mq;
+  if (Cfg::kTmaStore && !encode_bf16_map(&mo, o, Cfg::DH, Sq, (long long)B * Hq, 32))
     return cudaErrorInvalidValue;
   PrefillK64Params prm;
   prm.B = B;
@@ -90,7 +95,7 @@ static cudaError_t launch_prefill_k64(const void* q, const void* k, const void* 
   const int cap = Cfg::kCtasPerSm * dev.num_sms;
   const int grid = prm.num_items < cap ? prm.num_items : cap;
   return launch_pdl(attn_prefill_k64_sm103a<DH>, dim3(grid), dim3(Cfg::kThreads), smem, stream,
-                    mq, mk, mv, prm);
+                    mq, mk, mv, mo, prm);
 }
 
 // Head size 128 takes the two-CTA 64-key kernel up to this many keys per

@@ -79,8 +79,9 @@ typedef enum {
  *   causal   1: causal mask; 0: every key visible (window must then be <= 0)
  *   window, scale: see the conventions above.
  * B == 0 or S == 0 is a no-op returning ATTN_OK.
- * Work: 4*Dh FLOPs per visible (query, key) pair per query head; masked tiles
- * of 128x128 are never computed.
+ * Work: 4*Dh FLOPs per visible (query, key) pair per query head; wholly
+ * masked tiles (128 query rows by 128 keys, or by 64 keys at Dh 256 and at
+ * Dh 128 up to 1536 keys per head) are never computed.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
              int S, int Dh, int causal, int window, float scale, cudaStream_t stream);
@@ -246,7 +247,8 @@ int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
 /*
  * attn_status -- synchronise `stream`, then return (and clear) the current
  * device's latched error word: ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_INVALID_ARG,
- * or ATTN_ERR_CUDA if the synchronisation itself failed.
+ * or ATTN_ERR_CUDA if the synchronisation itself failed (or a prefill kernel
+ * found its dynamic shared memory not 1024-byte aligned and wrote nothing).
  */
 int attn_status(cudaStream_t stream);
 
