@@ -7,7 +7,12 @@
 //   ping-pong of the Dh <= 128 kernel does not fit.  One CTA per SM: Q
 //   (64 KiB), a two-stage K ring and a three-stage V ring of 32 KiB tiles
 //   (224 KiB; the third V stage lets a V tile load while the two P.V before
-//   it run); tensor memory S0 [0,64), S1 [64,128), O [256,512).
+//   it run); tensor memory S0 [0,64), S1 [64,128), Q [128,256), O [256,512).
+//   Q is copied from shared into tensor memory once per item (tcgen05.cp)
+//   and the S MMAs take it from there: with both operands in shared memory
+//   an N = 64 MMA reads 6 KiB per 128 x 64 x 16 step, more than shared
+//   memory delivers in the step's tensor-core time; with Q in tensor memory
+//   it reads 2 KiB.
 //
 //   Dh = 128, short sequences.  Two CTAs per SM, each with half of the
 //   shared memory (Q 32 KiB, two-stage K and V rings of 16 KiB tiles, a
@@ -82,6 +87,10 @@ struct PrefillK64Cfg {
   // alignment slack: that instance takes the dynamic shared memory as placed
   // (1024-byte aligned, which the kernel checks).
   static constexpr int kAlignSlack = kTmaStore ? 0 : 1024;
+  // Dh 256: Q is copied into tensor memory [128, 256) once per item and the S
+  // MMAs read it there, so that they stream only K from shared memory
+  static constexpr bool kQInTmem = DH == 256;
+  static constexpr uint32_t kColQ = 128;
 };
 
 // Every array is a whole number of KiB, so each starts 1024-byte aligned once
@@ -99,6 +108,7 @@ struct PrefillK64Smem {
   uint64_t k_full[Cfg::kStagesK], k_empty[Cfg::kStagesK];
   uint64_t v_full[Cfg::kStagesV], v_empty[Cfg::kStagesV];
   uint64_t s_full[2], p_full[2], pv_done, o_final, mma_done;
+  uint64_t qt_free;   // (Q in tensor memory) the item's last S MMA is done
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -231,7 +241,10 @@ __device__ __forceinline__ void prefill_k64_producer(PrefillK64Smem<DH>& sm, con
 // item: S of its first two tiles, then per tile t: P.V(t) once P(t) is
 // written, and S(t+2) into the buffer P(t) lived in (the tensor core runs one
 // thread's MMAs in order).  The first P.V of an item overwrites O: the
-// softmax threads publish that P only after their epilogue has read O.
+// softmax threads publish that P only after their epilogue has read O.  At
+// Dh 256 an item starts with the copy of Q into tensor memory; a copy issued
+// after an MMA is not ordered behind it, so the copy waits (qt_free) for the
+// previous item's last S MMA, which is long done by then.
 template <int DH>
 __device__ __forceinline__ void prefill_k64_issuer(PrefillK64Smem<DH>& sm, const PrefillK64Params& p,
                                                    uint32_t tbase, volatile int* abort) {
@@ -256,7 +269,10 @@ __device__ __forceinline__ void prefill_k64_issuer(PrefillK64Smem<DH>& sm, const
       // 16 columns (32 bytes) of Dh per MMA; a 64-column box holds 4 steps
       const uint32_t offq = ((kk / 4) * Cfg::kQBox + (kk % 4) * 32) >> 4;
       const uint32_t offk = ((kk / 4) * Cfg::kKBox + (kk % 4) * 32) >> 4;
-      mma_bf16_ss_warp(dS, dq + offq, b + offk, idesc_qk, kk > 0 ? 1u : 0u);
+      if constexpr (Cfg::kQInTmem)
+        mma_bf16_ts_warp(dS, tbase + Cfg::kColQ + 8 * kk, b + offk, idesc_qk, kk > 0 ? 1u : 0u);
+      else
+        mma_bf16_ss_warp(dS, dq + offq, b + offk, idesc_qk, kk > 0 ? 1u : 0u);
     }
     mma_commit_warp(&sm.s_full[t & 1u]);
     mma_commit_warp(&sm.k_empty[st]);
@@ -271,11 +287,27 @@ __device__ __forceinline__ void prefill_k64_issuer(PrefillK64Smem<DH>& sm, const
     const PrefillK64Tile tile = prefill_k64_tile_of(p, w);
     const int n = tile.hi - tile.lo + 1;
     if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, (uint32_t)nq & 1u, abort)))) break;
-    ++nq;
     tc_fence_after_sync();
+    uint64_t* q_done = &sm.q_empty;   // arrived on when the item's last S MMA is done
+    if constexpr (Cfg::kQInTmem) {
+      // the previous item's S MMAs read the tensor-memory copy of Q: the copy
+      // of this item's Q waits for the last of them
+      if (nq > 0 &&
+          !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.qt_free, (uint32_t)(nq - 1) & 1u, abort))))
+        break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < Cfg::DH / 16; ++kk)
+        tmem_cp_128x256b_warp(tbase + Cfg::kColQ + 8 * kk,
+                              dq + (((kk / 4) * Cfg::kQBox + (kk % 4) * 32) >> 4));
+      // the shared-memory Q is free once the copies are done
+      mma_commit_warp(&sm.q_empty);
+      q_done = &sm.qt_free;
+    }
+    ++nq;
     if (!(ok = issue_s(t))) break;
     if (n > 1 && !(ok = issue_s(t + 1))) break;
-    if (n <= 2) mma_commit_warp(&sm.q_empty);   // this item's last S is issued
+    if (n <= 2) mma_commit_warp(q_done);   // this item's last S is issued
     for (int i = 0; ok && i < n; ++i, ++t) {
       const int st = (int)(t % Cfg::kStagesV);
       const uint32_t ph = (t / Cfg::kStagesV) & 1u;
@@ -294,7 +326,7 @@ __device__ __forceinline__ void prefill_k64_issuer(PrefillK64Smem<DH>& sm, const
       mma_commit_warp(&sm.v_empty[st]);
       if (i + 2 < n) {
         if (!(ok = issue_s(t + 2))) break;
-        if (i + 2 == n - 1) mma_commit_warp(&sm.q_empty);
+        if (i + 2 == n - 1) mma_commit_warp(q_done);
       }
     }
     if (ok) mma_commit_warp(&sm.o_final);
@@ -546,6 +578,7 @@ __global__ void __launch_bounds__(PrefillK64Cfg<DH>::kThreads, PrefillK64Cfg<DH>
     mbar_init(&sm.pv_done, 1);
     mbar_init(&sm.o_final, 1);
     mbar_init(&sm.mma_done, 1);
+    mbar_init(&sm.qt_free, 1);
     fence_mbarrier_init();
   }
   if (warp == Cfg::kWarpProducer) {

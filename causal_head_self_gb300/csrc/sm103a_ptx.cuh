@@ -296,6 +296,16 @@ __device__ __forceinline__ void mma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
+// Copy a 128-row x 256-bit (16 bf16 per row) operand slice from shared memory
+// (described by a matrix descriptor, as an MMA operand) into tensor memory:
+// row r to lane r, eight 32-bit columns from taddr (one elected lane issues).
+__device__ __forceinline__ void tmem_cp_128x256b_warp(uint32_t taddr, uint64_t s_desc) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n}" ::"r"(taddr), "l"(s_desc)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
