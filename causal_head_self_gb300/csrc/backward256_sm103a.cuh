@@ -26,7 +26,12 @@
 // units per block pair against the 4 of a fused pass); there are no atomics
 // and the result is deterministic.  Tensor memory: two score buffers
 // [0, 64) and [64, 128), two dP buffers [128, 192) and [192, 256) (the dQ
-// pass uses one score buffer), the accumulator [256, 512).  Roles as in the
+// pass uses one score buffer), the accumulator [256, 512).  Columns a pass
+// leaves free hold an MMA operand copied from shared memory (tcgen05.cp)
+// once per item, so that its N = 64 score MMAs read less shared memory: K in
+// the dV pass (at [128, 256)), the first 128 columns of Q in the dQ pass (at
+// [64, 128)).  A copy is not ordered behind an MMA issued before it, so each
+// copy waits for the previous item's last reader of the old copy.  Roles as in the
 // Dh <= 128 kernels: two element-wise warpgroups on the two 32-column halves
 // of every 64-column tile (thread t owns tensor-memory lane t), one TMA
 // thread, one MMA warp.  Every wait is bounded.
@@ -50,6 +55,11 @@ struct Bwd256Cfg {
   static constexpr int kThreads = 32 * (4 * kWG + 2);
   static constexpr int kWarpProducer = 4 * kWG, kWarpIssuer = 4 * kWG + 1;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;   // + 64 b for buffer b
+  // dV pass: K (128 keys x 256, bf16 pairs) in the unused dP columns [128, 256)
+  static constexpr uint32_t kColKt = 128;
+  // dQ pass: Q's first 128 columns (bf16 pairs) in the unused second score
+  // buffer [64, 128)
+  static constexpr uint32_t kColQt = 64;
 };
 
 // Columns of a 64-column tile hold each warpgroup's bf16 pairs in the first
@@ -100,6 +110,7 @@ struct __align__(1024) Bwd256KvSmem {
   float lse2[kStagesStat][64];                  // the blocks' log-sum-exps (log2 units)
   float dlt[kStagesStat][64];                   // their D_i
   uint64_t kv_full, kv_empty;
+  uint64_t kt_free;   // (dV pass) the item's last S^T MMA, the last reader of K in tensor memory, is done
   uint64_t q_full[kStagesQ], q_empty[kStagesQ];
   uint64_t do_full[kStagesDO], do_empty[kStagesDO];
   uint64_t s_full[2], dp_full[2], p_full[2], ds_full[2], acc_final, mma_done;
@@ -250,7 +261,17 @@ __device__ __forceinline__ void bwd256_kv_issuer(Bwd256KvSmem<DK>& sm, const Bwd
   auto issue_scores = [&](uint32_t x) -> bool {
     if (!wait_all(&sm.q_full[qst(x)], qph(x))) return false;
     tc_fence_after_sync();
-    mma_s(Cfg::kColS + 64 * (x & 1u), dk_, dq_k + qst(x) * kStage);
+    if (!DK) {
+      // S^T = K Q^T with K from tensor memory: only Q streams from shared memory
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const uint32_t offb = ((kk / 4) * Cfg::kSmallBox + (kk % 4) * 32) >> 4;
+        mma_bf16_ts_warp(Cfg::kColS + 64 * (x & 1u), Cfg::kColKt + 8 * kk,
+                         dq_k + qst(x) * kStage + offb, idesc_s, kk > 0 ? 1u : 0u);
+      }
+    } else {
+      mma_s(Cfg::kColS + 64 * (x & 1u), dk_, dq_k + qst(x) * kStage);
+    }
     mma_commit_warp(&sm.s_full[x & 1u]);
     if (!DK) mma_commit_warp(&sm.q_empty[qst(x)]);   // (dV pass: S^T is Q's only reader)
     if (DK) {
@@ -271,13 +292,32 @@ __device__ __forceinline__ void bwd256_kv_issuer(Bwd256KvSmem<DK>& sm, const Bwd
     const BwdKvItem I = bwd256_kv_item_of(p, w);
     const int N = p.group * (I.hi - I.lo + 1);
     if (!(ok = wait_all(&sm.kv_full, (uint32_t)items & 1u))) break;
+    tc_fence_after_sync();
+    // the barrier the item's last S^T commits: kv_empty (K read from shared
+    // memory), or in the dV pass kt_free (K read from tensor memory)
+    uint64_t* k_done = &sm.kv_empty;
+    if (!DK) {
+      // copy K into tensor memory once the previous item's S^T MMAs, which
+      // read the previous copy, are done (a copy is not ordered behind an
+      // MMA issued before it); the shared-memory K is then free
+      if (items > 0 &&
+          !(ok = wait_all(&sm.kt_free, (uint32_t)(items - 1) & 1u)))
+        break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk)
+        tmem_cp_128x256b_warp(Cfg::kColKt + 8 * kk,
+                              dk_ + (((kk / 4) * Cfg::kBigBox + (kk % 4) * 32) >> 4));
+      mma_commit_warp(&sm.kv_empty);
+      k_done = &sm.kt_free;
+    }
     ++items;
     if (!(ok = issue_scores(u))) break;
-    if (N == 1) mma_commit_warp(&sm.kv_empty);
+    if (N == 1) mma_commit_warp(k_done);
     for (int n = 0; n < N; ++n, ++u) {
       if (n + 1 < N) {
         if (!(ok = issue_scores(u + 1))) break;
-        if (n + 2 == N) mma_commit_warp(&sm.kv_empty);   // the item's last read of K (and V)
+        if (n + 2 == N) mma_commit_warp(k_done);   // the item's last read of K (and V)
       }
       if (DK) {
         if (!(ok = wait_all(&sm.ds_full[u & 1u], (u >> 1) & 1u))) break;
@@ -446,6 +486,7 @@ __global__ void __launch_bounds__(Bwd256Cfg::kThreads, 1)
     sm.abort_flag = 0;
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
+    mbar_init(&sm.kt_free, 1);
     for (int i = 0; i < Smem::kStagesQ; ++i) {
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
@@ -517,6 +558,7 @@ struct __align__(1024) Bwd256QSmem {
   uint64_t v_full[kStagesV], v_empty[kStagesV];
   uint64_t s_full, s_free, acc_final, mma_done;
   uint64_t dp_full[2], ds_full[2];   // per dP / dS buffer
+  uint64_t qt_free;                  // the item's last S MMA (reader of Q in tensor memory) is done
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -620,6 +662,19 @@ __device__ __forceinline__ void bwd256_dq_issuer(Bwd256QSmem& sm, const BwdParam
       mma_bf16_ss_warp(d, a + offa, b + offb, idesc_s, kk > 0 ? 1u : 0u);
     }
   };
+  // S = Q K^T with Q's first 128 columns from tensor memory, the rest from
+  // shared memory
+  auto mma_qk = [&](uint32_t d, uint64_t b) {
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const uint32_t offa = ((kk / 4) * Cfg::kBigBox + (kk % 4) * 32) >> 4;
+      const uint32_t offb = ((kk / 4) * Cfg::kSmallBox + (kk % 4) * 32) >> 4;
+      if (kk < 8)
+        mma_bf16_ts_warp(d, Cfg::kColQt + 8 * kk, b + offb, idesc_s, kk > 0 ? 1u : 0u);
+      else
+        mma_bf16_ss_warp(d, dq_ + offa, b + offb, idesc_s, 1u);
+    }
+  };
   auto wait_all = [&](uint64_t* bar, uint32_t ph) -> bool {
     return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort));
   };
@@ -644,22 +699,36 @@ __device__ __forceinline__ void bwd256_dq_issuer(Bwd256QSmem& sm, const BwdParam
     const BwdQItem I = bwd256_q_item_of(p, w);
     const int N = I.hi - I.lo + 1;
     if (!(ok = wait_all(&sm.q_full, (uint32_t)items & 1u))) break;
+    // Q's first half into tensor memory, once the previous item's S MMAs
+    // (which read the previous copy) are done
+    if (items > 0 && !(ok = wait_all(&sm.qt_free, (uint32_t)(items - 1) & 1u))) break;
+    tc_fence_after_sync();
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      tmem_cp_128x256b_warp(Cfg::kColQt + 8 * kk,
+                            dq_ + (((kk / 4) * Cfg::kBigBox + (kk % 4) * 32) >> 4));
     ++items;
     if (!(ok = wait_all(&sm.k_full[kst(u)], kph(u)))) break;
     tc_fence_after_sync();
-    mma_s(Cfg::kColS, dq_, dk_k + kst(u) * kStage);                      // S = Q K^T
+    mma_qk(Cfg::kColS, dk_k + kst(u) * kStage);                          // S = Q K^T
     mma_commit_warp(&sm.s_full);
     if (!(ok = issue_dp(u))) break;
-    if (N == 1) mma_commit_warp(&sm.q_empty);
+    if (N == 1) {
+      mma_commit_warp(&sm.q_empty);
+      mma_commit_warp(&sm.qt_free);
+    }
     for (int n = 0; n < N; ++n, ++u) {
       if (n + 1 < N) {
         if (!(ok = wait_all(&sm.s_free, u & 1u))) break;
         if (!(ok = wait_all(&sm.k_full[kst(u + 1)], kph(u + 1)))) break;
         tc_fence_after_sync();
-        mma_s(Cfg::kColS, dq_, dk_k + kst(u + 1) * kStage);
+        mma_qk(Cfg::kColS, dk_k + kst(u + 1) * kStage);
         mma_commit_warp(&sm.s_full);
         if (!(ok = issue_dp(u + 1))) break;
-        if (n + 2 == N) mma_commit_warp(&sm.q_empty);
+        if (n + 2 == N) {
+          mma_commit_warp(&sm.q_empty);
+          mma_commit_warp(&sm.qt_free);
+        }
       }
       if (!(ok = wait_all(&sm.ds_full[u & 1u], (u >> 1) & 1u))) break;
       tc_fence_after_sync();
@@ -810,6 +879,7 @@ __global__ void __launch_bounds__(Bwd256Cfg::kThreads, 1)
       mbar_init(&sm.ds_full[i], Cfg::kEW);
     }
     mbar_init(&sm.acc_final, 1);
+    mbar_init(&sm.qt_free, 1);
     mbar_init(&sm.mma_done, 1);
     fence_mbarrier_init();
   }
