@@ -436,6 +436,42 @@ def _packed(ts, dev):
     return (host, devbuf), views
 
 
+def _pipelined_e2e(dev, stream, host_in, dev_in, run, dev_out, host_out, steps):
+    """Seconds per step of `steps` end-to-end steps pipelined over two device
+    buffer sets: step i's inputs cross to the device (a copy stream) while
+    step i-1 computes (on `stream`) and step i-2's result crosses back (a
+    second copy stream).  Every step copies its inputs in and its result out
+    inside the timed region; the buffers alternate, and each copy or launch
+    waits for the last use of the buffer it overwrites."""
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    t0.record(s_in)
+    for i in range(steps):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[b])      # step i-2's launch has read dev_in[b]
+            dev_in[b].copy_(host_in, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])         # step i-2's result has left dev_out[b]
+        run(b)
+        ev_comp[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            host_out[b].copy_(dev_out[b], non_blocking=True)
+            ev_out[b].record(s_out)
+    s_out.wait_event(ev_in[(steps - 1) % 2])
+    t1.record(s_out)
+    torch.cuda.synchronize(dev)
+    return t0.elapsed_time(t1) / 1e3 / steps
+
+
 def _row(work, unit, per_launch, lat, peak=None, **extra):
     """One timed row: throughput from back-to-back launches, latency beside it."""
     val = work / per_launch / (1e12 if unit == "TFLOP/s" else 1e9)
@@ -684,8 +720,33 @@ def run_gpu(args, rank, world, local_rank):
             e2e_d.append(e[1].elapsed_time(e[2]) / 1e3)
     if chs.attn_status() != chs.ATTN_OK:
         raise RuntimeError("device error in the end-to-end loop")
-    tp_e2e, td_e2e = statistics.mean(e2e_p), statistics.mean(e2e_d)
-    tp_e2e, td_e2e = max_over_ranks([tp_e2e, td_e2e], world, dev)
+    tp_ser, td_ser = statistics.mean(e2e_p), statistics.mean(e2e_d)
+    # the same steps pipelined (a second device buffer set per leg)
+    hp2, (qe2, ke2, ve2) = _packed((qh, kh, vh), dev)
+    hd2, (qde2, kce2, vce2, sle2) = _packed((qdh, kch, vch, slh), dev)
+    o2, od2 = torch.empty_like(o), torch.empty_like(od)
+    op2, odp2 = torch.empty_like(op).pin_memory(), torch.empty_like(odp).pin_memory()
+    pviews = [(qe, ke, ve, o), (qe2, ke2, ve2, o2)]
+    dviews = [(qde, kce, vce, sle, od), (qde2, kce2, vce2, sle2, od2)]
+    pipe_steps = max(6, min(40, 2 * args.steps))
+
+    def run_p(b):
+        x = pviews[b]
+        chs.attn_fwd(x[0], x[1], x[2], x[3], causal=bool(w_p["causal"]), window=w_p["window"],
+                     stream=stream)
+
+    def run_d(b):
+        x = dviews[b]
+        chs.attn_decode(x[0], x[1], x[2], x[3], x[4], window=w_d["window"], stream=stream)
+
+    tp_e2e = _pipelined_e2e(dev, stream, hp[0], [hp[1], hp2[1]], run_p, [o, o2], [op, op2],
+                            pipe_steps)
+    td_e2e = _pipelined_e2e(dev, stream, hd[0], [hd[1], hd2[1]], run_d, [od, od2], [odp, odp2],
+                            pipe_steps)
+    if chs.attn_status() != chs.ATTN_OK:
+        raise RuntimeError("device error in the pipelined end-to-end loop")
+    del hp2, hd2, qe2, ke2, ve2, qde2, kce2, vce2, sle2, o2, od2, op2, odp2, pviews, dviews
+    tp_e2e, td_e2e, tp_ser, td_ser = max_over_ranks([tp_e2e, td_e2e, tp_ser, td_ser], world, dev)
     if rank != 0:
         return None
     h2d_p, h2d_d = hp[0].numel(), hd[0].numel()   # bytes per step, padding included
@@ -763,9 +824,18 @@ def run_gpu(args, rank, world, local_rank):
         "e2e": {"value": job_rate(pf, tp_e2e, world) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d_p,
                 "d2h_bytes_per_step": o.numel() * o.element_size(),
+                "ms_per_step": tp_e2e * 1e3,
+                "method": f"{pipe_steps} steps pipelined over two device buffer sets (inputs of "
+                          "step i cross while step i-1 computes and step i-2's result returns)",
+                "serial": {"value": job_rate(pf, tp_ser, world) / 1e12, "unit": "TFLOP/s",
+                           "ms_per_step": tp_ser * 1e3,
+                           "method": "one step at a time: copy in, launch, copy out, synchronise"},
                 "decode": {"value": job_rate(db, td_e2e, world) / 1e9, "unit": "GB/s",
                            "h2d_bytes_per_step": h2d_d,
-                           "d2h_bytes_per_step": od.numel() * od.element_size()}},
+                           "d2h_bytes_per_step": od.numel() * od.element_size(),
+                           "ms_per_step": td_e2e * 1e3,
+                           "serial": {"value": job_rate(db, td_ser, world) / 1e9, "unit": "GB/s",
+                                      "ms_per_step": td_ser * 1e3}}},
         "prefill_shapes": shapes,
         "next_rows": extras,
         "gpu_launches": 3 * K,   # per step: the prefill kernel, the decode kernel and its combine
