@@ -11,6 +11,10 @@
 // online softmax that "多头注意力机制" (blog.euler0525.cn), section "Flash
 // Attention", and the textbook's section "Эффективные реализации" describe).
 //
+// This kernel runs head size 64, and head size 128 beyond 1536 keys per
+// head; shorter head-128 sequences and head size 256 run on the 64-key-tile
+// kernel (prefill_k64_sm103a.cuh).
+//
 // The kernel is persistent: one CTA per SM walks a list of work items, each
 // 256 query rows of one (b, h): two 128-row sub-tiles that take turns on the
 // tensor core, so that the softmax of one overlaps the MMAs of the other.
