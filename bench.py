@@ -386,10 +386,14 @@ def _time_launches(fn, flush, stream, iters=20, warmup=3):
             "mean": statistics.mean(ts)}
 
 
-def _time_throughput(fns, stream, iters=20, warmup=3):
-    """Mean time (s) per launch of `iters` launches issued back to back on
-    `stream`, launch i running fns[i % len(fns)] (each on its own copy of the
-    inputs), bracketed by one pair of CUDA events."""
+def _time_throughput(fns, stream, iters=20, warmup=3, graph=True):
+    """Mean time (s) per launch of `iters` launches back to back on `stream`,
+    launch i running fns[i % len(fns)] (each on its own copy of the inputs),
+    bracketed by one pair of CUDA events.  With `graph`, the same launches
+    are captured in one CUDA graph and the graph is replayed between the
+    events, so that the host's cost per call (Python binding, argument
+    checks, launch calls: about 13-15 us) does not set the rate of launches
+    shorter than it; returns (graph time, eager time), else the eager time."""
     for i in range(warmup):
         fns[i % len(fns)]()
     torch.cuda.synchronize()
@@ -399,7 +403,22 @@ def _time_throughput(fns, stream, iters=20, warmup=3):
         fns[i % len(fns)]()
     e1.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / 1e3 / iters
+    eager = e0.elapsed_time(e1) / 1e3 / iters
+    if not graph:
+        return eager
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(iters):
+            fns[i % len(fns)]()
+    g.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    captured = e0.elapsed_time(e1) / 1e3 / iters
+    del g
+    return captured, eager
 
 
 def input_sets(set_bytes, l2_bytes, cap=16):
@@ -472,11 +491,14 @@ def _pipelined_e2e(dev, stream, host_in, dev_in, run, dev_out, host_out, steps):
     return t0.elapsed_time(t1) / 1e3 / steps
 
 
-def _row(work, unit, per_launch, lat, peak=None, **extra):
-    """One timed row: throughput from back-to-back launches, latency beside it."""
+def _row(work, unit, per_launch, lat, peak=None, eager=None, **extra):
+    """One timed row: throughput from back-to-back launches (replayed from a
+    CUDA graph; `eager`: the same launches issued from Python), latency beside it."""
     val = work / per_launch / (1e12 if unit == "TFLOP/s" else 1e9)
     r = {"value": val, "unit": unit, "ms_per_launch": per_launch * 1e3,
          "latency_isolated_ms": {k: v * 1e3 for k, v in lat.items()}}
+    if eager is not None:
+        r["ms_per_launch_eager"] = eager * 1e3
     if peak is not None:
         r["frac_bf16" if unit == "TFLOP/s" else "frac_hbm"] = val / peak
     r.update(extra)
@@ -507,9 +529,9 @@ def time_prefill_configs(chs, dev, flush, stream, peaks, l2):
         sets = _copies(input_sets(_nbytes(q, k, v, o), l2), q, k, v, o)
         fns = [lambda s=s: chs.attn_fwd(*s, causal=bool(w["causal"]), window=w["window"])
                for s in sets]
-        t = _time_throughput(fns, stream)
+        t, t_eager = _time_throughput(fns, stream)
         lat = _time_launches(fns[0], flush, stream)
-        out[name] = _row(prefill_flops(w), "TFLOP/s", t, lat, peaks["bf16_tflops"],
+        out[name] = _row(prefill_flops(w), "TFLOP/s", t, lat, peaks["bf16_tflops"], eager=t_eager,
                          input_copies=len(sets))
         del q, k, v, o, sets, fns
     if chs.attn_status() != chs.ATTN_OK:
@@ -526,9 +548,10 @@ def _decode_row(chs, name, dev, flush, stream, peaks, l2, ring):
     sets = _copies(input_sets(_nbytes(qd, kcd, vcd), l2), qd, kcd, vcd, sld, od)
     call = chs.attn_decode_ring if ring else chs.attn_decode
     fns = [lambda s=s: call(*s, window=w["window"]) for s in sets]
-    t = _time_throughput(fns, stream)
+    t, t_eager = _time_throughput(fns, stream)
     lat = _time_launches(fns[0], flush, stream)
-    return _row(by, "GB/s", t, lat, peaks["hbm_gbs"], workload=name, input_copies=len(sets),
+    return _row(by, "GB/s", t, lat, peaks["hbm_gbs"], eager=t_eager, workload=name,
+                input_copies=len(sets),
                 tokens_per_s=w["B"] / t, tflops=decode_flops(w, sl.numpy()) / t / 1e12)
 
 
@@ -547,9 +570,9 @@ def time_next_rows(chs, dev, flush, stream, peaks, l2):
     o = torch.empty_like(q)
     sets = _copies(input_sets(_nbytes(q, kc, vc, o), l2), q, kc, vc, o)
     fns = [lambda s=s: chs.attn_fwd_chunk(s[0], s[1], s[2], w["start"], o=s[3]) for s in sets]
-    t = _time_throughput(fns, stream)
+    t, t_eager = _time_throughput(fns, stream)
     lat = _time_launches(fns[0], flush, stream)
-    out["F1_chunked_prefill"] = _row(chunk_flops(w), "TFLOP/s", t, lat, bf16, workload=name,
+    out["F1_chunked_prefill"] = _row(chunk_flops(w), "TFLOP/s", t, lat, bf16, eager=t_eager, workload=name,
                                      input_copies=len(sets))
     del q, kc, vc, o, sets, fns
 
@@ -566,9 +589,9 @@ def time_next_rows(chs, dev, flush, stream, peaks, l2):
     o = torch.empty_like(q)
     sets = _copies(input_sets(_nbytes(q, k, v, o), l2), q, k, v, o)
     fns = [lambda s=s: chs.attn_fwd(*s) for s in sets]
-    t = _time_throughput(fns, stream)
+    t, t_eager = _time_throughput(fns, stream)
     lat = _time_launches(fns[0], flush, stream)
-    out["F3_prefill_d256"] = _row(prefill_flops(w), "TFLOP/s", t, lat, bf16, workload=name,
+    out["F3_prefill_d256"] = _row(prefill_flops(w), "TFLOP/s", t, lat, bf16, eager=t_eager, workload=name,
                                   input_copies=len(sets))
     del q, k, v, o, sets, fns
 
@@ -589,12 +612,12 @@ def _backward_row(chs, name, dev, flush, stream, bf16, l2):
     sets = _copies(input_sets(_nbytes(q, k, v, o, do, dq, dk, dv, lse), l2),
                    q, k, v, o, do, lse, dq, dk, dv)
     fns = [lambda s=s: chs.attn_bwd(*s) for s in sets]
-    t = _time_throughput(fns, stream)
+    t, t_eager = _time_throughput(fns, stream)
     lat = _time_launches(fns[0], flush, stream)
     fl = 2.5 * 4 * w["Dh"] * w["B"] * w["Hq"] * visible_pairs(w["S"], w["causal"], w["window"])
     executed = "16*Dh (S in three passes, dP in two)" if w["Dh"] == 256 else \
         "14*Dh (S and dP in both passes)"
-    row = _row(fl, "TFLOP/s", t, lat, bf16, workload=name, input_copies=len(sets),
+    row = _row(fl, "TFLOP/s", t, lat, bf16, eager=t_eager, workload=name, input_copies=len(sets),
                flops="2.5 x the forward's (10*Dh per visible pair per head); "
                      f"the kernels execute {executed}")
     del q, k, v, do, o, lse, dq, dk, dv, sets, fns
