@@ -497,13 +497,33 @@ __global__ void __launch_bounds__(DH) attn_decode_tc_combine(const DecodeTcParam
   const float* mp = p.m_part + (size_t)bh * p.nsplit;
   const float* lp = p.l_part + (size_t)bh * p.nsplit;
   const float* op = p.o_part + (size_t)bh * p.nsplit * DH;
-  float M = -INFINITY;
-  for (int s = s_first; s <= s_last; ++s) M = fmaxf(M, mp[s]);
-  float o = 0.f, l = 0.f;
-  for (int s = s_first; s <= s_last; ++s) {
-    const float f = ex2_approx(mp[s] - M);
-    o = fmaf(f, op[(size_t)s * DH + d], o);
-    l = fmaf(f, lp[s], l);
+  // splits in groups of 8, every load of a group issued before any is used
+  // (one round of L2 latency per group), merged with a running maximum in
+  // split order
+  constexpr int kG = 8;
+  float M = -INFINITY, o = 0.f, l = 0.f;
+  for (int s0 = s_first; s0 <= s_last; s0 += kG) {
+    float mv[kG], lv[kG], ov[kG];
+#pragma unroll
+    for (int e = 0; e < kG; ++e) {
+      const bool in = s0 + e <= s_last;
+      mv[e] = in ? __ldcg(mp + s0 + e) : -INFINITY;
+      lv[e] = in ? __ldcg(lp + s0 + e) : 0.f;
+      ov[e] = in ? __ldcg(op + (size_t)(s0 + e) * DH + d) : 0.f;
+    }
+    float Mg = M;
+#pragma unroll
+    for (int e = 0; e < kG; ++e) Mg = fmaxf(Mg, mv[e]);
+    const float c = (M == -INFINITY) ? 0.f : ex2_approx(M - Mg);
+    o *= c;
+    l *= c;
+#pragma unroll
+    for (int e = 0; e < kG; ++e) {
+      const float f = (mv[e] == -INFINITY) ? 0.f : ex2_approx(mv[e] - Mg);
+      o = fmaf(f, ov[e], o);
+      l = fmaf(f, lv[e], l);
+    }
+    M = Mg;
   }
   p.o[(size_t)bh * DH + d] = __float2bfloat16(o / l);
 }
