@@ -86,3 +86,19 @@ def test_workspace_growth_inside_a_capture_is_refused():
     chs.attn_decode(q, kc, vc, sl, o)
     torch.cuda.synchronize()
     assert chs.attn_status() == chs.ATTN_OK
+
+
+def test_binding_takes_the_current_stream():
+    """A call without an explicit stream runs on torch's current stream: the
+    default one, one set with torch.cuda.stream, and a graph's capture stream."""
+    from causal_head_self_gb300 import _binding
+    assert _binding._stream_handle(None) == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert _binding._stream_handle(None) == s.cuda_stream
+    g = torch.cuda.CUDAGraph()
+    x = torch.zeros(1, device="cuda")
+    with torch.cuda.graph(g):
+        assert _binding._stream_handle(None) == torch.cuda.current_stream().cuda_stream
+        x.add_(1)
+    assert _binding._stream_handle(s) == s.cuda_stream
