@@ -4,7 +4,7 @@
 //
 //   Dh = 256 (the Gemma head size).  The accumulator O of one 128-row
 //   sub-tile takes 256 of the 512 tensor-memory columns, so the two-sub-tile
-//   ping-pong of the Dh <= 128 kernel does not fit.  One CTA per SM: Q
+//   ping-pong (prefill_sm103a.cuh) does not fit.  One CTA per SM: Q
 //   (64 KiB), a two-stage K ring and a three-stage V ring of 32 KiB tiles
 //   (224 KiB; the third V stage lets a V tile load while the two P.V before
 //   it run); tensor memory S0 [0,64), S1 [64,128), Q [128,256), O [256,512).
@@ -29,10 +29,10 @@
 // columns of its S buffer and read from there by the P.V MMA.
 //
 // The kernel is persistent (CTAs walk 128-row items, heaviest first) with the
-// roles of the Dh <= 128 kernel: one thread issues every TMA load, one warp
-// issues every MMA, four warps run the softmax and the epilogue (thread t owns
-// row t).  Masks, the lazy maximum and the chunked-prefill offset follow that
-// kernel.  Every wait is bounded.
+// roles of the ping-pong kernel (prefill_sm103a.cuh): one thread issues every
+// TMA load, one warp issues every MMA, four warps run the softmax and the
+// epilogue (thread t owns row t).  Masks, the lazy maximum and the
+// chunked-prefill offset follow that kernel.  Every wait is bounded.
 #pragma once
 
 #include <cstdint>
@@ -45,7 +45,7 @@ namespace chs {
 
 struct PrefillK64Params {
   int B, Hq, Hkv;
-  int Sq, Skv, q_off;   // as in the Dh <= 128 kernel
+  int Sq, Skv, q_off;   // as in the ping-pong kernel
   int causal, window;
   float scale_log2;
   int num_qblocks;      // ceil(Sq / 128)
@@ -133,13 +133,13 @@ struct PrefillK64Tile {
 };
 
 // Item w: heaviest query blocks first (causal work grows with the block),
-// dealt to the CTAs in snake order (see the Dh <= 128 kernel).
+// dealt to the CTAs in snake order (see the ping-pong kernel).
 __device__ __forceinline__ int prefill_k64_item(int k, int c, int G) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
 // The k-th work item of this CTA (num_items or more: none left).  With at
-// most two items per CTA the lighter one goes first, as in the Dh <= 128
+// most two items per CTA the lighter one goes first, as in the ping-pong
 // kernel: its latency-bound chain then overlaps the start of the long item.
 __device__ __forceinline__ int prefill_k64_cta_item(int k, int num_items) {
   const int G = gridDim.x, c = blockIdx.x;
@@ -338,7 +338,7 @@ __device__ __forceinline__ void prefill_k64_issuer(PrefillK64Smem<DH>& sm, const
 
 // Softmax and epilogue (warps 0-3; thread t owns row t of the item, TMEM lane
 // t): the online softmax of "Online normalizer calculation for softmax" with
-// the lazy maximum of the Dh <= 128 kernel, 64 scores per tile.
+// the lazy maximum of the ping-pong kernel, 64 scores per tile.
 template <int DH>
 __device__ __forceinline__ void prefill_k64_softmax(PrefillK64Smem<DH>& sm, const PrefillK64Params& p,
                                                     const CUtensorMap* map_o, uint32_t tbase,
@@ -366,7 +366,7 @@ __device__ __forceinline__ void prefill_k64_softmax(PrefillK64Smem<DH>& sm, cons
 
       if (tile.needs_mask(p, j)) {
         // keys this row may not see become -inf in tensor memory (as in the
-        // Dh <= 128 kernel): visible keys [klo, khi] as column offsets
+        // ping-pong kernel): visible keys [klo, khi] as column offsets
         // [clo, chi] of this 64-key tile
         const int kv0 = 64 * j;
         int khi = p.Skv - 1;
