@@ -47,6 +47,30 @@ def test_prefill_with_q_and_o_of_2_31_elements():
     del q, k, v, o
 
 
+@pytest.mark.parametrize("Hq,Hkv,Dh", [(16384, 2048, 128), (8192, 1024, 256)])
+def test_short_prefill_with_q_and_o_of_2_31_elements(Hq, Hkv, Dh):
+    """The 64-key-tile kernel (head size 128 up to 1536 keys, and head size
+    256): 1024 positions per head, so many heads that q and o hold 2^31
+    elements; causal, sampled heads and rows (the last head's rows sit past
+    2^31 elements)."""
+    B, S = 1, 1024
+    d = torch.device("cuda")
+    q = inputs.device_normal_bf16((B, Hq, S, Dh), 111, d)
+    k = inputs.device_normal_bf16((B, Hkv, S, Dh), 112, d)
+    v = inputs.device_normal_bf16((B, Hkv, S, Dh), 113, d)
+    assert q.numel() == 2 ** 31
+    o = chs.attn_fwd(q, k, v)
+    assert chs.attn_status() == chs.ATTN_OK
+    rows = sample_rows(S, 8, seed=9, must=(0, 127, 128, S - 1))
+    for h in (0, Hq // 2 - 1, Hq - 1):
+        g = h // (Hq // Hkv)
+        ref = oracle.attention(q[:, h:h + 1].cpu(), k[:, g:g + 1].cpu(), v[:, g:g + 1].cpu(),
+                               causal=True, rows=rows)
+        got = o[0, h, torch.from_numpy(rows).to(d)].float().cpu().numpy()
+        assert_close(got, ref[0, 0], what=f"head {h}")
+    del q, k, v, o
+
+
 def _window_caches(B, Hkv, Tmax, Dh, lens, W, seed):
     """Caches of NaN except each sequence's last W positions, which hold
     i.i.d. N(0, 1) values; also those visible keys and values alone."""
